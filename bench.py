@@ -1,0 +1,529 @@
+#!/usr/bin/env python3
+"""Benchmark of the varlen attention hot path on GB300 (one process per GPU).
+
+A step is one pass of every hot-path operation over one synthetic batch
+(config 2: 32768 packed tokens, lognormal document lengths with median 1024
+and sigma 1.2 clipped to [64, 16384], 32 query / 4 key-value heads, d = 128,
+bf16 inputs, float32 accumulation):
+
+  1. nsp_attn_fwd    -- schedule + varlen causal attention forward (out, lse)
+  2. nsp_attn_bwd    -- dq, dk, dv from out, lse, dout
+  3. ring legs       -- the stream split into 8 shards of 4096 tokens; one
+                        nsp_attn_fwd partial per non-empty causal (q-shard,
+                        kv-shard) pair (float32 out), nsp_lse_merge per shard
+  4. nsp_seq2head_permute -- q seq->head (8 groups) and back (head->seq)
+
+``value`` = useful attention TFLOP/s of the whole step: (4 d fwd + 10 d bwd
++ 4 d ring partials) x Hq x allowed (causal, same-document) pairs, divided
+by the step time; masked work is never counted.  Per-leg times, TFLOP/s and
+GB/s and the roofline of the dominant kernel are reported beside it.
+
+Timing: W warm-up steps, then K steps, each preceded (outside its timed
+region) by an L2 flush (a 256 MiB write, larger than the 129 MB L2), each
+timed with CUDA events on the launching stream; barrier + synchronize on
+both sides; max over ranks.  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from variable_length_sequence_gb300.workloads import CONFIGS, make_workload, shard_bounds  # noqa: E402
+
+METRIC = "varlen attn fwd+bwd useful TFLOP/s & % bf16 peak; merge/permute GB/s % HBM"
+CONFIG_ID = 2
+RING_SHARDS = 8
+PERMUTE_GROUPS = 8
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a scalar over ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- peaks / clocks
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def allowed_pairs_blocks(cu: np.ndarray, bounds):
+    """Non-empty causal (q-shard, kv-shard) pairs and their allowed pair counts
+    (a host-side count from cu_seqlens; no attention arithmetic)."""
+    cu = np.asarray(cu, np.int64)
+    pairs = []
+    for qs, (qa, qb) in enumerate(bounds):
+        for ks, (ka, kb) in enumerate(bounds[:qs + 1]):
+            n = 0
+            for b in range(len(cu) - 1):
+                s, e = int(cu[b]), int(cu[b + 1])
+                lo_q, hi_q = max(s, qa), min(e, qb)
+                if hi_q <= lo_q:
+                    continue
+                # queries t in [lo_q, hi_q) see keys [max(s, ka), min(t + 1, kb))
+                ts = np.arange(lo_q, hi_q, dtype=np.int64)
+                cnt = np.clip(np.minimum(ts + 1, kb) - max(s, ka), 0, None)
+                n += int(cnt.sum())
+            if n > 0:
+                pairs.append((qs, ks, n))
+    return pairs
+
+
+class Problem:
+    """Device-resident inputs, outputs and workspaces of one step."""
+
+    def __init__(self, nsp, w, device):
+        self.nsp = nsp
+        self.w = w
+        cfg = w.cfg
+        self.T, self.Hq, self.Hkv, self.d = w.T, cfg.Hq, cfg.Hkv, cfg.d
+        self.scale = self.d ** -0.5
+        dev = device
+        self.q = w.q.to(dev)
+        self.k = w.k.to(dev)
+        self.v = w.v.to(dev)
+        self.dout = w.dout.to(dev)
+        self.cu = torch.from_numpy(w.cu_seqlens).to(dev)
+        T, Hq, Hkv, d = self.T, self.Hq, self.Hkv, self.d
+        bf = torch.bfloat16
+        self.out = torch.empty((T, Hq, d), dtype=bf, device=dev)
+        self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.ws_f = torch.empty(nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d),
+                                dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d),
+                                dtype=torch.uint8, device=dev)
+        # ring legs
+        self.bounds = shard_bounds(T, RING_SHARDS)
+        self.ring_pairs = allowed_pairs_blocks(w.cu_seqlens, self.bounds)
+        n = T // RING_SHARDS
+        self.part_o = {(qs, ks): torch.empty((n, Hq, d), dtype=torch.float32, device=dev)
+                       for qs, ks, _ in self.ring_pairs}
+        self.part_l = {(qs, ks): torch.empty((Hq, n), dtype=torch.float32, device=dev)
+                       for qs, ks, _ in self.ring_pairs}
+        self.ws_r = torch.empty(nsp.nsp_attn_fwd_workspace_size(n, n, Hq, Hkv, d),
+                                dtype=torch.uint8, device=dev)
+        self.merged_o = torch.empty((T, Hq, d), dtype=bf, device=dev)
+        self.merged_l = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+        # permutation
+        self.perm = torch.empty((PERMUTE_GROUPS, T, Hq // PERMUTE_GROUPS, d), dtype=bf,
+                                device=dev)
+        self.unperm = torch.empty_like(self.q)
+        # work accounting
+        self.pairs = nsp.nsp_attn_pairs(w.cu_seqlens, True)
+        self.fwd_flop = 4.0 * d * Hq * self.pairs
+        self.bwd_flop = 10.0 * d * Hq * self.pairs
+        self.ring_flop = 4.0 * d * Hq * sum(c for _, _, c in self.ring_pairs)
+        nb = lambda t: t.numel() * t.element_size()
+        self.merge_bytes = 0
+        for qs in range(RING_SHARDS):
+            parts = [(a, b) for a, b, _ in self.ring_pairs if a == qs]
+            self.merge_bytes += sum(nb(self.part_o[p]) + nb(self.part_l[p]) for p in parts)
+        self.merge_bytes += nb(self.merged_o) + nb(self.merged_l)
+        self.permute_bytes = 2 * (nb(self.q) + nb(self.perm))   # read + write, both ways
+
+    # individual legs -------------------------------------------------------------
+    def fwd(self, stream):
+        self.nsp.nsp_attn_fwd(self.q, self.k, self.v, self.cu, len(self.w.lengths), 0, self.T, 0,
+                              self.T, self.Hq, self.Hkv, self.d, self.scale, True, self.out,
+                              self.lse, self.ws_f, stream)
+
+    def bwd(self, stream):
+        self.nsp.nsp_attn_bwd(self.q, self.k, self.v, self.out, self.dout, self.lse, self.cu,
+                              len(self.w.lengths), self.T, self.Hq, self.Hkv, self.d,
+                              self.scale, True, self.dq, self.dk, self.dv, self.ws_b, stream)
+
+    def ring_partials(self, stream):
+        n = self.T // RING_SHARDS
+        for qs, ks, _ in self.ring_pairs:
+            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
+            self.nsp.nsp_attn_fwd(self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n],
+                                  self.cu, len(self.w.lengths), qa, n, ka, n, self.Hq, self.Hkv,
+                                  self.d, self.scale, True, self.part_o[(qs, ks)],
+                                  self.part_l[(qs, ks)], self.ws_r, stream)
+
+    def merge(self, stream):
+        n = self.T // RING_SHARDS
+        for qs in range(RING_SHARDS):
+            keys = [(a, b) for a, b, _ in self.ring_pairs if a == qs]
+            qa = self.bounds[qs][0]
+            self.nsp.nsp_lse_merge([self.part_o[p] for p in keys],
+                                   [self.part_l[p] for p in keys],
+                                   self.merged_o[qa:qa + n], self.merged_l_view(qs), stream)
+
+    def merged_l_view(self, qs):
+        # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
+        if not hasattr(self, "_ml"):
+            n = self.T // RING_SHARDS
+            self._ml = [torch.empty((self.Hq, n), dtype=torch.float32, device=self.q.device)
+                        for _ in range(RING_SHARDS)]
+        return self._ml[qs]
+
+    def permute(self, stream):
+        self.nsp.nsp_seq2head_permute(self.q, self.perm, self.T, self.Hq, self.d,
+                                      PERMUTE_GROUPS, False, stream)
+        self.nsp.nsp_seq2head_permute(self.perm, self.unperm, self.T, self.Hq, self.d,
+                                      PERMUTE_GROUPS, True, stream)
+
+    LEGS = ("fwd", "bwd", "ring_partials", "merge", "permute")
+
+    def step(self, stream, events=None):
+        for i, leg in enumerate(self.LEGS):
+            if events is not None:
+                events[i][0].record(stream)
+            getattr(self, leg)(stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    from variable_length_sequence_gb300 import build as nsp_build
+    from variable_length_sequence_gb300 import nsp
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    if rank == 0 or not os.path.exists(nsp.LIB_PATH):
+        nsp_build.build()
+    barrier(world)
+    nsp.load()
+
+    w = make_workload(CONFIG_ID)
+    prob = Problem(nsp, w, device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    nlegs = len(Problem.LEGS)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prob.step(stream)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    leg_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nlegs)] for _ in range(K)]
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    launches0 = nsp.nsp_kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                       # L2 flush, outside the timed region
+        step_ev[i][0].record(stream)
+        prob.step(stream, leg_ev[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    launches = nsp.nsp_kernel_launches() - launches0
+
+    step_ms = [s.elapsed_time(e) for s, e in step_ev]
+    leg_ms = np.array([[s.elapsed_time(e) for s, e in legs] for legs in leg_ev])  # [K, nlegs]
+    total_ms = reduce_max(sum(step_ms), world, device)
+    ms_per_step = total_ms / K
+    useful = prob.fwd_flop + prob.bwd_flop + prob.ring_flop
+    value = reduce_sum(useful * K, world, device) / (total_ms * 1e-3) / 1e12
+
+    peaks = measured_peaks()
+    legs = dict(zip(Problem.LEGS, leg_ms.mean(0).tolist()))
+    leg_stats = {
+        "fwd": {"ms": legs["fwd"], "tflops": prob.fwd_flop / legs["fwd"] / 1e9},
+        "bwd": {"ms": legs["bwd"], "tflops": prob.bwd_flop / legs["bwd"] / 1e9},
+        "ring_partials": {"ms": legs["ring_partials"],
+                          "tflops": prob.ring_flop / legs["ring_partials"] / 1e9,
+                          "pairs": len(prob.ring_pairs)},
+        "merge": {"ms": legs["merge"], "gbs": prob.merge_bytes / legs["merge"] / 1e6,
+                  "frac_hbm": prob.merge_bytes / legs["merge"] / 1e6 / peaks["hbm_gbs"]},
+        "permute": {"ms": legs["permute"], "gbs": prob.permute_bytes / legs["permute"] / 1e6,
+                    "frac_hbm": prob.permute_bytes / legs["permute"] / 1e6 / peaks["hbm_gbs"]},
+    }
+    for k in ("fwd", "bwd", "ring_partials"):
+        leg_stats[k]["frac_bf16"] = leg_stats[k]["tflops"] / peaks["bf16_tflops"]
+    dom = max(Problem.LEGS, key=lambda k: legs[k])
+    if dom in ("merge", "permute"):
+        ach = leg_stats[dom]["gbs"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None}
+    else:
+        ach = leg_stats[dom]["tflops"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None}
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    roof["note"] = "duration = the whole C-ABI call (its small schedule kernels included)"
+
+    e2e = run_e2e(args, prob, nsp, w, device, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; lengths, Q/K/V/dOut N(0,1) rounded to bf16)",
+            "config": {"workload": CONFIGS[CONFIG_ID].name, "tokens": prob.T,
+                       "docs": len(w.lengths), "heads_q": prob.Hq, "heads_kv": prob.Hkv,
+                       "head_dim": prob.d, "causal": True, "ring_shards": RING_SHARDS,
+                       "permute_groups": PERMUTE_GROUPS,
+                       "step": "fwd + bwd + 8-shard ring partials + lse merge + seq<->head permute",
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       "parallelism": f"replicas x{world}"},
+            "useful_flop_per_step": useful,
+            "legs": leg_stats,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "wall_s": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, prob, nsp, w, device, stream, world):
+    """Same step through the public API with host buffers: pinned inputs are
+    copied in and the step's results (out, lse, dq, dk, dv) read back inside
+    the timed region."""
+    host_in = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "dout")}
+    host_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
+    outs = {n: torch.empty(getattr(prob, n).shape, dtype=getattr(prob, n).dtype).pin_memory()
+            for n in ("out", "lse", "dq", "dk", "dv")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_cu.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    K = max(1, min(args.steps, 5))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        for n, t in host_in.items():
+            getattr(prob, n).copy_(t, non_blocking=True)
+        prob.cu.copy_(host_cu, non_blocking=True)
+        prob.step(stream)
+        for n, t in outs.items():
+            t.copy_(getattr(prob, n), non_blocking=True)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    total_ms = reduce_max(sum(s.elapsed_time(e) for s, e in evs), world, device)
+    useful = prob.fwd_flop + prob.bwd_flop + prob.ring_flop
+    val = reduce_sum(useful * K, world, device) / (total_ms * 1e-3) / 1e12
+    return {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": total_ms / K}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_sample_rows(cu, n, seed):
+    rng = np.random.default_rng(seed)
+    T = int(cu[-1])
+    return np.sort(rng.choice(T, size=min(n, T), replace=False))
+
+
+def cpu_oracle_rate(w, seconds: float, seed: int = 0):
+    """Time the fp64 oracle forward on growing random row samples of the
+    workload (all heads) until about `seconds` of CPU work; return
+    (useful TFLOP/s, rows, elapsed)."""
+    import oracle
+    q, k, v = (w.f64(n) for n in ("q", "k", "v"))
+    cu = np.asarray(w.cu_seqlens, np.int64)
+    d, Hq = w.cfg.d, w.cfg.Hq
+    n = 16
+    done_flop, done_s, done_rows = 0.0, 0.0, 0
+    while done_s < seconds:
+        rows = cpu_sample_rows(cu, n, seed + n)
+        doc = np.searchsorted(cu, rows, side="right") - 1
+        pairs = float((rows - cu[doc] + 1).sum())
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q, k, v, cu, d ** -0.5, True, rows)
+        dt = time.perf_counter() - t0
+        done_flop += 4.0 * d * Hq * pairs
+        done_s += dt
+        done_rows += len(rows)
+        n *= 2
+    return done_flop / done_s / 1e12, done_rows, done_s
+
+
+def cpu_baseline(w, seconds: float):
+    rate, rows, el = cpu_oracle_rate(w, seconds)
+    return {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle forward on {rows} random query rows of "
+                      f"{CONFIGS[CONFIG_ID].name} (all {w.cfg.Hq} heads), {el:.1f} s; "
+                      "useful FLOP = 4 d Hq x allowed pairs of those rows"}
+
+
+def run_reference(args, world, rank, local):
+    """Reference arm: the fp64 CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = make_workload(CONFIG_ID, with_dout=False)
+    K, W = args.steps, args.warmup
+    per_step = max(1.0, min(20.0, 150.0 / max(1, K + W)))
+    for i in range(W):
+        cpu_oracle_rate(w, per_step, seed=1000 + i)
+    rates, wall = [], 0.0
+    for i in range(K):
+        r, rows, el = cpu_oracle_rate(w, per_step, seed=i)
+        rates.append(r)
+        wall += el
+    value = statistics.mean(rates)
+    cpu = {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"each step: fp64 oracle forward on random query rows of "
+                     f"{CONFIGS[CONFIG_ID].name} (all heads) for ~{per_step:.0f} s"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": wall / K * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": CONFIGS[CONFIG_ID].name},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("bench: --warmup raised to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

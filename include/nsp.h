@@ -1,0 +1,214 @@
+/*
+ * nsp.h -- C ABI of the GB300 (sm_103a) varlen attention hot path.
+ *
+ * One GPU, caller-owned device memory, caller stream.  The library computes:
+ *
+ *   - document-masked ("varlen") causal self-attention over a packed token
+ *     stream, forward and backward, with grouped-query heads;
+ *   - the chunk-partial attention of ring-style sequence parallelism (a query
+ *     range against a key range) and the log-sum-exp merge of such partials;
+ *   - the Ulysses seq-sharded -> head-sharded layout permutation.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, innermost last):
+ *   q, out, dout, dq : [tokens, Hq,  d]      k, v, dk, dv : [tokens, Hkv, d]
+ *   lse              : [Hq, tokens] float32 (natural log of the scaled scores)
+ *   cu_seqlens       : int32 [ndoc + 1], device memory, cu[0] = 0,
+ *                      non-decreasing, cu[ndoc] = total tokens of the stream.
+ *                      Zero-length documents are allowed.
+ * Element types: NSP_BF16 inputs are computed with float32 accumulation;
+ *   NSP_F32 inputs with true float32 arithmetic (no TF32).
+ * Ownership: the caller allocates and frees every buffer, including the
+ *   workspace.  The library allocates no device or host memory, never
+ *   synchronises the stream (except nsp_status_query) and enqueues all work
+ *   on `stream`.  Calls on different streams with different workspaces may
+ *   run concurrently.
+ * Alignment: every device pointer must be 16-byte aligned.
+ * Errors: scalar, alignment and size errors are detected on the host and
+ *   returned before anything is enqueued.  Errors in device data (a bad
+ *   cu_seqlens) are detected by the first kernel, recorded in the status word
+ *   at the start of the workspace, and make every later kernel of the call a
+ *   no-op; nsp_status_query() returns that word.  A CUDA launch failure
+ *   returns NSP_ERR_CUDA.  Every device-side wait is bounded: if a bound
+ *   expires the kernel records NSP_ERR_TIMEOUT and returns (it never traps).
+ *
+ * Pages the operations come from (cited by title and section):
+ *   [NSP]  "NSP: Accelerating Variable-Length LLM Training via Nested Sequence
+ *          Parallelism" -- Sec. 2.2 Sequence Packing, Sec. 2.3 recomputation.
+ *   [BASP] "BASP: Communication-Efficient Batch-Aware Sequence Parallelism for
+ *          LLM Training" -- Sec. II-A Scaled Dot-Product Attention, Sec. II-C
+ *          DeepSpeed Ulysses.
+ *   [HSAP] "HSAP: A Hierachical Sequence-aware Parallelism for Hybrid-Context
+ *          Generative Models" -- Sec. 2.1 Sequence Packing (cu_len),
+ *          Sec. 2.2.1 InterSP (ring, online accumulation), Sec. 2.2.2 IntraSP
+ *          (all-to-all), Sec. 3.2 attention-block patterns, Limitations
+ *          (fusing copy and rescale).
+ */
+#ifndef NSP_H_
+#define NSP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* nsp_stream_t;
+
+typedef enum {
+  NSP_OK = 0,
+  NSP_ERR_INVALID = 1,      /* bad scalar argument or bad cu_seqlens contents */
+  NSP_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d not 64/128)  */
+  NSP_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
+  NSP_ERR_CUDA = 4,         /* a CUDA call or launch failed                   */
+  NSP_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired             */
+  NSP_ERR_ALIGN = 6         /* a pointer is not 16-byte aligned               */
+} nsp_status;
+
+typedef enum { NSP_F32 = 0, NSP_BF16 = 1 } nsp_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nsp_status_str(int32_t status);
+
+/* Library version string, e.g. "nsp 0.1 sm_103a". */
+const char* nsp_version(void);
+
+/* Number of kernels this library has launched in this process so far (all
+ * devices, all streams; a relaxed atomic counter).  Lets callers and
+ * benchmarks count the library's own launches. */
+int64_t nsp_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * Varlen attention forward  ([BASP] Sec. II-A; [HSAP] Sec. 2.1, 2.2.1).
+ *
+ * For every query row t in [q_start, q_start + q_len) of the packed stream,
+ * every query head h and g = h / (Hq / Hkv):
+ *   J(t)  = keys of t's document, restricted to positions <= t if causal,
+ *           intersected with [kv_start, kv_start + kv_len);
+ *   x_j   = scale * <q[t,h], k[j,g]>,   lse[h,t] = ln sum_{j in J(t)} exp(x_j),
+ *   out[t,h] = sum_{j in J(t)} exp(x_j - lse[h,t]) v[j,g].
+ * A row with empty J(t) gets out = 0 and lse = -inf.
+ *
+ * Whole-stream attention: q_start = kv_start = 0, q_len = kv_len = T.
+ * Ring chunk partial ([HSAP] Sec. 2.2.1 / 3.2): `q` points at the first row
+ * of the query shard ([q_len, Hq, d]) and `k`, `v` at the first row of the
+ * key shard ([kv_len, Hkv, d]); q_start / kv_start are the shards' global
+ * token offsets, used only to compare positions with cu_seqlens.  Request
+ * out_dtype = NSP_F32 for partials that will be merged.
+ *
+ * Arguments: q, k, v device, io_dtype; cu_seqlens device int32 [ndoc+1];
+ *   Hq % Hkv == 0; d in {64, 128}; causal 0/1; out device [q_len, Hq, d] of
+ *   out_dtype (NSP_F32 or io_dtype); lse device float32 [Hq, q_len] (may be
+ *   NULL when not needed); workspace device, at least
+ *   nsp_attn_fwd_workspace_size(...) bytes, contents need no initialisation.
+ * ---------------------------------------------------------------------- */
+size_t nsp_attn_fwd_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t Hkv,
+                                   int32_t d);
+
+int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                     int32_t ndoc, int64_t q_start, int64_t q_len, int64_t kv_start,
+                     int64_t kv_len, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                     int32_t causal, int32_t io_dtype, void* out, int32_t out_dtype,
+                     float* lse, void* workspace, size_t workspace_bytes, nsp_stream_t stream);
+
+/* Host-only argument check of nsp_attn_fwd (no CUDA call): returns the
+ * status nsp_attn_fwd would return before enqueuing anything. */
+int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                              int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                              int32_t Hkv, int32_t d, int32_t causal, int32_t io_dtype,
+                              const void* out, int32_t out_dtype, const void* workspace,
+                              size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * Varlen attention backward over the whole stream ([NSP] Sec. 2.3: the
+ * backward recomputes attention; only out and lse are kept).
+ *
+ * Gradients of L = sum(dout * out) for the forward above (q_start =
+ * kv_start = 0, q_len = kv_len = T):
+ *   delta_t = <dout[t,h], out[t,h]>,  p_tj = exp(x_tj - lse[h,t]),
+ *   dS_tj = p_tj (<dout[t,h], v[j,g]> - delta_t),
+ *   dq[t,h] = scale sum_j dS_tj k[j,g],
+ *   dk[j,g] = scale sum_{h in g} sum_t dS_tj q[t,h],
+ *   dv[j,g] = sum_{h in g} sum_t p_tj dout[t,h].
+ * out and lse must be the forward's results for the same inputs.
+ * dq, dk, dv are written (not accumulated) in io_dtype.  The workspace (at
+ * least nsp_attn_bwd_workspace_size bytes) holds the float32 dq accumulator
+ * and delta; its contents need no initialisation.  dq is summed with float
+ * atomics, so it may differ between runs in the last bits.
+ * ---------------------------------------------------------------------- */
+size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
+
+int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, const int32_t* cu_seqlens,
+                     int32_t ndoc, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                     int32_t causal, int32_t io_dtype, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, nsp_stream_t stream);
+
+int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const void* out,
+                              const void* dout, const float* lse, const int32_t* cu_seqlens,
+                              int32_t ndoc, int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                              int32_t causal, int32_t io_dtype, const void* dq,
+                              const void* dk, const void* dv, const void* workspace,
+                              size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * Log-sum-exp merge of n partials of the same T query rows over disjoint
+ * key sets ([HSAP] Sec. 2.2.1 online accumulation; Limitations "rescale"):
+ *   m = max_i lse_i;  m = -inf -> out = 0, lse = -inf;  otherwise
+ *   lse = m + ln sum_i exp(lse_i - m),  out = sum_i exp(lse_i - lse) out_i.
+ *
+ * outs, lses: HOST arrays of n DEVICE pointers (1 <= n <= 64); outs[i] is
+ *   float32 [T, H, d], lses[i] float32 [H, T].  out: device [T, H, d] of
+ *   out_dtype (NSP_F32 or NSP_BF16, round-to-nearest-even); lse: device
+ *   float32 [H, T] (may be NULL).  out and lse must not overlap any input.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_lse_merge(const float* const* outs, const float* const* lses, int32_t n,
+                      int64_t T, int32_t H, int32_t d, void* out, int32_t out_dtype,
+                      float* lse, nsp_stream_t stream);
+
+int32_t nsp_lse_merge_validate(const float* const* outs, const float* const* lses, int32_t n,
+                               int64_t T, int32_t H, int32_t d, const void* out,
+                               int32_t out_dtype, const float* lse);
+
+/* ------------------------------------------------------------------------
+ * Ulysses seq -> head permutation ([HSAP] Sec. 2.2.2: blocks in
+ * R^{n x H x d} per group become R^{N x h x d}, h = H / P; [BASP] Sec. II-C).
+ * With the P sequence shards stacked on this device as in = [T, H, d]:
+ *   inverse = 0:  out[g][t][j][:] = in[t][g*h + j][:]    out = [P, T, h, d]
+ *   inverse = 1:  out[t][g*h + j][:] = in[g][t][j][:]    (head -> seq)
+ * Elements are elem_bytes wide (1, 2, 4 or 8) and copied bit-exactly.
+ * H % P == 0; in and out must not overlap.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_seq2head_permute(const void* in, void* out, int64_t T, int32_t H, int32_t d,
+                             int32_t P, int32_t elem_bytes, int32_t inverse,
+                             nsp_stream_t stream);
+
+int32_t nsp_seq2head_permute_validate(const void* in, const void* out, int64_t T, int32_t H,
+                                      int32_t d, int32_t P, int32_t elem_bytes);
+
+/* ------------------------------------------------------------------------
+ * Status word of the last call that used `workspace`.  Synchronises `stream`
+ * first (the only synchronising call).  Returns NSP_OK, the recorded device
+ * error (NSP_ERR_INVALID for bad cu_seqlens, NSP_ERR_TIMEOUT), or
+ * NSP_ERR_CUDA if the synchronisation itself failed.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_status_query(const void* workspace, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Useful work of a whole-stream causal/bidirectional attention, from a HOST
+ * copy of cu_seqlens (NSP's cost model takes "attention FLOPs" of the routed
+ * inputs, [NSP] Sec. 4.1): pairs = allowed (query, key) pairs per query head.
+ * Writes *pairs; returns NSP_ERR_INVALID for a malformed cu_seqlens.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_attn_pairs(const int32_t* cu_seqlens_host, int32_t ndoc, int32_t causal,
+                       double* pairs);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSP_H_ */

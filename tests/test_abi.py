@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads without a GPU, exports every function
+include/nsp.h declares, and rejects bad arguments on the host before any
+CUDA call (only the *_validate entry points and host helpers run here)."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+from variable_length_sequence_gb300 import build as nsp_build
+from variable_length_sequence_gb300 import nsp
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nsp_build.build()
+    return nsp.load()
+
+
+def test_exports_every_header_function(lib):
+    names = nsp.header_functions()
+    assert "nsp_attn_fwd" in names and "nsp_seq2head_permute" in names
+    for n in names:
+        assert hasattr(lib, n), f"libnsp.so does not export {n}"
+    assert set(names) >= set(nsp._SIGNATURES), "binding names a function the header lacks"
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert nsp.status_str(st).startswith("NSP_")
+    assert nsp.status_str(99) == "NSP_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.nsp_version()
+
+
+A = 1 << 20          # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def fwd_args(**kw):
+    a = dict(q=A, k=A + 4096, v=A + 8192, cu=A + 12288, ndoc=3, q_start=0, q_len=300,
+             kv_start=0, kv_len=300, Hq=32, Hkv=4, d=128, causal=1, io=nsp.NSP_BF16,
+             out=A + 16384, out_dtype=nsp.NSP_BF16, ws=A + 32768,
+             ws_bytes=nsp.nsp_attn_fwd_workspace_size(300, 300, 32, 4, 128))
+    a.update(kw)
+    return a
+
+
+def call_fwd_validate(lib, a):
+    return lib.nsp_attn_fwd_validate(a["q"], a["k"], a["v"], a["cu"], a["ndoc"], a["q_start"],
+                                     a["q_len"], a["kv_start"], a["kv_len"], a["Hq"], a["Hkv"],
+                                     a["d"], a["causal"], a["io"], a["out"], a["out_dtype"],
+                                     a["ws"], a["ws_bytes"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, nsp.NSP_OK),
+    ({"Hq": 30}, nsp.NSP_ERR_INVALID),                 # Hq % Hkv != 0
+    ({"Hkv": 0}, nsp.NSP_ERR_INVALID),
+    ({"ndoc": 0}, nsp.NSP_ERR_INVALID),
+    ({"d": 96}, nsp.NSP_ERR_UNSUPPORTED),
+    ({"causal": 2}, nsp.NSP_ERR_INVALID),
+    ({"io": 7}, nsp.NSP_ERR_INVALID),
+    ({"out_dtype": nsp.NSP_F32}, nsp.NSP_OK),          # float32 partials
+    ({"io": nsp.NSP_F32, "out_dtype": nsp.NSP_BF16}, nsp.NSP_ERR_INVALID),
+    ({"q_len": -1}, nsp.NSP_ERR_INVALID),
+    ({"q": A + 8}, nsp.NSP_ERR_ALIGN),
+    ({"cu": A + 4}, nsp.NSP_ERR_ALIGN),
+    ({"q": 0}, nsp.NSP_ERR_INVALID),
+    ({"ws": 0}, nsp.NSP_ERR_WORKSPACE),
+    ({"ws_bytes": 100}, nsp.NSP_ERR_WORKSPACE),
+    ({"q_len": 0, "kv_len": 0, "ws_bytes": 4096}, nsp.NSP_OK),
+])
+def test_fwd_validation(lib, kw, expect):
+    assert call_fwd_validate(lib, fwd_args(**kw)) == expect
+
+
+def test_bwd_validation(lib):
+    ws = nsp.nsp_attn_bwd_workspace_size(1000, 32, 4, 128)
+    assert ws >= 1000 * 32 * 128 * 4             # holds the float32 dq accumulator
+    ptrs = [A + 4096 * i for i in range(10)]
+    ok = lib.nsp_attn_bwd_validate(*ptrs[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
+                                   *ptrs[7:10], A + (1 << 16), ws)
+    assert ok == nsp.NSP_OK
+    assert lib.nsp_attn_bwd_validate(*ptrs[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
+                                     *ptrs[7:10], A + (1 << 16), ws - 1) == nsp.NSP_ERR_WORKSPACE
+    bad = list(ptrs)
+    bad[5] = A + 4                                 # lse misaligned
+    assert lib.nsp_attn_bwd_validate(*bad[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
+                                     *bad[7:10], A + (1 << 16), ws) == nsp.NSP_ERR_ALIGN
+
+
+def test_merge_and_permute_validation(lib):
+    outs = (C.c_void_p * 2)(A, A + 4096)
+    lses = (C.c_void_p * 2)(A + 8192, A + 12288)
+    v = lib.nsp_lse_merge_validate
+    assert v(C.cast(outs, C.c_void_p), C.cast(lses, C.c_void_p), 2, 16, 4, 128, A + 65536,
+             nsp.NSP_BF16, A + 131072) == nsp.NSP_OK
+    assert v(C.cast(outs, C.c_void_p), C.cast(lses, C.c_void_p), 0, 16, 4, 128, A + 65536,
+             nsp.NSP_BF16, None) == nsp.NSP_ERR_INVALID
+    assert v(C.cast(outs, C.c_void_p), C.cast(lses, C.c_void_p), 65, 16, 4, 128, A + 65536,
+             nsp.NSP_BF16, None) == nsp.NSP_ERR_INVALID
+    p = lib.nsp_seq2head_permute_validate
+    assert p(A, A + (1 << 24), 1024, 32, 128, 8, 2) == nsp.NSP_OK
+    assert p(A, A + (1 << 24), 1024, 32, 128, 5, 2) == nsp.NSP_ERR_INVALID   # H % P
+    assert p(A, A + (1 << 24), 1024, 32, 128, 8, 3) == nsp.NSP_ERR_INVALID   # elem size
+    assert p(A, A + 1024, 1024, 32, 128, 8, 2) == nsp.NSP_ERR_INVALID        # overlap
+    assert p(A + 2, A + (1 << 24), 1024, 32, 128, 8, 2) == nsp.NSP_ERR_ALIGN
+
+
+def test_attn_pairs_counts_allowed_pairs(lib):
+    cu = np.array([0, 3, 3, 7, 8], dtype=np.int32)       # lengths 3, 0, 4, 1
+    brute_c = sum(1 for b in range(4) for t in range(cu[b], cu[b + 1])
+                  for j in range(cu[b], t + 1))
+    brute_n = sum(int(cu[b + 1] - cu[b]) ** 2 for b in range(4))
+    assert nsp.nsp_attn_pairs(cu, True) == brute_c == 6 + 10 + 1
+    assert nsp.nsp_attn_pairs(cu, False) == brute_n == 9 + 16 + 1
+    with pytest.raises(nsp.NspError):
+        nsp.nsp_attn_pairs(np.array([0, 5, 3], dtype=np.int32))

@@ -1,0 +1,257 @@
+// C ABI entry points: host-side validation, workspace carving and dispatch.
+// Nothing here allocates memory or synchronises (except nsp_status_query).
+#include <cstdio>
+#include <atomic>
+#include <cstring>
+
+#include "nsp_internal.cuh"
+
+namespace nsp {
+
+std::atomic<long long> g_kernel_launches{0};
+
+void count_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace nsp
+
+using namespace nsp;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool dtype_ok(int32_t t) { return t == NSP_F32 || t == NSP_BF16; }
+
+constexpr int64_t kMaxTokens = (int64_t)1 << 30;   // keeps tile counts in int32
+
+int32_t check_common(int32_t ndoc, int32_t Hq, int32_t Hkv, int32_t d, int32_t causal,
+                     int32_t io_dtype) {
+  if (ndoc < 1) return NSP_ERR_INVALID;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return NSP_ERR_INVALID;
+  if (causal != 0 && causal != 1) return NSP_ERR_INVALID;
+  if (!dtype_ok(io_dtype)) return NSP_ERR_INVALID;
+  if (d != 64 && d != 128) return NSP_ERR_UNSUPPORTED;
+  return NSP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nsp_status_str(int32_t status) {
+  switch (status) {
+    case NSP_OK: return "NSP_OK";
+    case NSP_ERR_INVALID: return "NSP_ERR_INVALID: invalid argument or cu_seqlens contents";
+    case NSP_ERR_UNSUPPORTED: return "NSP_ERR_UNSUPPORTED: valid but unsupported shape or type";
+    case NSP_ERR_WORKSPACE: return "NSP_ERR_WORKSPACE: workspace missing or too small";
+    case NSP_ERR_CUDA: return "NSP_ERR_CUDA: a CUDA call or kernel launch failed";
+    case NSP_ERR_TIMEOUT: return "NSP_ERR_TIMEOUT: a bounded device-side wait expired";
+    case NSP_ERR_ALIGN: return "NSP_ERR_ALIGN: a pointer is not 16-byte aligned";
+    default: return "NSP_ERR_UNKNOWN";
+  }
+}
+
+const char* nsp_version(void) { return "nsp 0.1 sm_103a"; }
+
+int64_t nsp_kernel_launches(void) { return (int64_t)g_kernel_launches.load(); }
+
+size_t nsp_attn_fwd_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t Hkv,
+                                   int32_t d) {
+  (void)Hq; (void)Hkv; (void)d;
+  if (q_len < 0 || kv_len < 0) return 0;
+  return fwd_ws_layout(q_len, kv_len).total;
+}
+
+int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                              int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                              int32_t Hkv, int32_t d, int32_t causal, int32_t io_dtype,
+                              const void* out, int32_t out_dtype, const void* workspace,
+                              size_t workspace_bytes) {
+  int32_t st = check_common(ndoc, Hq, Hkv, d, causal, io_dtype);
+  if (st != NSP_OK) return st;
+  if (q_start < 0 || q_len < 0 || kv_start < 0 || kv_len < 0) return NSP_ERR_INVALID;
+  if (q_start + q_len > kMaxTokens || kv_start + kv_len > kMaxTokens) return NSP_ERR_UNSUPPORTED;
+  if (out_dtype != NSP_F32 && out_dtype != io_dtype) return NSP_ERR_INVALID;
+  // Buffers of zero elements may be NULL (empty tensors have no storage).
+  if (!cu_seqlens || (q_len > 0 && (!q || !out)) || (kv_len > 0 && (!k || !v)))
+    return NSP_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(cu_seqlens))
+    return NSP_ERR_ALIGN;
+  if (!workspace || workspace_bytes < fwd_ws_layout(q_len, kv_len).total)
+    return NSP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NSP_ERR_ALIGN;
+  return NSP_OK;
+}
+
+int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                     int32_t ndoc, int64_t q_start, int64_t q_len, int64_t kv_start,
+                     int64_t kv_len, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                     int32_t causal, int32_t io_dtype, void* out, int32_t out_dtype,
+                     float* lse, void* workspace, size_t workspace_bytes,
+                     nsp_stream_t stream) {
+  int32_t st = nsp_attn_fwd_validate(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start,
+                                     kv_len, Hq, Hkv, d, causal, io_dtype, out, out_dtype,
+                                     workspace, workspace_bytes);
+  if (st != NSP_OK) return st;
+  if (lse && !aligned16(lse)) return NSP_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = out_dtype; p.out = out; p.lse = lse;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  if (launch_fwd_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (q_len == 0) return NSP_OK;
+  bool launched = false;
+  if (launch_attn_fwd_tc(p, L, ws, s, &launched) != cudaSuccess) return NSP_ERR_CUDA;
+  if (!launched && launch_attn_fwd_simt(p, s) != cudaSuccess) return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d) {
+  (void)Hkv;
+  if (T < 0 || Hq < 1 || d < 1) return 0;
+  return bwd_ws_layout(T, Hq, d).total;
+}
+
+int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const void* out,
+                              const void* dout, const float* lse, const int32_t* cu_seqlens,
+                              int32_t ndoc, int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                              int32_t causal, int32_t io_dtype, const void* dq,
+                              const void* dk, const void* dv, const void* workspace,
+                              size_t workspace_bytes) {
+  int32_t st = check_common(ndoc, Hq, Hkv, d, causal, io_dtype);
+  if (st != NSP_OK) return st;
+  if (T < 0) return NSP_ERR_INVALID;
+  if (T > kMaxTokens) return NSP_ERR_UNSUPPORTED;
+  if (!cu_seqlens) return NSP_ERR_INVALID;
+  if (T > 0 && (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv))
+    return NSP_ERR_INVALID;
+  const void* ptrs[] = {q, k, v, out, dout, lse, cu_seqlens, dq, dk, dv};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return NSP_ERR_ALIGN;
+  if (!workspace || workspace_bytes < bwd_ws_layout(T, Hq, d).total) return NSP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NSP_ERR_ALIGN;
+  return NSP_OK;
+}
+
+int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, const int32_t* cu_seqlens,
+                     int32_t ndoc, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                     int32_t causal, int32_t io_dtype, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = nsp_attn_bwd_validate(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d,
+                                     causal, io_dtype, dq, dk, dv, workspace, workspace_bytes);
+  if (st != NSP_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  const BwdWsLayout L = bwd_ws_layout(T, Hq, d);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = io_dtype; p.out = nullptr; p.lse = nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  if (launch_fwd_schedule(p, L.q, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (T == 0) return NSP_OK;
+  if (launch_bwd_key_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+int32_t nsp_lse_merge_validate(const float* const* outs, const float* const* lses, int32_t n,
+                               int64_t T, int32_t H, int32_t d, const void* out,
+                               int32_t out_dtype, const float* lse) {
+  if (n < 1 || n > 64 || T < 0 || H < 1 || d < 4 || d % 4 != 0) return NSP_ERR_INVALID;
+  if (!dtype_ok(out_dtype)) return NSP_ERR_INVALID;
+  if (!outs || !lses) return NSP_ERR_INVALID;
+  if (T == 0) return NSP_OK;
+  if (!out) return NSP_ERR_INVALID;
+  for (int i = 0; i < n; ++i) {
+    if (!outs[i] || !lses[i]) return NSP_ERR_INVALID;
+    if (!aligned16(outs[i]) || !aligned16(lses[i])) return NSP_ERR_ALIGN;
+  }
+  if (!aligned16(out) || (lse && !aligned16(lse))) return NSP_ERR_ALIGN;
+  return NSP_OK;
+}
+
+int32_t nsp_lse_merge(const float* const* outs, const float* const* lses, int32_t n,
+                      int64_t T, int32_t H, int32_t d, void* out, int32_t out_dtype,
+                      float* lse, nsp_stream_t stream) {
+  int32_t st = nsp_lse_merge_validate(outs, lses, n, T, H, d, out, out_dtype, lse);
+  if (st != NSP_OK) return st;
+  if (T == 0) return NSP_OK;
+  if (launch_lse_merge(outs, lses, n, T, H, d, out, out_dtype, lse,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+int32_t nsp_seq2head_permute_validate(const void* in, const void* out, int64_t T, int32_t H,
+                                      int32_t d, int32_t P, int32_t elem_bytes) {
+  if (T < 0 || H < 1 || d < 1 || P < 1 || H % P != 0) return NSP_ERR_INVALID;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return NSP_ERR_INVALID;
+  if (T == 0) return NSP_OK;
+  if (!in || !out) return NSP_ERR_INVALID;
+  if (!aligned16(in) || !aligned16(out)) return NSP_ERR_ALIGN;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t n = (uintptr_t)T * H * d * elem_bytes;
+  if (T > 0 && a < b + n && b < a + n) return NSP_ERR_INVALID;     // overlap
+  return NSP_OK;
+}
+
+int32_t nsp_seq2head_permute(const void* in, void* out, int64_t T, int32_t H, int32_t d,
+                             int32_t P, int32_t elem_bytes, int32_t inverse,
+                             nsp_stream_t stream) {
+  int32_t st = nsp_seq2head_permute_validate(in, out, T, H, d, P, elem_bytes);
+  if (st != NSP_OK) return st;
+  if (inverse != 0 && inverse != 1) return NSP_ERR_INVALID;
+  if (T == 0) return NSP_OK;
+  if (launch_permute(in, out, T, H, d, P, elem_bytes, inverse,
+                     reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+int32_t nsp_status_query(const void* workspace, nsp_stream_t stream) {
+  if (!workspace) return NSP_ERR_INVALID;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  int32_t st = 0;
+  if (cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return st;
+}
+
+int32_t nsp_attn_pairs(const int32_t* cu_seqlens_host, int32_t ndoc, int32_t causal,
+                       double* pairs) {
+  if (!cu_seqlens_host || !pairs || ndoc < 1 || cu_seqlens_host[0] != 0) return NSP_ERR_INVALID;
+  double acc = 0.0;
+  for (int i = 0; i < ndoc; ++i) {
+    const int64_t L = (int64_t)cu_seqlens_host[i + 1] - cu_seqlens_host[i];
+    if (L < 0) return NSP_ERR_INVALID;
+    acc += causal ? 0.5 * (double)L * (double)(L + 1) : (double)L * (double)L;
+  }
+  *pairs = acc;
+  return NSP_OK;
+}
+
+}  // extern "C"

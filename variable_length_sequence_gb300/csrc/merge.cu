@@ -1,0 +1,122 @@
+// Log-sum-exp merge of ring-attention partials (HSAP, Sec. 2.2.1: the
+// key/value blocks circulate and each rank accumulates its queries' partial
+// results online; HSAP's Limitations call this step the "rescale").
+//
+// For each (token t, head h), given n partials (out_i, lse_i) over disjoint
+// key sets:  m = max_i lse_i;  if m = -inf the row saw no key: out = 0 and
+// lse = -inf;  else lse = m + ln sum_i exp(lse_i - m) and
+// out = sum_i exp(lse_i - lse) out_i.
+//
+// HBM-bound: every partial row is read once (float4 per lane), the merged
+// row written once.  A warp walks 32 consecutive tokens of one head so the
+// lse reads ([H, T] layout) are warp-coalesced and reused from L1; the
+// row-wise weights are computed once per row per warp.
+#include "nsp_internal.cuh"
+
+namespace nsp {
+namespace {
+
+constexpr int kMaxPartials = 64;
+constexpr int kMergeThreads = 256;
+
+struct MergePtrs {
+  const float* out[kMaxPartials];
+  const float* lse[kMaxPartials];
+};
+
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p));
+  return r;
+}
+
+template <typename TO>
+__device__ __forceinline__ void st4(TO* p, float4 v);
+template <>
+__device__ __forceinline__ void st4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(MergePtrs ptrs, int n,
+                                                                  int64_t T, int H, int d,
+                                                                  TO* __restrict__ out,
+                                                                  float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kMergeThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kMergeThreads) >> 5;
+  const int64_t tgroups = (T + 31) / 32;
+  const int d4 = d / 4;
+  for (int64_t wi = warp; wi < tgroups * H; wi += nwarps) {
+    const int h = (int)(wi / tgroups);
+    const int64_t t0 = (wi % tgroups) * 32;
+    // lane l: merged lse of token t0 + l
+    const int64_t tl = t0 + lane;
+    float m = -INFINITY;
+    if (tl < T)
+      for (int i = 0; i < n; ++i) m = fmaxf(m, __ldg(ptrs.lse[i] + (int64_t)h * T + tl));
+    float L = -INFINITY;
+    if (m != -INFINITY) {
+      float s = 0.f;
+      for (int i = 0; i < n; ++i) s += expf(__ldg(ptrs.lse[i] + (int64_t)h * T + tl) - m);
+      L = m + logf(s);
+    }
+    if (tl < T && lse_out != nullptr) lse_out[(int64_t)h * T + tl] = L;
+    const int rows = (int)min((int64_t)32, T - t0);
+    for (int r = 0; r < rows; ++r) {
+      const float Lr = __shfl_sync(0xffffffffu, L, r);
+      const int64_t t = t0 + r;
+      const int64_t off = (t * H + h) * (int64_t)d;
+      for (int c = lane; c < d4; c += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Lr != -INFINITY) {
+          for (int i = 0; i < n; ++i) {
+            const float li = __ldg(ptrs.lse[i] + (int64_t)h * T + t);
+            const float w = expf(li - Lr);
+            const float4 o = ld_stream4(ptrs.out[i] + off + 4 * c);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+          }
+        }
+        st4<TO>(out + off + 4 * c, acc);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,
+                             int64_t T, int H, int d, void* out, int out_dtype, float* lse,
+                             cudaStream_t s) {
+  MergePtrs ptrs;
+  for (int i = 0; i < n; ++i) { ptrs.out[i] = outs[i]; ptrs.lse[i] = lses[i]; }
+  for (int i = n; i < kMaxPartials; ++i) { ptrs.out[i] = nullptr; ptrs.lse[i] = nullptr; }
+  const int64_t work = ((T + 31) / 32) * H;
+  int64_t blocks = ceil_div(work, (int64_t)(kMergeThreads / 32));
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (out_dtype == NSP_BF16)
+    lse_merge_kernel<__nv_bfloat16><<<(unsigned)blocks, kMergeThreads, 0, s>>>(
+        ptrs, n, T, H, d, reinterpret_cast<__nv_bfloat16*>(out), lse);
+  else
+    lse_merge_kernel<float><<<(unsigned)blocks, kMergeThreads, 0, s>>>(
+        ptrs, n, T, H, d, reinterpret_cast<float*>(out), lse);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace nsp

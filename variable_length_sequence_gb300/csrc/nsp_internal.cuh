@@ -1,0 +1,140 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "nsp.h"
+
+namespace nsp {
+
+// Fixed-size header at the start of every attention workspace.
+struct WsHeader {
+  int32_t status;       // nsp_status recorded by device code (0 = OK)
+  int32_t counter;      // dynamic work-fetch counter (reset by the prep kernel)
+  int32_t n_items;      // number of scheduled work items
+  int32_t max_cost;     // largest per-q-tile KV-tile count
+  int32_t counter2;     // second work counter (backward)
+  int32_t n_items2;
+  int32_t pad[58];      // header is 256 bytes
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header must stay 256 bytes");
+
+constexpr int kTileM = 128;        // query rows per tile (tcgen05 M)
+constexpr int kTileN = 128;        // keys per KV tile
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Forward workspace layout (all offsets from the workspace base).
+struct FwdWsLayout {
+  size_t tiles;        // int2 [n_qtiles]: first/last KV tile of each query tile
+  size_t order;        // int32 [n_qtiles]: query tiles, most KV tiles first
+  size_t hist;         // int32 [n_kvtiles + 2]: counting-sort buckets
+  size_t total;
+  int64_t n_qtiles, n_kvtiles;
+};
+
+inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
+  FwdWsLayout L;
+  L.n_qtiles = ceil_div(q_len, kTileM);
+  L.n_kvtiles = ceil_div(kv_len, kTileN);
+  size_t off = sizeof(WsHeader);
+  L.tiles = off;  off = align_up(off + sizeof(int2) * (size_t)L.n_qtiles, 256);
+  L.order = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_qtiles, 256);
+  L.hist = off;   off = align_up(off + sizeof(int32_t) * (size_t)(L.n_kvtiles + 2), 256);
+  L.total = off;
+  return L;
+}
+
+// Backward workspace: header, forward-style schedule for query tiles and a
+// schedule for key tiles, delta [Hq, T] f32, dq accumulator [T, Hq, d] f32.
+struct BwdWsLayout {
+  FwdWsLayout q;       // query-tile schedule (shares the header)
+  size_t ktiles;       // int2 [n_kvtiles]: first/last query tile that sees each key tile
+  size_t korder;       // int32 [n_kvtiles]
+  size_t khist;        // int32 [n_qtiles + 2]
+  size_t delta;        // float [Hq, T]
+  size_t dq_acc;       // float [T, Hq, d]
+  size_t total;
+};
+
+inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d) {
+  BwdWsLayout L;
+  L.q = fwd_ws_layout(T, T);
+  size_t off = L.q.total;
+  L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.q.n_kvtiles, 256);
+  L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.q.n_kvtiles, 256);
+  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.q.n_qtiles + 2), 256);
+  L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)T, 256);
+  L.dq_acc = off; off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
+  L.total = off;
+  return L;
+}
+
+// Problem description passed by value to kernels.
+struct AttnProblem {
+  const void* q; const void* k; const void* v;
+  const int32_t* cu; int32_t ndoc;
+  int64_t q_start, q_len, kv_start, kv_len;
+  int32_t Hq, Hkv, d;
+  float scale;
+  int32_t causal;
+  int32_t io_dtype, out_dtype;
+  void* out; float* lse;
+  WsHeader* hdr;
+};
+
+// ---- launchers implemented in the .cu files (return cudaError_t) ----
+cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
+                                cudaStream_t s);
+cudaError_t launch_bwd_key_schedule(const AttnProblem& p, const BwdWsLayout& L, char* ws,
+                                    cudaStream_t s);
+cudaError_t launch_attn_fwd_simt(const AttnProblem& p, cudaStream_t s);
+cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
+                               cudaStream_t s, bool* launched);
+cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const void* dout,
+                                 const float* lse, void* dq, void* dk, void* dv,
+                                 const BwdWsLayout& L, char* ws, cudaStream_t s);
+cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,
+                             int64_t T, int H, int d, void* out, int out_dtype, float* lse,
+                             cudaStream_t s);
+cudaError_t launch_permute(const void* in, void* out, int64_t T, int H, int d, int P,
+                           int elem_bytes, int inverse, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Adds n to the library-wide count of kernels launched (nsp_kernel_launches).
+void count_launches(int n);
+
+}  // namespace nsp
+
+// ---- device helpers ----
+#ifdef __CUDACC__
+namespace nsp {
+
+__device__ __forceinline__ float ld_in(const float* p) { return *p; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ void st_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Index of the document holding global token t: the last b with cu[b] <= t
+// (binary search over cu[0..ndoc]); zero-length documents are never returned.
+__device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int ndoc, int64_t t) {
+  int lo = 0, hi = ndoc;            // answer in [0, ndoc - 1]
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ bool status_bad(const WsHeader* hdr) {
+  return *((volatile const int32_t*)&hdr->status) != 0;
+}
+
+}  // namespace nsp
+#endif

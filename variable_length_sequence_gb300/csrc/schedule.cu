@@ -1,0 +1,176 @@
+// Varlen tile scheduler: from cu_seqlens (device) build, for every 128-row
+// query tile, the contiguous range of 128-key tiles it must visit, and the
+// order in which persistent CTAs should take the tiles (most KV tiles first,
+// longest-processing-time order).  Fully masked KV tiles are never listed.
+//
+// The block patterns come from HSAP ("Sequence-aware Parallelism", Sec. 3.2,
+// "Partition attention computation blocks"): for a causally masked packed
+// sequence, a (query block, key block) pair is either empty, causal
+// (diagonal), a full cross block, or a block cut by a document edge.  Here
+// the "empty" blocks are dropped at schedule time and the cut blocks are
+// masked per row inside the attention kernels.  Balancing by block count
+// mirrors SAP's regional load balancing (same section) on one GPU.
+//
+// Mode 0 (forward / backward dQ view): tile i covers query rows
+//   [q_start + 128 i, ...) and lists KV tiles j (keys [kv_start + 128 j, ...)).
+// Mode 1 (backward dK/dV view): tile j covers keys [128 j, ...) of the whole
+//   stream and lists the query tiles whose rows can see any of those keys.
+//
+// One block of 1024 threads; the first mode-0 launch of a call validates
+// cu_seqlens and resets the workspace status word.
+#include "nsp_internal.cuh"
+
+namespace nsp {
+namespace {
+
+constexpr int kSchedThreads = 1024;
+
+struct SchedArgs {
+  const int32_t* cu;
+  int32_t ndoc;
+  int64_t q_start, q_len, kv_start, kv_len;
+  int32_t causal;
+  int32_t mode;        // 0: query tiles list KV tiles; 1: key tiles list query tiles
+  int32_t validate;
+  int2* tiles;
+  int32_t* order;
+  int32_t* hist;       // n_buckets ints
+  int32_t n_tiles;     // tiles to schedule
+  int32_t n_buckets;   // max cost + 1 (cost = number of listed tiles)
+  WsHeader* hdr;
+  int32_t second;      // write counters into counter2 / n_items2
+};
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
+  __shared__ int s_bad;
+  __shared__ int s_max;
+  __shared__ int s_scan[kSchedThreads];
+  const int tid = threadIdx.x;
+  if (tid == 0) { s_bad = 0; s_max = 0; }
+  __syncthreads();
+
+  if (a.validate) {
+    if (tid == 0) {
+      if (a.ndoc < 1 || a.cu[0] != 0) s_bad = 1;
+      const int64_t total = a.cu[a.ndoc];
+      if (total < a.q_start + a.q_len || total < a.kv_start + a.kv_len) s_bad = 1;
+    }
+    for (int i = tid; i < a.ndoc; i += kSchedThreads)
+      if (a.cu[i] > a.cu[i + 1]) s_bad = 1;
+    __syncthreads();
+    if (s_bad) {
+      if (tid == 0) {
+        a.hdr->status = NSP_ERR_INVALID;
+        a.hdr->n_items = 0; a.hdr->counter = 0;
+        a.hdr->n_items2 = 0; a.hdr->counter2 = 0;
+        a.hdr->max_cost = 0;
+      }
+      return;
+    }
+    if (tid == 0) a.hdr->status = NSP_OK;
+  } else if (status_bad(a.hdr)) {
+    if (tid == 0) { a.hdr->n_items2 = 0; a.hdr->counter2 = 0; }
+    return;
+  }
+
+  for (int i = tid; i < a.n_buckets; i += kSchedThreads) a.hist[i] = 0;
+  __syncthreads();
+
+  const int64_t q_end = a.q_start + a.q_len, kv_end = a.kv_start + a.kv_len;
+  for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
+    int lo_t = 0, hi_t = -1;
+    if (a.mode == 0) {
+      const int64_t r0 = a.q_start + (int64_t)i * kTileM;
+      const int64_t r1 = min(r0 + kTileM, q_end) - 1;          // last row of the tile
+      const int b0 = doc_of(a.cu, a.ndoc, r0), b1 = doc_of(a.cu, a.ndoc, r1);
+      const int64_t lo = max((int64_t)a.cu[b0], a.kv_start);
+      const int64_t hi = min(a.causal ? r1 + 1 : (int64_t)a.cu[b1 + 1], kv_end);  // exclusive
+      if (hi > lo) {
+        lo_t = (int)((lo - a.kv_start) / kTileN);
+        hi_t = (int)((hi - 1 - a.kv_start) / kTileN);
+      }
+    } else {
+      const int64_t k0 = (int64_t)i * kTileN;
+      const int64_t k1 = min(k0 + kTileN, a.kv_len) - 1;
+      const int b0 = doc_of(a.cu, a.ndoc, k0), b1 = doc_of(a.cu, a.ndoc, k1);
+      const int64_t lo = a.causal ? k0 : (int64_t)a.cu[b0];
+      const int64_t hi = (int64_t)a.cu[b1 + 1];                // exclusive
+      lo_t = (int)(lo / kTileM);
+      hi_t = (int)((hi - 1) / kTileM);
+    }
+    a.tiles[i] = make_int2(lo_t, hi_t);
+    const int cost = hi_t - lo_t + 1;
+    atomicAdd(&a.hist[cost], 1);
+    atomicMax(&s_max, cost);
+  }
+  __syncthreads();
+
+  // Exclusive scan in descending cost order: start[c] = sum_{c' > c} hist[c'].
+  // Thread t owns a contiguous run of reversed bucket indices.
+  const int per = (a.n_buckets + kSchedThreads - 1) / kSchedThreads;
+  const int r_begin = tid * per, r_end = min(r_begin + per, a.n_buckets);
+  int local = 0;
+  for (int r = r_begin; r < r_end; ++r) local += a.hist[a.n_buckets - 1 - r];
+  s_scan[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < kSchedThreads; off <<= 1) {
+    const int add = tid >= off ? s_scan[tid - off] : 0;
+    __syncthreads();
+    s_scan[tid] += add;
+    __syncthreads();
+  }
+  int run = s_scan[tid] - local;          // exclusive prefix of this thread's run
+  for (int r = r_begin; r < r_end; ++r) {
+    const int c = a.n_buckets - 1 - r;
+    const int h = a.hist[c];
+    a.hist[c] = run;
+    run += h;
+  }
+  __syncthreads();
+
+  for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
+    const int2 t = a.tiles[i];
+    const int pos = atomicAdd(&a.hist[t.y - t.x + 1], 1);
+    a.order[pos] = i;
+  }
+  if (tid == 0) {
+    if (a.second) { a.hdr->counter2 = 0; a.hdr->n_items2 = a.n_tiles; }
+    else { a.hdr->counter = 0; a.hdr->n_items = a.n_tiles; a.hdr->max_cost = s_max; }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
+                                cudaStream_t s) {
+  SchedArgs a;
+  a.cu = p.cu; a.ndoc = p.ndoc;
+  a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
+  a.causal = p.causal; a.mode = 0; a.validate = 1;
+  a.tiles = reinterpret_cast<int2*>(ws + L.tiles);
+  a.order = reinterpret_cast<int32_t*>(ws + L.order);
+  a.hist = reinterpret_cast<int32_t*>(ws + L.hist);
+  a.n_tiles = (int32_t)L.n_qtiles;
+  a.n_buckets = (int32_t)L.n_kvtiles + 2;
+  a.hdr = p.hdr; a.second = 0;
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_key_schedule(const AttnProblem& p, const BwdWsLayout& L, char* ws,
+                                    cudaStream_t s) {
+  SchedArgs a;
+  a.cu = p.cu; a.ndoc = p.ndoc;
+  a.q_start = 0; a.q_len = p.q_len; a.kv_start = 0; a.kv_len = p.kv_len;
+  a.causal = p.causal; a.mode = 1; a.validate = 0;
+  a.tiles = reinterpret_cast<int2*>(ws + L.ktiles);
+  a.order = reinterpret_cast<int32_t*>(ws + L.korder);
+  a.hist = reinterpret_cast<int32_t*>(ws + L.khist);
+  a.n_tiles = (int32_t)L.q.n_kvtiles;
+  a.n_buckets = (int32_t)L.q.n_qtiles + 2;
+  a.hdr = p.hdr; a.second = 1;
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace nsp

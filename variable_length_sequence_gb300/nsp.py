@@ -1,0 +1,236 @@
+"""Thin Python binding of ``libnsp.so`` (C ABI declared in ``include/nsp.h``).
+
+Argument marshalling only: every function named like the C entry point takes
+torch tensors (or raw integers) and passes their data pointers, sizes and the
+current CUDA stream to the library.  All computation happens in the
+library's kernels; there is no Python or CPU fallback, and loading fails
+loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnsp.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "nsp.h")
+
+NSP_OK, NSP_ERR_INVALID, NSP_ERR_UNSUPPORTED, NSP_ERR_WORKSPACE = 0, 1, 2, 3
+NSP_ERR_CUDA, NSP_ERR_TIMEOUT, NSP_ERR_ALIGN = 4, 5, 6
+NSP_F32, NSP_BF16 = 0, 1
+
+_lib: Optional[C.CDLL] = None
+
+_vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
+
+_SIGNATURES = {
+    "nsp_status_str": (C.c_char_p, [_i32]),
+    "nsp_version": (C.c_char_p, []),
+    "nsp_kernel_launches": (_i64, []),
+    "nsp_attn_fwd_workspace_size": (_sz, [_i64, _i64, _i32, _i32, _i32]),
+    "nsp_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32,
+                            _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
+                                     _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
+    "nsp_attn_bwd_workspace_size": (_sz, [_i64, _i32, _i32, _i32]),
+    "nsp_attn_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                            _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "nsp_attn_bwd_validate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                     _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz]),
+    "nsp_lse_merge": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "nsp_lse_merge_validate": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp]),
+    "nsp_seq2head_permute": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "nsp_seq2head_permute_validate": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32]),
+    "nsp_status_query": (_i32, [_vp, _vp]),
+    "nsp_attn_pairs": (_i32, [_vp, _i32, _i32, C.POINTER(C.c_double)]),
+}
+
+
+class NspError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_str(status)} ({status})")
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/nsp.h."""
+    with open(HEADER) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nsp_[a-z0-9_]+)\s*\(", src)))
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Load libnsp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = C.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().nsp_status_str(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("libnsp takes contiguous tensors only")
+    return t.data_ptr() or None
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NSP_BF16
+    if t.dtype == torch.float32:
+        return NSP_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(fn: str, st: int) -> int:
+    if st != NSP_OK:
+        raise NspError(fn, st)
+    return st
+
+
+# ----------------------------------------------------------------------------- raw entry points
+
+def nsp_attn_fwd_workspace_size(q_len: int, kv_len: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load().nsp_attn_fwd_workspace_size(q_len, kv_len, Hq, Hkv, d))
+
+
+def nsp_attn_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(load().nsp_attn_bwd_workspace_size(T, Hq, Hkv, d))
+
+
+def nsp_attn_fwd(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq, Hkv, d,
+                 scale, causal, out, lse, workspace, stream=None) -> int:
+    st = load().nsp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(ndoc),
+                             int(q_start), int(q_len), int(kv_start), int(kv_len), int(Hq),
+                             int(Hkv), int(d), float(scale), int(bool(causal)), _dtype(q),
+                             _ptr(out), _dtype(out), _ptr(lse), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check("nsp_attn_fwd", st)
+
+
+def nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d, scale, causal,
+                 dq, dk, dv, workspace, stream=None) -> int:
+    st = load().nsp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                             _ptr(cu_seqlens), int(ndoc), int(T), int(Hq), int(Hkv), int(d),
+                             float(scale), int(bool(causal)), _dtype(q), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check("nsp_attn_bwd", st)
+
+
+def nsp_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], out, lse,
+                  stream=None) -> int:
+    n = len(outs)
+    T, H, d = outs[0].shape
+    po = (C.c_void_p * n)(*[_ptr(o) for o in outs])
+    pl = (C.c_void_p * n)(*[_ptr(l) for l in lses])
+    st = load().nsp_lse_merge(C.cast(po, C.c_void_p), C.cast(pl, C.c_void_p), n, T, H, d,
+                              _ptr(out), _dtype(out), _ptr(lse), _stream(stream))
+    return _check("nsp_lse_merge", st)
+
+
+def nsp_seq2head_permute(inp, out, T, H, d, P, inverse=False, stream=None) -> int:
+    st = load().nsp_seq2head_permute(_ptr(inp), _ptr(out), int(T), int(H), int(d), int(P),
+                                     inp.element_size(), int(bool(inverse)), _stream(stream))
+    return _check("nsp_seq2head_permute", st)
+
+
+def nsp_kernel_launches() -> int:
+    return int(load().nsp_kernel_launches())
+
+
+def nsp_status_query(workspace, stream=None) -> int:
+    return int(load().nsp_status_query(_ptr(workspace), _stream(stream)))
+
+
+def nsp_attn_pairs(cu_seqlens_host, causal=True) -> float:
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    out = C.c_double(0.0)
+    st = load().nsp_attn_pairs(cu.ctypes.data, len(cu) - 1, int(bool(causal)), C.byref(out))
+    _check("nsp_attn_pairs", st)
+    return out.value
+
+
+# ----------------------------------------------------------------------------- conveniences
+
+def attn_fwd(q, k, v, cu_seqlens, scale=None, causal=True, out_dtype=None, q_start=0,
+             kv_start=0, workspace=None, stream=None):
+    """Allocate out/lse/workspace with torch and call nsp_attn_fwd.
+
+    q [q_len, Hq, d], k/v [kv_len, Hkv, d] on the GPU, cu_seqlens int32 on the GPU.
+    """
+    q_len, Hq, d = q.shape
+    kv_len, Hkv, _ = k.shape
+    scale = d ** -0.5 if scale is None else scale
+    out = torch.empty((q_len, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((Hq, q_len), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_fwd_workspace_size(q_len, kv_len, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q.device)
+    nsp_attn_fwd(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, q_start, q_len, kv_start, kv_len,
+                 Hq, Hkv, d, scale, causal, out, lse, workspace, stream)
+    return out, lse
+
+
+def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, workspace=None,
+             stream=None):
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_bwd_workspace_size(T, Hq, Hkv, d), dtype=torch.uint8,
+                                device=q.device)
+    nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, d,
+                 scale, causal, dq, dk, dv, workspace, stream)
+    return dq, dk, dv
+
+
+def lse_merge(outs, lses, out_dtype=torch.float32, stream=None):
+    T, H, d = outs[0].shape
+    out = torch.empty((T, H, d), dtype=out_dtype, device=outs[0].device)
+    lse = torch.empty((H, T), dtype=torch.float32, device=outs[0].device)
+    nsp_lse_merge(outs, lses, out, lse, stream)
+    return out, lse
+
+
+def seq2head(x, P, stream=None):
+    T, H, d = x.shape
+    out = torch.empty((P, T, H // P, d), dtype=x.dtype, device=x.device)
+    nsp_seq2head_permute(x, out, T, H, d, P, False, stream)
+    return out
+
+
+def head2seq(y, stream=None):
+    P, T, h, d = y.shape
+    out = torch.empty((T, P * h, d), dtype=y.dtype, device=y.device)
+    nsp_seq2head_permute(y, out, T, P * h, d, P, True, stream)
+    return out
