@@ -1,14 +1,540 @@
-// tcgen05 forward path (not yet enabled: the dispatcher falls back to the
-// CUDA-core kernel).
-#include "nsp_internal.cuh"
+// Varlen attention forward on the 5th-generation tensor cores (tcgen05,
+// TMEM accumulators, TMA loads), bf16 inputs, float32 accumulation, d = 128.
+//
+// What it computes is the definition of the CUDA-core path (scaled
+// dot-product attention inside each packed document, BASP Sec. II-A, HSAP
+// Sec. 2.1 cu_len; optionally a ring partial block, HSAP Sec. 2.2.1), with
+// the blockwise online softmax (Milakov and Gimelshein, cited by HSAP
+// Sec. 2.2.1) so no score matrix is ever stored.
+//
+// Work decomposition.  The schedule kernel lists, per 128-row query tile
+// (aligned to the start of the query range), the contiguous range of
+// 128-key tiles its rows may see, and orders the query tiles by that count,
+// longest first.  A work item is (query tile, pair of query heads of one
+// KV group): both heads read the same K/V tiles, so every K/V tile loaded
+// into shared memory feeds two 128x128x128 QK^T and two PV products.  A
+// persistent grid of one CTA per SM takes items from an atomic counter.
+//
+// CTA roles (320 threads):
+//   warps 0-3  softmax for head h0 (TMEM lanes 0-127, one query row each)
+//   warps 4-7  softmax for head h0+1
+//   warp 8     TMA producer and work fetch
+//   warp 9     TMEM allocation and the single MMA-issuing thread
+// The softmax reads each S row from TMEM twice (row maximum first, then
+// exponentials 32 columns at a time), which keeps it within the 168
+// registers a thread gets when 10 warps share the four SM sub-partitions.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
+// P (bf16, two per 32-bit cell) is written over the first 64 columns of S
+// and read from TMEM by the PV product.  The tensor core alternates
+// between the two heads, so one head's softmax overlaps the other head's
+// MMAs.  The running output is rescaled only when a row's maximum grows
+// by more than 2^8 (the result is exact either way: numerator and
+// denominator share the same reference maximum).
+//
+// Masking: every query row sees one contiguous key interval [lo, hi) (its
+// document's start up to itself, clipped to the key range), so a KV tile
+// is either fully visible to a row or masked per column by two compares;
+// tiles no row can see are never scheduled.
+#include <cudaTypedefs.h>
+
+#include "tc_ptx.cuh"
 
 namespace nsp {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 128, HD = 128;
+constexpr int NSTAGE = 2;
+constexpr int kThreads = 320;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+constexpr uint32_t kColBlockBytes = 128 * 64 * 2;        // 128 rows x 64 bf16 (one swizzle span)
+constexpr uint32_t kTileBytes = 2 * kColBlockBytes;      // 128 x 128 bf16
+// TMEM columns of S (and P) and O for the two query heads of an item.
+__host__ __device__ constexpr uint32_t col_s(int t) { return t == 0 ? 0u : 128u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return t == 0 ? 256u : 384u; }
+constexpr float kRescaleThreshold = 8.0f;                 // log2 units
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Item {
+  int qtile;      // query tile index (-1: none)
+  int h0;         // first of the two query heads
+  int g;          // key/value head
+  int j_lo;       // first KV tile
+  int n_kv;       // number of KV tiles (0: no key visible; -1: stop)
+  int pad[3];
+};
+
+struct __align__(1024) Smem {
+  uint8_t q[2][kTileBytes];
+  uint8_t k[NSTAGE][kTileBytes];
+  uint8_t v[NSTAGE][kTileBytes];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[NSTAGE], k_empty[NSTAGE], v_full[NSTAGE], v_empty[NSTAGE];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t item_full[2], item_empty[2];
+  Item items[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;      // + alignment slack
+
+// S = Q K^T: 8 MMAs of K = 16 over the head dimension.  Both operands are
+// K-major with 128-byte swizzle; stepping K by 16 elements moves the start
+// address by 32 bytes inside a swizzle span, and the second 64-wide half of
+// the head dimension lives in the next 16 KB column block.  The start
+// address field holds address >> 4 and never carries (shared memory <
+// 256 KB), so descriptors are advanced by adding offset >> 4.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_saddr, uint32_t k_saddr) {
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+  const uint64_t qd = smem_desc_sw128(q_saddr, 16, 1024);
+  const uint64_t kd = smem_desc_sw128(k_saddr, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kColBlockBytes + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V: P (bf16) from TMEM, 8 columns per K = 16 keys; V is MN-major
+// (keys are K, the head dimension is N): 16 keys = two 8-row groups
+// (SBO = 1024 B), the two 64-wide halves of N are one column block apart
+// (LBO = 16 KB).
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_saddr,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, HD, true);
+  const uint64_t vd = smem_desc_sw128(v_saddr, kColBlockBytes, 1024);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Long bounded wait used only to drain in-flight TMA copies after an abort.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitTimeoutCycles) return;
+  }
+}
+
+// Store 32 consecutive output elements of one row (raw float32 bits in v).
+template <typename TO>
+__device__ __forceinline__ void store_row_chunk(TO* dst, const uint32_t (&v)[32], float scale);
+
+template <>
+__device__ __forceinline__ void store_row_chunk<__nv_bfloat16>(__nv_bfloat16* dst,
+                                                               const uint32_t (&v)[32],
+                                                               float scale) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+template <>
+__device__ __forceinline__ void store_row_chunk<float>(float* dst, const uint32_t (&v)[32],
+                                                       float scale) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d4[i] = make_float4(__uint_as_float(v[4 * i]) * scale, __uint_as_float(v[4 * i + 1]) * scale,
+                        __uint_as_float(v[4 * i + 2]) * scale,
+                        __uint_as_float(v[4 * i + 3]) * scale);
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const AttnProblem p,
+                       const int2* __restrict__ tiles, const int* __restrict__ order) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WsHeader* hdr = p.hdr;
+  if (status_bad(hdr)) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_full[t], 1);
+      mbar_init(&sm.item_full[t], 1);
+      mbar_init(&sm.item_empty[t], 1 + 8);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+  const int n_pairs = p.Hq >> 1;
+  const int G = p.Hq / p.Hkv;
+  const int n_items = hdr->n_items * n_pairs;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it_count = 0, q_count = 0, kv_count = 0;
+      bool ok = true;
+      while (ok) {
+        const int idx = atomicAdd(&hdr->counter, 1);
+        Item it;
+        it.qtile = -1; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
+        if (idx < n_items) {
+          const int qt = order[idx / n_pairs];
+          const int pair = idx - (idx / n_pairs) * n_pairs;
+          const int2 tr = tiles[qt];
+          it.qtile = qt;
+          it.h0 = 2 * pair;
+          it.g = (2 * pair) / G;
+          it.j_lo = tr.x;
+          it.n_kv = tr.y - tr.x + 1;
+        }
+        const uint32_t slot = it_count & 1;
+        if (it_count >= 2 &&
+            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
+          ok = false;
+          break;
+        }
+        sm.items[slot] = it;
+        mbar_arrive(&sm.item_full[slot]);
+        ++it_count;
+        if (it.n_kv <= 0) {
+          if (it.n_kv < 0) break;
+          continue;
+        }
+        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, abort_flag, hdr)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+        const int row0 = it.qtile * BM;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full, (it.h0 + t) * HD + cb * 64,
+                        row0);
+        ++q_count;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
+          const int key0 = (it.j_lo + jj) * BN;
+          if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.k[st] + cb * kColBlockBytes, &tm_k, &sm.k_full[st], it.g * HD + cb * 64,
+                        key0);
+          if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            // the K copy just issued is in flight: drain it before leaving
+            drain_wait(&sm.k_full[st], use & 1);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.v[st] + cb * kColBlockBytes, &tm_v, &sm.v_full[st], it.g * HD + cb * 64,
+                        key0);
+          ++kv_count;
+        }
+      }
+      if (!ok) {
+        // Abort: wait (bounded) for every copy still in flight to land.
+        if (q_count >= 1) drain_wait(&sm.q_full, (q_count - 1) & 1);
+        for (uint32_t s = 0; s < NSTAGE && s < kv_count; ++s) {
+          const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % NSTAGE);
+          drain_wait(&sm.k_full[last % NSTAGE], (last / NSTAGE) & 1);
+          drain_wait(&sm.v_full[last % NSTAGE], (last / NSTAGE) & 1);
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it_count = 0, q_count = 0, kv_count = 0;
+      uint32_t p_count[2] = {0, 0};
+      const uint32_t q_saddr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+      while (true) {
+        const uint32_t slot = it_count & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        const Item it = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++it_count;
+        if (it.n_kv < 0) break;
+        if (it.n_kv == 0) continue;
+        if (!mbar_wait(&sm.q_full, q_count & 1, abort_flag, hdr)) break;
+        ++q_count;
+        bool ok = true;
+        {
+          const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
+          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) break;
+          tc_fence_after();
+          const uint32_t ks = smem_u32(sm.k[st]);
+          issue_qk(tmem + col_s(0), q_saddr[0], ks);
+          mma_commit(&sm.s_full[0]);
+          issue_qk(tmem + col_s(1), q_saddr[1], ks);
+          mma_commit(&sm.s_full[1]);
+          mma_commit(&sm.k_empty[st]);
+          if (it.n_kv == 1) mma_commit(&sm.q_empty);
+        }
+        for (int jj = 0; jj < it.n_kv && ok; ++jj) {
+          const uint32_t st = (kv_count + jj) % NSTAGE, use = (kv_count + jj) / NSTAGE;
+          const bool has_next = jj + 1 < it.n_kv;
+          const uint32_t stn = (kv_count + jj + 1) % NSTAGE, usen = (kv_count + jj + 1) / NSTAGE;
+          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+          const uint32_t vs = smem_u32(sm.v[st]);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) continue;
+            if (!mbar_wait(&sm.p_full[t], p_count[t] & 1, abort_flag, hdr)) { ok = false; continue; }
+            ++p_count[t];
+            tc_fence_after();
+            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0);
+            if (t == 1) mma_commit(&sm.v_empty[st]);
+            if (!has_next) {
+              mma_commit(&sm.o_full[t]);
+              continue;
+            }
+            if (t == 0) {
+              if (!mbar_wait(&sm.k_full[stn], usen & 1, abort_flag, hdr)) { ok = false; continue; }
+              tc_fence_after();
+            }
+            issue_qk(tmem + col_s(t), q_saddr[t], smem_u32(sm.k[stn]));
+            mma_commit(&sm.s_full[t]);
+            if (t == 1) {
+              mma_commit(&sm.k_empty[stn]);
+              if (jj + 2 == it.n_kv) mma_commit(&sm.q_empty);
+            }
+          }
+        }
+        if (!ok) break;
+        kv_count += it.n_kv;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + col_s(t);
+    const uint32_t o_tm = tmem + lane_base + col_o(t);
+    const float sl2 = p.scale * kLog2e;
+    const int64_t kv_end = p.kv_start + p.kv_len;
+    uint32_t it_count = 0, s_count = 0, o_count = 0;
+    TO* const out = reinterpret_cast<TO*>(p.out);
+    while (true) {
+      const uint32_t slot = it_count & 1;
+      if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+      const Item it = sm.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+      ++it_count;
+      if (it.n_kv < 0) break;
+      const int h = it.h0 + t;
+      const int64_t row = (int64_t)it.qtile * BM + r;         // query-range relative
+      const bool valid = row < p.q_len;
+      int lo = 0, hi = 0;                                      // key-range relative [lo, hi)
+      if (valid) {
+        const int64_t tg = p.q_start + row;
+        const int b = doc_of(p.cu, p.ndoc, tg);
+        const int64_t glo = max((int64_t)__ldg(p.cu + b), p.kv_start);
+        const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1), kv_end);
+        lo = (int)(glo - p.kv_start);
+        hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
+      }
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int jj = 0; jj < it.n_kv; ++jj) {
+        if (!mbar_wait(&sm.s_full[t], s_count & 1, abort_flag, hdr)) { ok = false; break; }
+        ++s_count;
+        tc_fence_after();
+        const int key0 = (it.j_lo + jj) * BN;
+        const bool full = lo <= key0 && key0 + BN <= hi;
+        const int a = lo - key0, b = hi - key0;                // visible columns [a, b)
+        // pass 1: row maximum of the visible scores
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(s_tm + c * 32, sr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = c * 32 + i;
+            const float x = (full || (col >= a && col < b)) ? __uint_as_float(sr[i]) : -INFINITY;
+            mt = fmaxf(mt, x);
+          }
+        }
+        const float m_new = fmaxf(m, mt * sl2);
+        // Rescale the running output only when the maximum grew a lot.
+        const bool need = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
+        if (__any_sync(0xffffffffu, need)) {
+          const float corr = need ? ex2(m - m_new) : 1.f;
+          l *= corr;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(o_tm + c * 32, orow);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * corr);
+            tmem_st32(o_tm + c * 32, orow);
+          }
+          tmem_wait_st();
+        }
+        if (need || m == -INFINITY) m = m_new;
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        // pass 2: p = 2^(s * scale * log2 e - m), row sum, bf16 P over S
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(s_tm + c * 32, sr);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c * 32 + 2 * i;
+            const bool v0 = full || (col >= a && col < b);
+            const bool v1 = full || (col + 1 >= a && col + 1 < b);
+            const float p0 = v0 ? ex2(fmaf(__uint_as_float(sr[2 * i]), sl2, -mb)) : 0.f;
+            const float p1 = v1 ? ex2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -mb)) : 0.f;
+            l += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_tm + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[t]);
+      }
+      if (!ok) break;
+      // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      TO* dst = out + (row * p.Hq + h) * HD;
+      if (it.n_kv > 0) {
+        if (!mbar_wait(&sm.o_full[t], o_count & 1, abort_flag, hdr)) break;
+        ++o_count;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(o_tm + c * 32, orow);
+          tmem_wait_ld();
+          if (valid) store_row_chunk<TO>(dst + c * 32, orow, inv);
+        }
+      } else if (valid) {
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_row_chunk<TO>(dst + c * 32, z, 0.f);
+      }
+      if (valid && p.lse != nullptr)
+        p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows, cols] bf16 row-major, box = 64 columns x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TO>
+cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, cudaStream_t s,
+                         const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
+  auto kern = attn_fwd_tc_kernel<TO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = num_sms();
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p,
+                                          reinterpret_cast<const int2*>(ws + L.tiles),
+                                          reinterpret_cast<const int*>(ws + L.order));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                cudaStream_t s, bool* launched) {
-  (void)p; (void)L; (void)ws; (void)s;
   *launched = false;
-  return cudaSuccess;
+  if (p.io_dtype != NSP_BF16 || p.d != HD || (p.Hq / p.Hkv) % 2 != 0) return cudaSuccess;
+  if (p.q_len <= 0 || p.kv_len <= 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.q_len, (int64_t)p.Hq * HD) ||
+      !make_map(&mk, p.k, p.kv_len, (int64_t)p.Hkv * HD) ||
+      !make_map(&mv, p.v, p.kv_len, (int64_t)p.Hkv * HD))
+    return cudaSuccess;                       // no tensor-map support: CUDA-core path
+  *launched = true;
+  return p.out_dtype == NSP_F32 ? launch_typed<float>(p, L, ws, s, mq, mk, mv)
+                                : launch_typed<__nv_bfloat16>(p, L, ws, s, mq, mk, mv);
 }
 
 }  // namespace nsp
