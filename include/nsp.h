@@ -124,6 +124,38 @@ int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
                               size_t workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * nsp_attn_fwd without a workspace argument.  No page has a counterpart of
+ * this entry point: it exists for callers that cannot allocate device
+ * memory where they run attention (code inside a custom allocator or
+ * memory-pool callback, plugins whose host framework owns every device
+ * allocation, processes that must keep a fixed footprint after start-up).
+ *
+ * Same arguments, semantics, layouts and results as nsp_attn_fwd, minus
+ * workspace / workspace_bytes.  The scheduler scratch lives in a 1 MiB
+ * static __device__ array of the library instead, present on every GPU that
+ * loads the library until the process exits; nothing is allocated (no
+ * cudaMalloc, cudaFree or allocating library call).
+ *   Limit: nsp_attn_fwd_workspace_size(q_len, kv_len, ...) must not exceed
+ *   1 MiB (about 8.3 million query tokens when q_len = kv_len); larger
+ *   problems return NSP_ERR_WORKSPACE before anything is enqueued.
+ *   device_status: optional device int32; receives (stream-ordered) the
+ *   status word the kernels recorded (NSP_OK, NSP_ERR_INVALID for a bad
+ *   cu_seqlens, NSP_ERR_TIMEOUT); NULL to skip.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current) and caches it; make that
+ *   first call before any stream capture.
+ *   Every call shares the one array per device: calls whose kernels overlap
+ *   on the GPU (other streams, other host threads) race and must be
+ *   serialised by the caller.  Each call rewrites all the scratch it reads.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                             const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                             int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                             int32_t Hkv, int32_t d, float scale, int32_t causal,
+                             int32_t io_dtype, void* out, int32_t out_dtype, float* lse,
+                             int32_t* device_status, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Varlen attention backward over the whole stream ([NSP] Sec. 2.3: the
  * backward recomputes attention; only out and lse are kept).
  *

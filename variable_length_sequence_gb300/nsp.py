@@ -36,6 +36,8 @@ _SIGNATURES = {
                             _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
+    "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
+                                    _i32, _i32, _f32, _i32, _i32, _vp, _i32, _vp, _vp, _vp]),
     "nsp_attn_bwd_workspace_size": (_sz, [_i64, _i32, _i32, _i32]),
     "nsp_attn_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                             _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -133,6 +135,18 @@ def nsp_attn_fwd(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq
                              _ptr(out), _dtype(out), _ptr(lse), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream))
     return _check("nsp_attn_fwd", st)
+
+
+def nsp_attn_fwd_noalloc(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq, Hkv,
+                         d, scale, causal, out, lse, device_status=None, stream=None) -> int:
+    """nsp_attn_fwd for callers that cannot allocate: no workspace argument
+    (the library's static device scratch is used; see include/nsp.h)."""
+    st = load().nsp_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(ndoc),
+                                     int(q_start), int(q_len), int(kv_start), int(kv_len),
+                                     int(Hq), int(Hkv), int(d), float(scale), int(bool(causal)),
+                                     _dtype(q), _ptr(out), _dtype(out), _ptr(lse),
+                                     _ptr(device_status), _stream(stream))
+    return _check("nsp_attn_fwd_noalloc", st)
 
 
 def nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d, scale, causal,
