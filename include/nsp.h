@@ -100,7 +100,7 @@ int64_t nsp_kernel_launches(void);
  * out_dtype = NSP_F32 for partials that will be merged.
  *
  * Arguments: q, k, v device, io_dtype; cu_seqlens device int32 [ndoc+1];
- *   Hq % Hkv == 0; d in {64, 128}; causal 0/1; out device [q_len, Hq, d] of
+ *   Hq % Hkv == 0; d in {64, 128}; scale > 0 and finite; causal 0/1; out device [q_len, Hq, d] of
  *   out_dtype (NSP_F32 or io_dtype); lse device float32 [Hq, q_len] (may be
  *   NULL when not needed); workspace device, at least
  *   nsp_attn_fwd_workspace_size(...) bytes, contents need no initialisation.

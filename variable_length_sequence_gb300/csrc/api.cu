@@ -35,6 +35,9 @@ inline bool dtype_ok(int32_t t) { return t == NSP_F32 || t == NSP_BF16; }
 
 constexpr int64_t kMaxTokens = (int64_t)1 << 30;   // keeps tile counts in int32
 
+// The softmax scale must be a positive finite number (a temperature).
+inline bool scale_ok(float scale) { return scale > 0.f && scale <= 3.0e38f; }
+
 int32_t check_common(int32_t ndoc, int32_t Hq, int32_t Hkv, int32_t d, int32_t causal,
                      int32_t io_dtype) {
   if (ndoc < 1) return NSP_ERR_INVALID;
@@ -106,6 +109,7 @@ int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t*
                                      kv_len, Hq, Hkv, d, causal, io_dtype, out, out_dtype,
                                      workspace, workspace_bytes);
   if (st != NSP_OK) return st;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
   if (lse && !aligned16(lse)) return NSP_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
@@ -159,6 +163,7 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   int32_t st = nsp_attn_bwd_validate(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d,
                                      causal, io_dtype, dq, dk, dv, workspace, workspace_bytes);
   if (st != NSP_OK) return st;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
   const BwdWsLayout L = bwd_ws_layout(T, Hq, d);
@@ -171,7 +176,10 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   if (launch_fwd_schedule(p, L.q, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
   if (T == 0) return NSP_OK;
   if (launch_bwd_key_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
-  if (launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s) != cudaSuccess)
+  bool launched = false;
+  if (launch_attn_bwd_tc(p, out, dout, lse, dq, dk, dv, L, ws, s, &launched) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  if (!launched && launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s) != cudaSuccess)
     return NSP_ERR_CUDA;
   return NSP_OK;
 }

@@ -149,29 +149,6 @@ __global__ void __launch_bounds__(kFwdThreads) attn_fwd_simt_kernel(AttnProblem 
 }
 
 // ---------------------------------------------------------------- backward
-// delta[h, t] = <dout[t,h], out[t,h]> (one warp per row), computed from the
-// stored output as the forward returned it.
-template <typename TI, int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ out,
-                                                        const TI* __restrict__ dout,
-                                                        float* __restrict__ delta, int64_t T,
-                                                        int Hq, const WsHeader* hdr) {
-  if (status_bad(hdr)) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t rr = warp; rr < T * Hq; rr += nwarps) {
-    const int64_t t = rr / Hq;
-    const int h = (int)(rr % Hq);
-    float acc = 0.f;
-    for (int c = lane; c < D; c += 32)
-      acc = fmaf(ld_in(out + rr * D + c), ld_in(dout + rr * D + c), acc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) delta[(int64_t)h * T + t] = acc;
-  }
-}
-
 // Key-stationary dK/dV: a block owns 32 keys of one KV head, loops over the
 // query heads of the group and over every query tile whose rows can see its
 // keys, recomputing p from lse; dQ partial sums go to a float32 accumulator
@@ -299,16 +276,6 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
   }
 }
 
-template <typename TO>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         TO* __restrict__ dq, int64_t n,
-                                                         const WsHeader* hdr) {
-  if (status_bad(hdr)) return;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-    st_out(dq + i, acc[i]);
-}
-
 template <typename TI, typename TO, int D>
 cudaError_t fwd_dispatch(const AttnProblem& p, cudaStream_t s) {
   dim3 grid((unsigned)ceil_div(p.q_len, kFwdBM), (unsigned)p.Hq);
@@ -325,10 +292,8 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
   if (e != cudaSuccess) return e;
-  const int nsm = num_sms();
-  bwd_delta_kernel<TI, D><<<nsm * 8, 256, 0, s>>>(reinterpret_cast<const TI*>(out),
-                                                  reinterpret_cast<const TI*>(dout), delta, T,
-                                                  p.Hq, p.hdr); count_launches(1);
+  e = launch_bwd_delta(out, dout, delta, T, p.Hq, D, p.io_dtype, p.hdr, s);
+  if (e != cudaSuccess) return e;
   const size_t smem = sizeof(BwdSmem<D>);
   e = cudaFuncSetAttribute(attn_bwd_dkdv_simt_kernel<TI, D>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -337,9 +302,9 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   attn_bwd_dkdv_simt_kernel<TI, D><<<grid, kBwdThreads, smem, s>>>(
       p, reinterpret_cast<const TI*>(dout), lse, delta, dq_acc, reinterpret_cast<TI*>(dk),
       reinterpret_cast<TI*>(dv)); count_launches(1);
-  dq_convert_kernel<TI><<<nsm * 8, 256, 0, s>>>(dq_acc, reinterpret_cast<TI*>(dq),
-                                               T * p.Hq * D, p.hdr); count_launches(1);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_dq_convert(dq_acc, dq, T * p.Hq * D, p.io_dtype, p.hdr, s);
 }
 
 }  // namespace

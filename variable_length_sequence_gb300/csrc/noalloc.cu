@@ -72,6 +72,7 @@ extern "C" int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void
                                      reinterpret_cast<const void*>(uintptr_t(256)),
                                      kNoAllocScratchBytes);
   if (st != NSP_OK) return st;
+  if (!(scale > 0.f && scale <= 3.0e38f)) return NSP_ERR_INVALID;
   if ((lse && (reinterpret_cast<uintptr_t>(lse) & 15u)) ||
       (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)))
     return NSP_ERR_ALIGN;

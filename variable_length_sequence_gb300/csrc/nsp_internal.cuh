@@ -97,6 +97,13 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
 cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const void* dout,
                                  const float* lse, void* dq, void* dk, void* dv,
                                  const BwdWsLayout& L, char* ws, cudaStream_t s);
+cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv,
+                               const BwdWsLayout& L, char* ws, cudaStream_t s, bool* launched);
+cudaError_t launch_bwd_delta(const void* out, const void* dout, float* delta, int64_t T, int Hq,
+                             int d, int io_dtype, WsHeader* hdr, cudaStream_t s);
+cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n, int io_dtype,
+                              WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,
                              int64_t T, int H, int d, void* out, int out_dtype, float* lse,
                              cudaStream_t s);
