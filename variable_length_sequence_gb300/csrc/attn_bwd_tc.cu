@@ -64,8 +64,8 @@ struct __align__(1024) Smem {
   uint8_t q[2][kTileBytes];
   uint8_t dout[2][kTileBytes];
   uint8_t ds[kTileBytes];
-  float lse2[BQ];
-  float delta[BQ];
+  float lse2[2][BQ];           // lse * log2(e) of the stage's query rows
+  float delta[2][BQ];
   uint64_t kv_full, kv_empty;
   uint64_t qdo_full[2], qdo_empty[2];
   uint64_t s_full, ds_full, dq_full, dq_empty, dkv_full, dkv_empty;
@@ -75,8 +75,13 @@ struct __align__(1024) Smem {
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-static_assert(kSmemBytes <= 232448, "backward tile set exceeds 227 KB of shared memory");
+// Dynamic shared memory: the tile set plus whatever alignment slack still
+// fits under the 227 KB limit; the kernel checks at run time that the
+// 1024-byte-aligned tile set fits (the base is 1024-aligned in practice).
+constexpr size_t kSmemLimit = 232448;
+static_assert(sizeof(Smem) <= kSmemLimit, "backward tile set exceeds 227 KB of shared memory");
+constexpr size_t kSmemBytes =
+    sizeof(Smem) + 1024 <= kSmemLimit ? sizeof(Smem) + 1024 : kSmemLimit;
 
 // D (+)= A B^T with both operands K-major, 128-byte swizzle (as the forward QK^T).
 __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
@@ -120,8 +125,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 struct BwdArgs {
   AttnProblem p;
-  const float* lse;       // [Hq, T]
-  const float* delta;     // [Hq, T]
+  const float* lse2;      // [Hq, Tp] lse * log2(e), padded rows
+  const float* delta;     // [Hq, Tp]
+  int64_t Tp;
   float* dq_acc;          // [T, Hq, d] float32, zeroed
   __nv_bfloat16* dk;      // [T, Hkv, d]
   __nv_bfloat16* dv;
@@ -134,13 +140,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = p.hdr;
   if (status_bad(hdr)) return;
+  {
+    uint32_t dyn_bytes;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+    const uint32_t base = smem_u32(smem_raw);
+    if (((base + 1023u) & ~1023u) - base + sizeof(Smem) > dyn_bytes) {
+      if (threadIdx.x == 0) atomicExch(&hdr->status, (int)NSP_ERR_UNSUPPORTED);
+      return;
+    }
+  }
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kTileBytes);
+          mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kTileBytes + 2 * BQ * sizeof(float));
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
             tma_load_2d(sm.q[st] + cb * kColBlockBytes, &tm_q, &sm.qdo_full[st], h * HD + cb * 64,
@@ -237,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm.dout[st] + cb * kColBlockBytes, &tm_do, &sm.qdo_full[st],
                         h * HD + cb * 64, i * BQ);
           }
+          const int64_t row = (int64_t)h * a.Tp + (int64_t)i * BQ;
+          bulk_load(sm.lse2[st], a.lse2 + row, BQ * sizeof(float), &sm.qdo_full[st]);
+          bulk_load(sm.delta[st], a.delta + row, BQ * sizeof(float), &sm.qdo_full[st]);
           ++qc;
         }
       }
@@ -339,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;                 // 0: query columns / head dims 0-63; 1: 64-127
     const int wq = warp & 3;
     const int r = wq * 32 + lane;             // TMEM lane: key row (S^T, dV, dK) or query row (dQ)
-    const int tid_wg = r;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale * kLog2e;
     const uint32_t ds_row = smem_u32(sm.ds) + wg * kColBlockBytes + r * 128;
@@ -364,17 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < it.steps && ok; ++n) {
         const int h = it.g * G + n / it.n_q;
         const int64_t q0 = (int64_t)(it.i_lo + n % it.n_q) * BQ;
-        // stage lse * log2 e and delta of this step's query columns (my half)
-        named_bar_sync(1 + wg, 128);
-        {
-          const int c = tid_wg & 63;
-          const int64_t q = q0 + wg * 64 + c;
-          if (tid_wg < 64)
-            sm.lse2[wg * 64 + c] = q < T ? __ldg(a.lse + (int64_t)h * T + q) * kLog2e : 0.f;
-          else
-            sm.delta[wg * 64 + c] = q < T ? __ldg(a.delta + (int64_t)h * T + q) : 0.f;
-        }
-        named_bar_sync(1 + wg, 128);
+        const uint32_t st = qc & 1;
+        // the stage's lse2 / delta rows arrive with its Q and dOut tiles
+        if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        const float* lse2s = sm.lse2[st];
+        const float* deltas = sm.delta[st];
         if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -385,22 +396,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + kColDP + col0, dp);
           tmem_wait_ld();
           const int64_t qg0 = q0 + col0;
-          const bool full = qlo <= qg0 && qg0 + 32 <= qhi;
+          // visible query columns of this key, clipped to the chunk: [loc, hic)
+          const int loc = (int)min(max(qlo - qg0, (int64_t)0), (int64_t)32);
+          const int hic = (int)min(max(qhi - qg0, (int64_t)0), (int64_t)32);
+          const uint32_t span = (uint32_t)(hic - loc);
+          const bool full_w = __all_sync(0xffffffffu, qlo <= qg0 && qg0 + 32 <= qhi);
           uint32_t pk[16], dk[16];
+          if (full_w) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pv[2], dsv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cc = col0 + 2 * e + u;
-              const int64_t qg = qg0 + 2 * e + u;
-              const bool vis = full || (qg >= qlo && qg < qhi);
-              const float pr = vis ? ex2(fmaf(__uint_as_float(s[2 * e + u]), sl2, -sm.lse2[cc])) : 0.f;
-              pv[u] = pr;
-              dsv[u] = pr * (__uint_as_float(dp[2 * e + u]) - sm.delta[cc]);
+            for (int e = 0; e < 16; ++e) {
+              const int cc = col0 + 2 * e;
+              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]));
+              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2s[cc + 1]));
+              pk[e] = pack_bf16x2(p0, p1);
+              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - deltas[cc]),
+                                  p1 * (__uint_as_float(dp[2 * e + 1]) - deltas[cc + 1]));
             }
-            pk[e] = pack_bf16x2(pv[0], pv[1]);
-            dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int cc = col0 + 2 * e;
+              const bool v0 = (uint32_t)(2 * e - loc) < span;
+              const bool v1 = (uint32_t)(2 * e + 1 - loc) < span;
+              const float x0 = fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]);
+              const float x1 = fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2s[cc + 1]);
+              const float p0 = ex2(v0 ? x0 : -INFINITY);
+              const float p1 = ex2(v1 ? x1 : -INFINITY);
+              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - deltas[cc] : 0.f;
+              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - deltas[cc + 1] : 0.f;
+              pk[e] = pack_bf16x2(p0, p1);
+              dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
+            }
           }
           tmem_st16(tmem + lane_base + kColS + wg * 64 + c * 16, pk);
 #pragma unroll
@@ -510,18 +536,20 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
     return cudaSuccess;
   *launched = true;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
+  float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
   float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * HD, s);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_delta(out, dout, delta, T, p.Hq, HD, p.io_dtype, p.hdr, s);
+  e = launch_bwd_delta(out, dout, lse, delta, lse2, T, L.Tp, p.Hq, HD, p.io_dtype, p.hdr, s);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   BwdArgs a;
   a.p = p;
-  a.lse = lse;
+  a.lse2 = lse2;
   a.delta = delta;
+  a.Tp = L.Tp;
   a.dq_acc = dq_acc;
   a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
   a.dv = reinterpret_cast<__nv_bfloat16*>(dv);

@@ -383,20 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_count;
         tc_fence_after();
         const int key0 = (it.j_lo + jj) * BN;
-        const bool full = lo <= key0 && key0 + BN <= hi;
-        const int a = lo - key0, b = hi - key0;                // visible columns [a, b)
-        // pass 1: row maximum of the visible scores
+        // visible columns are [a, b): one unsigned compare per column; a
+        // warp whose rows all see the whole tile skips the mask entirely
+        const int a = lo - key0;
+        const uint32_t span = (uint32_t)(hi - lo);
+        const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + BN <= hi);
+        // pass 1: row maximum of the visible scores (two TMEM loads per wait)
         float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(s_tm + c * 32, sr);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t sa[32], sb[32];
+          tmem_ld32(s_tm + (2 * c2) * 32, sa);
+          tmem_ld32(s_tm + (2 * c2 + 1) * 32, sb);
           tmem_wait_ld();
+          if (full_w) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = c * 32 + i;
-            const float x = (full || (col >= a && col < b)) ? __uint_as_float(sr[i]) : -INFINITY;
-            mt = fmaxf(mt, x);
+            for (int i = 0; i < 32; ++i)
+              mt = fmaxf(mt, fmaxf(__uint_as_float(sa[i]), __uint_as_float(sb[i])));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int ca = 2 * c2 * 32 + i, cb = ca + 32;
+              const float xa = (uint32_t)(ca - a) < span ? __uint_as_float(sa[i]) : -INFINITY;
+              const float xb = (uint32_t)(cb - a) < span ? __uint_as_float(sb[i]) : -INFINITY;
+              mt = fmaxf(mt, fmaxf(xa, xb));
+            }
           }
         }
         const float m_new = fmaxf(m, mt * sl2);
@@ -420,22 +431,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mb = (m == -INFINITY) ? 0.f : m;
         // pass 2: p = 2^(s * scale * log2 e - m), row sum, bf16 P over S
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(s_tm + c * 32, sr);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t sr[2][32];
+          tmem_ld32(s_tm + (2 * c2) * 32, sr[0]);
+          tmem_ld32(s_tm + (2 * c2 + 1) * 32, sr[1]);
           tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c * 32 + 2 * i;
-            const bool v0 = full || (col >= a && col < b);
-            const bool v1 = full || (col + 1 >= a && col + 1 < b);
-            const float p0 = v0 ? ex2(fmaf(__uint_as_float(sr[2 * i]), sl2, -mb)) : 0.f;
-            const float p1 = v1 ? ex2(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, -mb)) : 0.f;
-            l += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = 2 * c2 + h2;
+            uint32_t pk[16];
+            float ls = 0.f;
+            if (full_w) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[h2][2 * i]), sl2, -mb));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[h2][2 * i + 1]), sl2, -mb));
+                ls += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int col = c * 32 + 2 * i;
+                const float x0 = fmaf(__uint_as_float(sr[h2][2 * i]), sl2, -mb);
+                const float x1 = fmaf(__uint_as_float(sr[h2][2 * i + 1]), sl2, -mb);
+                const float p0 = ex2((uint32_t)(col - a) < span ? x0 : -INFINITY);
+                const float p1 = ex2((uint32_t)(col + 1 - a) < span ? x1 : -INFINITY);
+                ls += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+            }
+            l += ls;
+            tmem_st16(s_tm + c * 16, pk);
           }
-          tmem_st16(s_tm + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();

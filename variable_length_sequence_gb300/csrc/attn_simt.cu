@@ -170,8 +170,8 @@ struct BwdSmem {
 template <typename TI, int D>
 __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
     AttnProblem p, const TI* __restrict__ dout, const float* __restrict__ lse,
-    const float* __restrict__ delta, float* __restrict__ dq_acc, TI* __restrict__ dk,
-    TI* __restrict__ dv) {
+    const float* __restrict__ delta, int64_t delta_stride, float* __restrict__ dq_acc,
+    TI* __restrict__ dk, TI* __restrict__ dv) {
   constexpr int DQ = D / 4;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
           sm.lo[tid] = p.cu[b];
           sm.hi[tid] = p.causal ? t + 1 : (int64_t)p.cu[b + 1];
           sm.lse[tid] = lse[(int64_t)h * T + t];
-          sm.delta[tid] = delta[(int64_t)h * T + t];
+          sm.delta[tid] = delta[(int64_t)h * delta_stride + t];
         } else {
           sm.lo[tid] = 0; sm.hi[tid] = 0; sm.lse[tid] = 0.f; sm.delta[tid] = 0.f;
         }
@@ -292,7 +292,8 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_delta(out, dout, delta, T, p.Hq, D, p.io_dtype, p.hdr, s);
+  e = launch_bwd_delta(out, dout, lse, delta, reinterpret_cast<float*>(ws + L.lse2), T, L.Tp,
+                       p.Hq, D, p.io_dtype, p.hdr, s);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(BwdSmem<D>);
   e = cudaFuncSetAttribute(attn_bwd_dkdv_simt_kernel<TI, D>,
@@ -300,7 +301,7 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)ceil_div(T, kBwdBK), (unsigned)p.Hkv);
   attn_bwd_dkdv_simt_kernel<TI, D><<<grid, kBwdThreads, smem, s>>>(
-      p, reinterpret_cast<const TI*>(dout), lse, delta, dq_acc, reinterpret_cast<TI*>(dk),
+      p, reinterpret_cast<const TI*>(dout), lse, delta, L.Tp, dq_acc, reinterpret_cast<TI*>(dk),
       reinterpret_cast<TI*>(dv)); count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -49,15 +49,18 @@ inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
 }
 
 // Backward workspace: header, forward-style schedule for query tiles and a
-// schedule for key tiles, delta [Hq, T] f32, dq accumulator [T, Hq, d] f32.
+// schedule for key tiles, delta and lse * log2(e) [Hq, Tp] f32 (rows padded
+// to Tp = whole 128-row tiles, padding zeroed), dq accumulator [T, Hq, d] f32.
 struct BwdWsLayout {
   FwdWsLayout q;       // query-tile schedule (shares the header)
   size_t ktiles;       // int2 [n_kvtiles]: first/last query tile that sees each key tile
   size_t korder;       // int32 [n_kvtiles]
   size_t khist;        // int32 [n_qtiles + 2]
-  size_t delta;        // float [Hq, T]
+  size_t delta;        // float [Hq, Tp]
+  size_t lse2;         // float [Hq, Tp]
   size_t dq_acc;       // float [T, Hq, d]
   size_t total;
+  int64_t Tp;
 };
 
 inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d) {
@@ -67,7 +70,9 @@ inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d) {
   L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.q.n_kvtiles, 256);
   L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.q.n_kvtiles, 256);
   L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.q.n_qtiles + 2), 256);
-  L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)T, 256);
+  L.Tp = L.q.n_qtiles * kTileM;
+  L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
+  L.lse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off; off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
   L.total = off;
   return L;
@@ -100,8 +105,9 @@ cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const vo
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
                                const BwdWsLayout& L, char* ws, cudaStream_t s, bool* launched);
-cudaError_t launch_bwd_delta(const void* out, const void* dout, float* delta, int64_t T, int Hq,
-                             int d, int io_dtype, WsHeader* hdr, cudaStream_t s);
+cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
+                             float* lse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
+                             WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n, int io_dtype,
                               WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,
