@@ -205,7 +205,7 @@ class Problem:
         self.dv = torch.empty_like(self.v)
         self.ws_f = torch.empty(nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d),
                                 dtype=torch.uint8, device=dev)
-        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d),
+        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, nsp.NSP_BF16),
                                 dtype=torch.uint8, device=dev)
         # ring legs
         self.bounds = shard_bounds(T, RING_SHARDS)

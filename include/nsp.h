@@ -168,11 +168,15 @@ int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  *   dv[j,g] = sum_{h in g} sum_t p_tj dout[t,h].
  * out and lse must be the forward's results for the same inputs.
  * dq, dk, dv are written (not accumulated) in io_dtype.  The workspace (at
- * least nsp_attn_bwd_workspace_size bytes) holds the float32 dq accumulator
- * and delta; its contents need no initialisation.  dq is summed with float
- * atomics, so it may differ between runs in the last bits.
+ * least nsp_attn_bwd_workspace_size bytes for the same T, heads, d and
+ * io_dtype) holds the tile schedules, delta and lse * log2(e); its contents
+ * need no initialisation.  bf16 with d = 128 and an even Hq / Hkv runs on the
+ * tensor cores (dq, dk, dv each written once, deterministic); other shapes run
+ * on CUDA cores, whose dq is summed with float atomics in a float32
+ * accumulator that the workspace then also holds (last bits may vary).
  * ---------------------------------------------------------------------- */
-size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d);
+size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                                   int32_t io_dtype);
 
 int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, const int32_t* cu_seqlens,

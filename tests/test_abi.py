@@ -73,8 +73,10 @@ def test_fwd_validation(lib, kw, expect):
 
 
 def test_bwd_validation(lib):
-    ws = nsp.nsp_attn_bwd_workspace_size(1000, 32, 4, 128)
-    assert ws >= 1000 * 32 * 128 * 4             # holds the float32 dq accumulator
+    ws = nsp.nsp_attn_bwd_workspace_size(1000, 32, 4, 128, nsp.NSP_BF16)
+    # only the CUDA-core path (here: float32 inputs) needs a float32 dq accumulator
+    ws32 = nsp.nsp_attn_bwd_workspace_size(1000, 32, 4, 128, nsp.NSP_F32)
+    assert ws32 >= ws + 1000 * 32 * 128 * 4
     ptrs = [A + 4096 * i for i in range(10)]
     ok = lib.nsp_attn_bwd_validate(*ptrs[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
                                    *ptrs[7:10], A + (1 << 16), ws)

@@ -31,8 +31,8 @@ def test_bad_cu_seqlens_reported(nsp, bad):
     # a valid call on the same workspace resets the status
     nsp.attn_fwd(q, k, v, torch.from_numpy(w.cu_seqlens).cuda(), workspace=ws)
     assert nsp.nsp_status_query(ws) == nsp_mod.NSP_OK
-    wsb = torch.empty(nsp.nsp_attn_bwd_workspace_size(200, 4, 2, 128), dtype=torch.uint8,
-                      device="cuda")
+    wsb = torch.empty(nsp.nsp_attn_bwd_workspace_size(200, 4, 2, 128, nsp_mod.NSP_BF16),
+                      dtype=torch.uint8, device="cuda")
     nsp.attn_bwd(q, k, v, out, do, lse, cu_d, workspace=wsb)
     assert nsp.nsp_status_query(wsb) == nsp_mod.NSP_ERR_INVALID
 

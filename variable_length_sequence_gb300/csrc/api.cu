@@ -128,10 +128,10 @@ int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t*
   return NSP_OK;
 }
 
-size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d) {
-  (void)Hkv;
-  if (T < 0 || Hq < 1 || d < 1) return 0;
-  return bwd_ws_layout(T, Hq, d).total;
+size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
+                                   int32_t io_dtype) {
+  if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;
+  return bwd_ws_layout(T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total;
 }
 
 int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const void* out,
@@ -150,7 +150,9 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
   const void* ptrs[] = {q, k, v, out, dout, lse, cu_seqlens, dq, dk, dv};
   for (const void* x : ptrs)
     if (!aligned16(x)) return NSP_ERR_ALIGN;
-  if (!workspace || workspace_bytes < bwd_ws_layout(T, Hq, d).total) return NSP_ERR_WORKSPACE;
+  if (!workspace ||
+      workspace_bytes < bwd_ws_layout(T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total)
+    return NSP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NSP_ERR_ALIGN;
   return NSP_OK;
 }
@@ -166,22 +168,19 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   if (!scale_ok(scale)) return NSP_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
-  const BwdWsLayout L = bwd_ws_layout(T, Hq, d);
+  const bool tc = bwd_tc_eligible(io_dtype, d, Hq, Hkv);
+  const BwdWsLayout L = bwd_ws_layout(T, Hq, d, !tc);
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
   p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
   p.io_dtype = io_dtype; p.out_dtype = io_dtype; p.out = nullptr; p.lse = nullptr;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
-  if (launch_fwd_schedule(p, L.q, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (launch_bwd_schedules(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
   if (T == 0) return NSP_OK;
-  if (launch_bwd_key_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
-  bool launched = false;
-  if (launch_attn_bwd_tc(p, out, dout, lse, dq, dk, dv, L, ws, s, &launched) != cudaSuccess)
-    return NSP_ERR_CUDA;
-  if (!launched && launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s) != cudaSuccess)
-    return NSP_ERR_CUDA;
-  return NSP_OK;
+  const cudaError_t e = tc ? launch_attn_bwd_tc(p, out, dout, lse, dq, dk, dv, L, ws, s)
+                           : launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s);
+  return e == cudaSuccess ? NSP_OK : NSP_ERR_CUDA;
 }
 
 int32_t nsp_lse_merge_validate(const float* const* outs, const float* const* lses, int32_t n,

@@ -1,37 +1,40 @@
 // Varlen attention backward on the tcgen05 tensor cores, bf16 inputs,
-// float32 accumulation, d = 128.
+// float32 accumulation, d = 128: two persistent kernels, no atomics.
 //
 // Gradients of L = sum(dOut * out) for document-masked attention (BASP
 // Sec. II-A, HSAP Sec. 2.1), recomputing the probabilities from the saved
 // lse instead of storing them (the recomputation NSP Sec. 2.3 discusses):
 //   P = exp(scale Q K^T - lse),  dP = dOut V^T,  dS = P (dP - delta),
 //   dV = P^T dOut,  dK = scale dS^T Q,  dQ = scale dS K,
-// delta = rowsum(dOut * out) (computed by bwd_delta_kernel beforehand).
+// with delta = rowsum(dOut * out) and lse * log2(e) prepared by
+// bwd_delta_kernel in padded [Hq, Tp] rows.
 //
-// Work item: one 128-key tile of one KV head.  It walks every (query head
-// of the group, 128-row query tile that can see the keys) pair; the key
-// tile's dK and dV accumulate in TMEM over the whole walk, so they are
-// written once, without atomics.  dQ of each step is added to a float32
-// accumulator with vector reductions (red.global.add.v4.f32).
+// dK/dV kernel (key-stationary).  Work item: one 128-key tile of one KV
+// head.  It walks every 64-row query sub-tile that can see the keys, for
+// the query heads of the group taken two at a time; the two heads are two
+// chains that ping-pong on the tensor core (one chain's softmax overlaps
+// the other chain's MMAs) and accumulate into the same dV and dK in TMEM:
+//   S^T  = K Q^T      (M = 128 keys, N = 64 queries)   TMEM [128X, 128X+64)
+//   dP^T = V dOut^T                                     TMEM [128X+64, 128X+128)
+//   P^T and dS^T (bf16) are written back over S^T and dP^T by the softmax
+//   dV  += P^T dOut   (A = P^T from TMEM, B = dOut MN-major)   TMEM [256, 384)
+//   dK  += dS^T Q     (A = dS^T from TMEM, B = Q MN-major)     TMEM [384, 512)
+// dK and dV are written once per item, in bf16.
 //
-// Per step (keys are the M dimension of the transposed products):
-//   S^T  = K Q^T          TMEM R0 [0,128)     (A = K, B = Q, both K-major smem)
-//   dP^T = V dOut^T       TMEM R1 [128,256)   (A = V, B = dOut, K-major)
-//   softmax warps: P^T = 2^(S^T scale log2e - lse log2e), dS^T = P^T (dP^T - delta),
-//     P^T (bf16) written over S^T in TMEM, dS^T (bf16) to shared memory in a
-//     128-byte-swizzled [q-block][key][64] layout
-//   dV  += P^T dOut       TMEM R2 [256,384)   (A = P^T from TMEM, B = dOut MN-major)
-//   dK  += dS^T Q         TMEM R3 [384,512)   (A = dS^T smem K-major, B = Q MN-major)
-//   dQ   = dS K           TMEM R1             (A = dS smem MN-major, B = K MN-major)
-//   epilogue warps: dQ rows (TMEM lane = query row) -> scale -> red.add to global
-// The next step's S^T is issued right after this step's dQ (the tensor core
-// executes its MMAs in order, so S^T never overwrites P^T before dV read it);
-// its dP^T waits until the dQ rows have been read out of R1.
+// dQ kernel (query-stationary, the shape of the forward).  Work item: one
+// 128-row query tile for a pair of query heads of one KV group; it walks the
+// 64-key sub-tiles the rows can see; the two heads ping-pong:
+//   S  = Q K^T        (M = 128 queries, N = 64 keys)   TMEM [256X, 256X+64)
+//   dP = dOut V^T                                       TMEM [256X+64, 256X+128)
+//   dS (bf16) is written back over S
+//   dQ += dS K        (A = dS from TMEM, B = K MN-major)   TMEM [256X+128, 256X+256)
+// dQ is scaled and written once per item, in bf16.
 //
-// CTA roles (320 threads): warps 0-3 and 4-7 each own half of the query
-// columns of the softmax and half of the head dimension of the dQ epilogue
-// (TMEM lanes 0-127 each); warp 8 is the TMA producer; warp 9 allocates TMEM
-// and one of its threads issues every MMA.  All waits are bounded.
+// Roles (320 threads): warps 0-3 run chain / head 0, warps 4-7 chain / head
+// 1 (one TMEM lane each), warp 8 is the TMA producer and work fetcher, warp
+// 9 allocates TMEM and one of its threads issues every MMA.  Masking is one
+// unsigned compare per element against the row's (or key's) visible
+// interval, skipped for fully visible chunks.  All waits are bounded.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -41,79 +44,43 @@ namespace {
 
 using namespace tc;
 
-constexpr int BK = 128, BQ = 128, HD = 128;
+constexpr int HD = 128;
+constexpr int SUB = kBwdSub;                          // 64
 constexpr int kThreads = 320;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
-constexpr uint32_t kColBlockBytes = 128 * 64 * 2;
-constexpr uint32_t kTileBytes = 2 * kColBlockBytes;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+constexpr uint32_t kBlk128 = 128 * 64 * 2;            // 128 rows x 64 bf16 column block
+constexpr uint32_t kBlk64 = 64 * 64 * 2;              // 64 rows x 64 bf16 column block
+constexpr uint32_t kTile128 = 2 * kBlk128;            // 128 x 128 bf16
+constexpr uint32_t kTile64 = 2 * kBlk64;              // 64 x 128 bf16
 constexpr float kLog2e = 1.4426950408889634f;
-
-struct BwdItem {
-  int ktile;      // 128-key tile
-  int g;          // key/value head
-  int i_lo;       // first query tile that sees the keys
-  int n_q;        // number of query tiles
-  int steps;      // G * n_q (-1: stop)
-  int pad[3];
-};
-
-struct __align__(1024) Smem {
-  uint8_t k[kTileBytes];
-  uint8_t v[kTileBytes];
-  uint8_t q[2][kTileBytes];
-  uint8_t dout[2][kTileBytes];
-  uint8_t ds[kTileBytes];
-  float lse2[2][BQ];           // lse * log2(e) of the stage's query rows
-  float delta[2][BQ];
-  uint64_t kv_full, kv_empty;
-  uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full, ds_full, dq_full, dq_empty, dkv_full, dkv_empty;
-  uint64_t item_full[2], item_empty[2];
-  BwdItem items[2];
-  uint32_t tmem_base;
-  int abort_flag;
-};
-
-// Dynamic shared memory: the tile set plus whatever alignment slack still
-// fits under the 227 KB limit; the kernel checks at run time that the
-// 1024-byte-aligned tile set fits (the base is 1024-aligned in practice).
 constexpr size_t kSmemLimit = 232448;
-static_assert(sizeof(Smem) <= kSmemLimit, "backward tile set exceeds 227 KB of shared memory");
-constexpr size_t kSmemBytes =
-    sizeof(Smem) + 1024 <= kSmemLimit ? sizeof(Smem) + 1024 : kSmemLimit;
 
-// D (+)= A B^T with both operands K-major, 128-byte swizzle (as the forward QK^T).
-__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
-                                       bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+// ---------------------------------------------------------------- MMA helpers
+
+// D = A B^T, A and B K-major (128-byte swizzle), K = 128 (head dim).
+// a_blk / b_blk: byte distance between the two 64-wide column blocks.
+__device__ __forceinline__ void mma_k128(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_blk,
+                                         uint32_t b_saddr, uint32_t b_blk, uint32_t idesc) {
   const uint64_t ad = smem_desc_sw128(a_saddr, 16, 1024);
   const uint64_t bd = smem_desc_sw128(b_saddr, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = ((kk >> 2) * kColBlockBytes + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, ad + off, bd + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    const uint32_t ao = ((kk >> 2) * a_blk + (kk & 3) * 32) >> 4;
+    const uint32_t bo = ((kk >> 2) * b_blk + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, ad + ao, bd + bo, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-template <typename TO>
-__device__ __forceinline__ void store_row32(TO* dst, const uint32_t (&v)[32], float scale) {
-  if constexpr (sizeof(TO) == 2) {
-    uint32_t w[16];
+// D (+)= A[tmem] B, K = 64 (4 steps of 16, 8 TMEM columns each); B is
+// MN-major with K along its rows (16 rows = 2048 B per step) and its two
+// 64-wide N blocks b_blk bytes apart.
+__device__ __forceinline__ void mma_tk64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
+                                         uint32_t b_blk, uint32_t idesc, bool accumulate) {
+  const uint64_t bd = smem_desc_sw128(b_saddr, b_blk, 1024);
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  } else {
-    float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      d4[i] = make_float4(__uint_as_float(v[4 * i]) * scale, __uint_as_float(v[4 * i + 1]) * scale,
-                          __uint_as_float(v[4 * i + 2]) * scale,
-                          __uint_as_float(v[4 * i + 3]) * scale);
-  }
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, bd + ((kk * 2048) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -123,53 +90,104 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                                 float scale) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// 1024-aligned view of dynamic shared memory, or nullptr (error recorded)
+// when the aligned structure would not fit in the launch's allocation.
+template <typename S>
+__device__ __forceinline__ S* smem_view(uint8_t* raw, WsHeader* hdr) {
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  const uint32_t base = smem_u32(raw);
+  if (((base + 1023u) & ~1023u) - base + sizeof(S) > dyn_bytes) {
+    if (threadIdx.x == 0) atomicExch(&hdr->status, (int)NSP_ERR_UNSUPPORTED);
+    return nullptr;
+  }
+  return reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                              ~static_cast<uintptr_t>(1023));
+}
+
+template <typename S>
+constexpr size_t smem_bytes() {
+  return sizeof(S) + 1024 <= kSmemLimit ? sizeof(S) + 1024 : kSmemLimit;
+}
+
 struct BwdArgs {
   AttnProblem p;
-  const float* lse2;      // [Hq, Tp] lse * log2(e), padded rows
+  const float* lse2;      // [Hq, Tp] lse * log2(e)
   const float* delta;     // [Hq, Tp]
   int64_t Tp;
-  float* dq_acc;          // [T, Hq, d] float32, zeroed
+  __nv_bfloat16* dq;      // [T, Hq, d]
   __nv_bfloat16* dk;      // [T, Hkv, d]
   __nv_bfloat16* dv;
-  const int2* ktiles;     // per key tile: first/last query tile
-  const int* korder;      // key tiles, most query tiles first
+  const int2* qtiles;     // per 128-row query tile: first/last 64-key sub-tile
+  const int* qorder;
+  const int2* ktiles;     // per 128-key tile: first/last 64-row query sub-tile
+  const int* korder;
 };
 
+// ================================================================ dK / dV
+
+constexpr int KV_NS = 2;
+
+struct KvItem {
+  int ktile, g, i_lo, n_q, steps, pad[3];   // steps = (G / 2) * n_q; -1 stops
+};
+
+struct __align__(1024) SmemKV {
+  uint8_t k[kTile128];
+  uint8_t v[kTile128];
+  uint8_t q[2][KV_NS][kTile64];
+  uint8_t dout[2][KV_NS][kTile64];
+  float lse2[2][KV_NS][SUB];
+  float delta[2][KV_NS][SUB];
+  uint64_t kv_full, kv_empty;
+  uint64_t qdo_full[2][KV_NS], qdo_empty[2][KV_NS];
+  uint64_t s_full[2], p_full[2];
+  uint64_t dkv_full, dkv_empty;
+  uint64_t item_full[2], item_empty[2];
+  KvItem items[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memory");
+
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_do, const BwdArgs a) {
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q64,
+                            const __grid_constant__ CUtensorMap tm_do64,
+                            const __grid_constant__ CUtensorMap tm_k128,
+                            const __grid_constant__ CUtensorMap tm_v128, const BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = p.hdr;
   if (status_bad(hdr)) return;
-  {
-    uint32_t dyn_bytes;
-    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
-    const uint32_t base = smem_u32(smem_raw);
-    if (((base + 1023u) & ~1023u) - base + sizeof(Smem) > dyn_bytes) {
-      if (threadIdx.x == 0) atomicExch(&hdr->status, (int)NSP_ERR_UNSUPPORTED);
-      return;
-    }
-  }
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  SmemKV* smp = smem_view<SmemKV>(smem_raw, hdr);
+  if (smp == nullptr) return;
+  SmemKV& sm = *smp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.qdo_full[s], 1);
-      mbar_init(&sm.qdo_empty[s], 1);
-      mbar_init(&sm.item_full[s], 1);
-      mbar_init(&sm.item_empty[s], 1 + 8);
+    for (int x = 0; x < 2; ++x) {
+      for (int s = 0; s < KV_NS; ++s) {
+        mbar_init(&sm.qdo_full[x][s], 1);
+        mbar_init(&sm.qdo_empty[x][s], 1);
+      }
+      mbar_init(&sm.s_full[x], 1);
+      mbar_init(&sm.p_full[x], 128);
+      mbar_init(&sm.item_full[x], 1);
+      mbar_init(&sm.item_empty[x], 1 + 8);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.ds_full, 256);
-    mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_empty, 256);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, 256);
     sm.abort_flag = 0;
@@ -180,10 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_q64);
+    tma_prefetch_desc(&tm_do64);
+    tma_prefetch_desc(&tm_k128);
+    tma_prefetch_desc(&tm_v128);
   }
   tc_fence_before();
   __syncthreads();
@@ -192,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
   const int G = p.Hq / p.Hkv;
+  const int npair = G >> 1;
   const int64_t T = p.q_len;
   const int n_items = hdr->n_items2 * p.Hkv;
 
@@ -202,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok) {
         const int idx = atomicAdd(&hdr->counter2, 1);
-        BwdItem it;
+        KvItem it;
         it.ktile = 0; it.g = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
         if (idx < n_items) {
           const int kt = a.korder[idx / p.Hkv];
@@ -211,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           it.g = idx - (idx / p.Hkv) * p.Hkv;
           it.i_lo = tr.x;
           it.n_q = tr.y - tr.x + 1;
-          it.steps = G * it.n_q;
+          it.steps = npair * it.n_q;
         }
         const uint32_t slot = it_count & 1;
         if (it_count >= 2 &&
@@ -227,124 +246,116 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile128);
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
-          tma_load_2d(sm.k + cb * kColBlockBytes, &tm_k, &sm.kv_full, it.g * HD + cb * 64,
-                      it.ktile * BK);
-          tma_load_2d(sm.v + cb * kColBlockBytes, &tm_v, &sm.kv_full, it.g * HD + cb * 64,
-                      it.ktile * BK);
+          tma_load_2d(sm.k + cb * kBlk128, &tm_k128, &sm.kv_full, it.g * HD + cb * 64,
+                      it.ktile * 128);
+          tma_load_2d(sm.v + cb * kBlk128, &tm_v128, &sm.kv_full, it.g * HD + cb * 64,
+                      it.ktile * 128);
         }
         ++kv_count;
-        for (int n = 0; n < it.steps; ++n) {
-          const int h = it.g * G + n / it.n_q;
-          const int i = it.i_lo + n % it.n_q;
-          const uint32_t st = qc & 1, use = qc >> 1;
-          if (use >= 1 && !mbar_wait(&sm.qdo_empty[st], (use - 1) & 1, abort_flag, hdr)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kTileBytes + 2 * BQ * sizeof(float));
+        for (int n = 0; n < it.steps && ok; ++n) {
+          const int pair = n / it.n_q;
+          const int i = it.i_lo + (n - pair * it.n_q);
+          const uint32_t st = qc % KV_NS, use = qc / KV_NS;
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            tma_load_2d(sm.q[st] + cb * kColBlockBytes, &tm_q, &sm.qdo_full[st], h * HD + cb * 64,
-                        i * BQ);
-            tma_load_2d(sm.dout[st] + cb * kColBlockBytes, &tm_do, &sm.qdo_full[st],
-                        h * HD + cb * 64, i * BQ);
+          for (int x = 0; x < 2; ++x) {
+            if (!ok) continue;
+            const int h = it.g * G + 2 * pair + x;
+            if (use >= 1 &&
+                !mbar_wait(&sm.qdo_empty[x][st], (use - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              continue;
+            }
+            mbar_arrive_expect_tx(&sm.qdo_full[x][st], 2 * kTile64 + 2 * SUB * sizeof(float));
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+              tma_load_2d(sm.q[x][st] + cb * kBlk64, &tm_q64, &sm.qdo_full[x][st],
+                          h * HD + cb * 64, i * SUB);
+              tma_load_2d(sm.dout[x][st] + cb * kBlk64, &tm_do64, &sm.qdo_full[x][st],
+                          h * HD + cb * 64, i * SUB);
+            }
+            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * SUB;
+            bulk_load(sm.lse2[x][st], a.lse2 + row, SUB * sizeof(float), &sm.qdo_full[x][st]);
+            bulk_load(sm.delta[x][st], a.delta + row, SUB * sizeof(float), &sm.qdo_full[x][st]);
           }
-          const int64_t row = (int64_t)h * a.Tp + (int64_t)i * BQ;
-          bulk_load(sm.lse2[st], a.lse2 + row, BQ * sizeof(float), &sm.qdo_full[st]);
-          bulk_load(sm.delta[st], a.delta + row, BQ * sizeof(float), &sm.qdo_full[st]);
-          ++qc;
+          if (ok) ++qc;
         }
       }
       if (!ok) {
+        // abort: every copy issued so far completes on its stage barrier
         if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
-        for (uint32_t s = 0; s < 2 && s < qc; ++s) {
-          const uint32_t last = qc - 1 - ((qc - 1 - s) & 1);
-          drain_wait(&sm.qdo_full[last & 1], (last >> 1) & 1);
-        }
+        for (uint32_t j = (qc > KV_NS ? qc - KV_NS : 0); j <= qc; ++j)
+          for (int x = 0; x < 2; ++x) drain_wait(&sm.qdo_full[x][j % KV_NS], (j / KV_NS) & 1);
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, true, false);   // B MN-major
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, 128, true, true);    // A, B MN-major
-      const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v), ds_s = smem_u32(sm.ds);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, SUB, false, false);   // S^T, dP^T
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, true, false);   // dV, dK
+      const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v);
       uint32_t it_count = 0, items_done = 0, qc = 0;
+      uint32_t pc[2] = {0, 0};
       bool ok = true;
       while (ok) {
         const uint32_t slot = it_count & 1;
         if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
-        const BwdItem it = sm.items[slot];
+        const KvItem it = sm.items[slot];
         mbar_arrive(&sm.item_empty[slot]);
         ++it_count;
         if (it.steps < 0) break;
         if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
         for (int n = 0; n < it.steps && ok; ++n) {
-          const uint32_t st = qc & 1;
-          const uint32_t q_s = smem_u32(sm.q[st]), do_s = smem_u32(sm.dout[st]);
+          const uint32_t st = qc % KV_NS;
           if (n == 0) {
-            if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
-            tc_fence_after();
-            mma_kk(tmem + kColS, k_s, q_s, false);                 // S^T = K Q^T
-          }
-          if (qc > 0 && !mbar_wait(&sm.dq_empty, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
-          tc_fence_after();
-          mma_kk(tmem + kColDP, v_s, do_s, false);                 // dP^T = V dOut^T
-          mma_commit(&sm.s_full);
-          if (!mbar_wait(&sm.ds_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
-          tc_fence_after();
-          if (n == 0 && items_done > 0 &&
-              !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool acc = n > 0;
-          {
-            // dV += P^T dOut: P^T columns of query rows 0-63 at [0,32), 64-127 at [64,96)
-            const uint64_t bd = smem_desc_sw128(do_s, kColBlockBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t a_col = kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-              mma_ts(tmem + kColDV, tmem + a_col, bd + ((kk * 2048) >> 4), idesc_pv,
-                     (acc || kk > 0) ? 1u : 0u);
+            for (int x = 0; x < 2; ++x) {
+              if (!ok) continue;
+              if (!mbar_wait(&sm.qdo_full[x][st], (qc / KV_NS) & 1, abort_flag, hdr)) {
+                ok = false;
+                continue;
+              }
+              tc_fence_after();
+              mma_k128(tmem + 128 * x, k_s, kBlk128, smem_u32(sm.q[x][st]), kBlk64, idesc_s);
+              mma_k128(tmem + 128 * x + 64, v_s, kBlk128, smem_u32(sm.dout[x][st]), kBlk64,
+                       idesc_s);
+              mma_commit(&sm.s_full[x]);
             }
+            if (!ok) break;
           }
-          {
-            // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
-            const uint64_t ad = smem_desc_sw128(ds_s, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(q_s, kColBlockBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t aoff = ((kk >> 2) * kColBlockBytes + (kk & 3) * 32) >> 4;
-              mma_ss(tmem + kColDK, ad + aoff, bd + ((kk * 2048) >> 4), idesc_pv,
-                     (acc || kk > 0) ? 1u : 0u);
-            }
-          }
-          mma_commit(&sm.qdo_empty[st]);
-          {
-            // dQ = dS K: A = dS MN-major (M = query rows), B = K MN-major
-            const uint64_t ad = smem_desc_sw128(ds_s, kColBlockBytes, 1024);
-            const uint64_t bd = smem_desc_sw128(k_s, kColBlockBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + kColDP, ad + ((kk * 2048) >> 4), bd + ((kk * 2048) >> 4), idesc_dq,
-                     kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&sm.dq_full);
-          if (n + 1 < it.steps) {
-            const uint32_t stn = (qc + 1) & 1;
-            if (!mbar_wait(&sm.qdo_full[stn], ((qc + 1) >> 1) & 1, abort_flag, hdr)) {
+          for (int x = 0; x < 2; ++x) {
+            if (!ok) continue;
+            if (!mbar_wait(&sm.p_full[x], pc[x] & 1, abort_flag, hdr)) { ok = false; continue; }
+            ++pc[x];
+            const bool first = (n == 0 && x == 0);
+            if (first && items_done > 0 &&
+                !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
               ok = false;
-              break;
+              continue;
             }
             tc_fence_after();
-            mma_kk(tmem + kColS, k_s, smem_u32(sm.q[stn]), false);
+            mma_tk64(tmem + 256, tmem + 128 * x, smem_u32(sm.dout[x][st]), kBlk64, idesc_acc,
+                     !first);
+            mma_tk64(tmem + 384, tmem + 128 * x + 64, smem_u32(sm.q[x][st]), kBlk64, idesc_acc,
+                     !first);
+            mma_commit(&sm.qdo_empty[x][st]);
+            if (n + 1 < it.steps) {
+              const uint32_t stn = (qc + 1) % KV_NS;
+              if (!mbar_wait(&sm.qdo_full[x][stn], ((qc + 1) / KV_NS) & 1, abort_flag, hdr)) {
+                ok = false;
+                continue;
+              }
+              tc_fence_after();
+              mma_k128(tmem + 128 * x, k_s, kBlk128, smem_u32(sm.q[x][stn]), kBlk64, idesc_s);
+              mma_k128(tmem + 128 * x + 64, v_s, kBlk128, smem_u32(sm.dout[x][stn]), kBlk64,
+                       idesc_s);
+              mma_commit(&sm.s_full[x]);
+            }
           }
-          ++qc;
+          if (ok) ++qc;
         }
         if (!ok) break;
         mma_commit(&sm.dkv_full);
@@ -353,59 +364,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax + epilogues
-    const int wg = warp >> 2;                 // 0: query columns / head dims 0-63; 1: 64-127
+    // ------------------------------------------------------------ softmax + dK/dV epilogue
+    const int x = warp >> 2;
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;             // TMEM lane: key row (S^T, dV, dK) or query row (dQ)
+    const int r = wq * 32 + lane;                          // TMEM lane = key row
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + 128 * x;
+    const uint32_t dp_tm = s_tm + 64;
     const float sl2 = p.scale * kLog2e;
-    const uint32_t ds_row = smem_u32(sm.ds) + wg * kColBlockBytes + r * 128;
-    uint32_t it_count = 0, items_done = 0, qc = 0;
+    uint32_t it_count = 0, items_done = 0, qc = 0, sc = 0;
     bool ok = true;
     while (ok) {
       const uint32_t slot = it_count & 1;
       if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
-      const BwdItem it = sm.items[slot];
+      const KvItem it = sm.items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.steps < 0) break;
-      // this thread's key and the query interval [qlo, qhi) that sees it
-      const int64_t key = (int64_t)it.ktile * BK + r;
-      int64_t qlo = 0, qhi = 0;
+      const int64_t key = (int64_t)it.ktile * 128 + r;
+      int64_t qlo = 0, qhi = 0;                             // queries that see this key
       if (key < T) {
         const int b = doc_of(p.cu, p.ndoc, key);
         qlo = p.causal ? key : (int64_t)__ldg(p.cu + b);
         qhi = (int64_t)__ldg(p.cu + b + 1);
       }
       for (int n = 0; n < it.steps && ok; ++n) {
-        const int h = it.g * G + n / it.n_q;
-        const int64_t q0 = (int64_t)(it.i_lo + n % it.n_q) * BQ;
-        const uint32_t st = qc & 1;
-        // the stage's lse2 / delta rows arrive with its Q and dOut tiles
-        if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
-        const float* lse2s = sm.lse2[st];
-        const float* deltas = sm.delta[st];
-        if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+        const int pair = n / it.n_q;
+        const int64_t q0 = (int64_t)(it.i_lo + (n - pair * it.n_q)) * SUB;
+        const uint32_t st = qc % KV_NS;
+        if (!mbar_wait(&sm.qdo_full[x][st], (qc / KV_NS) & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait(&sm.s_full[x], sc & 1, abort_flag, hdr)) { ok = false; break; }
+        ++sc;
         tc_fence_after();
+        const float* lse2s = sm.lse2[x][st];
+        const float* deltas = sm.delta[x][st];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int col0 = wg * 64 + c * 32;
           uint32_t s[32], dp[32];
-          tmem_ld32(tmem + lane_base + kColS + col0, s);
-          tmem_ld32(tmem + lane_base + kColDP + col0, dp);
+          tmem_ld32(s_tm + c * 32, s);
+          tmem_ld32(dp_tm + c * 32, dp);
           tmem_wait_ld();
-          const int64_t qg0 = q0 + col0;
-          // visible query columns of this key, clipped to the chunk: [loc, hic)
+          const int64_t qg0 = q0 + c * 32;
           const int loc = (int)min(max(qlo - qg0, (int64_t)0), (int64_t)32);
           const int hic = (int)min(max(qhi - qg0, (int64_t)0), (int64_t)32);
           const uint32_t span = (uint32_t)(hic - loc);
-          const bool full_w = __all_sync(0xffffffffu, qlo <= qg0 && qg0 + 32 <= qhi);
+          const bool full_w = __all_sync(0xffffffffu, loc == 0 && hic == 32);
           uint32_t pk[16], dk[16];
           if (full_w) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int cc = col0 + 2 * e;
+              const int cc = c * 32 + 2 * e;
               const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]));
               const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2s[cc + 1]));
               pk[e] = pack_bf16x2(p0, p1);
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int cc = col0 + 2 * e;
+              const int cc = c * 32 + 2 * e;
               const bool v0 = (uint32_t)(2 * e - loc) < span;
               const bool v1 = (uint32_t)(2 * e + 1 - loc) < span;
               const float x0 = fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]);
@@ -428,41 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
             }
           }
-          tmem_st16(tmem + lane_base + kColS + wg * 64 + c * 16, pk);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = c * 4 + u;                     // 8 query columns per 16 bytes
-            st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
-                         dk[4 * u + 2], dk[4 * u + 3]);
-          }
+          tmem_st16(s_tm + c * 16, pk);       // P^T over S^T (columns already read)
+          tmem_st16(dp_tm + c * 16, dk);      // dS^T over dP^T
         }
         tmem_wait_st();
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.ds_full);
-        // dQ rows of this step: TMEM lane = query row, my half of the head dimension
-        if (!mbar_wait(&sm.dq_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const int64_t qrow = q0 + r;
-          float* dst = a.dq_acc + (qrow * p.Hq + h) * HD + wg * 64;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kColDP + wg * 64 + c * 32, v);
-            tmem_wait_ld();
-            if (qrow < T) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                red_add_v4(dst + c * 32 + 4 * u, __uint_as_float(v[4 * u]) * p.scale,
-                           __uint_as_float(v[4 * u + 1]) * p.scale,
-                           __uint_as_float(v[4 * u + 2]) * p.scale,
-                           __uint_as_float(v[4 * u + 3]) * p.scale);
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
+        mbar_arrive(&sm.p_full[x]);
         ++qc;
       }
       if (!ok) break;
@@ -470,15 +450,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sm.dkv_full, items_done & 1, abort_flag, hdr)) break;
       tc_fence_after();
       {
-        const uint32_t col = wg == 0 ? kColDV : kColDK;
-        const float sc = wg == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + (key * p.Hkv + it.g) * HD;
+        const uint32_t col = x == 0 ? 256u : 384u;
+        const float scale = x == 0 ? 1.f : p.scale;
+        __nv_bfloat16* dst = (x == 0 ? a.dv : a.dk) + (key * p.Hkv + it.g) * HD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + col + c * 32, v);
           tmem_wait_ld();
-          if (key < T) store_row32<__nv_bfloat16>(dst + c * 32, v, sc);
+          if (key < T) store_row32_bf16(dst + c * 32, v, scale);
         }
       }
       tc_fence_before();
@@ -495,6 +475,344 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================================================ dQ
+
+constexpr int Q_NS = 3;
+
+struct QItem {
+  int qtile, h0, g, j_lo, n_kv, pad[3];     // n_kv 64-key sub-tiles; -1 stops
+};
+
+struct __align__(1024) SmemQ {
+  uint8_t q[2][kTile128];
+  uint8_t dout[2][kTile128];
+  uint8_t k[Q_NS][kTile64];
+  uint8_t v[Q_NS][kTile64];
+  uint64_t qdo_full, qdo_empty;
+  uint64_t k_full[Q_NS], k_empty[Q_NS], v_full[Q_NS], v_empty[Q_NS];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t item_full[2], item_empty[2];
+  QItem items[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(SmemQ) <= kSmemLimit, "dQ tile set exceeds shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q128,
+                          const __grid_constant__ CUtensorMap tm_do128,
+                          const __grid_constant__ CUtensorMap tm_k64,
+                          const __grid_constant__ CUtensorMap tm_v64, const BwdArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const AttnProblem& p = a.p;
+  WsHeader* hdr = p.hdr;
+  if (status_bad(hdr)) return;
+  SmemQ* smp = smem_view<SmemQ>(smem_raw, hdr);
+  if (smp == nullptr) return;
+  SmemQ& sm = *smp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.qdo_full, 1);
+    mbar_init(&sm.qdo_empty, 1);
+    for (int s = 0; s < Q_NS; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sm.s_full[x], 1);
+      mbar_init(&sm.p_full[x], 128);
+      mbar_init(&sm.o_full[x], 1);
+      mbar_init(&sm.item_full[x], 1);
+      mbar_init(&sm.item_empty[x], 1 + 8);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q128);
+    tma_prefetch_desc(&tm_do128);
+    tma_prefetch_desc(&tm_k64);
+    tma_prefetch_desc(&tm_v64);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+  const int n_pairs = p.Hq >> 1;
+  const int G = p.Hq / p.Hkv;
+  const int64_t T = p.q_len;
+  const int n_items = hdr->n_items * n_pairs;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it_count = 0, q_count = 0, kv_count = 0;
+      bool ok = true;
+      while (ok) {
+        const int idx = atomicAdd(&hdr->counter, 1);
+        QItem it;
+        it.qtile = 0; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
+        if (idx < n_items) {
+          const int qt = a.qorder[idx / n_pairs];
+          const int pair = idx - (idx / n_pairs) * n_pairs;
+          const int2 tr = a.qtiles[qt];
+          it.qtile = qt;
+          it.h0 = 2 * pair;
+          it.g = (2 * pair) / G;
+          it.j_lo = tr.x;
+          it.n_kv = tr.y - tr.x + 1;
+        }
+        const uint32_t slot = it_count & 1;
+        if (it_count >= 2 &&
+            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
+          ok = false;
+          break;
+        }
+        sm.items[slot] = it;
+        mbar_arrive(&sm.item_full[slot]);
+        ++it_count;
+        if (it.n_kv <= 0) {
+          if (it.n_kv < 0) break;
+          continue;
+        }
+        if (q_count >= 1 && !mbar_wait(&sm.qdo_empty, (q_count - 1) & 1, abort_flag, hdr)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.qdo_full, 4 * kTile128);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            tma_load_2d(sm.q[x] + cb * kBlk128, &tm_q128, &sm.qdo_full, (it.h0 + x) * HD + cb * 64,
+                        it.qtile * 128);
+            tma_load_2d(sm.dout[x] + cb * kBlk128, &tm_do128, &sm.qdo_full,
+                        (it.h0 + x) * HD + cb * 64, it.qtile * 128);
+          }
+        ++q_count;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = kv_count % Q_NS, use = kv_count / Q_NS;
+          const int key0 = (it.j_lo + jj) * SUB;
+          if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.k_full[st], kTile64);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.k[st] + cb * kBlk64, &tm_k64, &sm.k_full[st], it.g * HD + cb * 64, key0);
+          if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            drain_wait(&sm.k_full[st], use & 1);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.v_full[st], kTile64);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.v[st] + cb * kBlk64, &tm_v64, &sm.v_full[st], it.g * HD + cb * 64, key0);
+          ++kv_count;
+        }
+      }
+      if (!ok) {
+        if (q_count >= 1) drain_wait(&sm.qdo_full, (q_count - 1) & 1);
+        for (uint32_t j = (kv_count > Q_NS ? kv_count - Q_NS : 0); j < kv_count; ++j) {
+          drain_wait(&sm.k_full[j % Q_NS], (j / Q_NS) & 1);
+          drain_wait(&sm.v_full[j % Q_NS], (j / Q_NS) & 1);
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, SUB, false, false);   // S, dP
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, false);    // dQ
+      uint32_t it_count = 0, q_count = 0, kv_count = 0;
+      uint32_t pc[2] = {0, 0};
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it_count & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        const QItem it = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++it_count;
+        if (it.n_kv < 0) break;
+        if (it.n_kv == 0) continue;
+        if (!mbar_wait(&sm.qdo_full, q_count & 1, abort_flag, hdr)) break;
+        ++q_count;
+        {
+          const uint32_t st = kv_count % Q_NS, use = kv_count / Q_NS;
+          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) break;
+          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            mma_k128(tmem + 256 * x, smem_u32(sm.q[x]), kBlk128, smem_u32(sm.k[st]), kBlk64,
+                     idesc_s);
+            mma_k128(tmem + 256 * x + 64, smem_u32(sm.dout[x]), kBlk128, smem_u32(sm.v[st]),
+                     kBlk64, idesc_s);
+            mma_commit(&sm.s_full[x]);
+          }
+          mma_commit(&sm.v_empty[st]);
+          if (it.n_kv == 1) mma_commit(&sm.qdo_empty);
+        }
+        for (int jj = 0; jj < it.n_kv && ok; ++jj) {
+          const uint32_t st = (kv_count + jj) % Q_NS;
+          const bool has_next = jj + 1 < it.n_kv;
+          const uint32_t stn = (kv_count + jj + 1) % Q_NS, usen = (kv_count + jj + 1) / Q_NS;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!ok) continue;
+            if (!mbar_wait(&sm.p_full[x], pc[x] & 1, abort_flag, hdr)) { ok = false; continue; }
+            ++pc[x];
+            tc_fence_after();
+            mma_tk64(tmem + 256 * x + 128, tmem + 256 * x, smem_u32(sm.k[st]), kBlk64, idesc_dq,
+                     jj > 0);
+            if (x == 1) mma_commit(&sm.k_empty[st]);
+            if (!has_next) {
+              mma_commit(&sm.o_full[x]);
+              continue;
+            }
+            if (x == 0) {
+              if (!mbar_wait(&sm.k_full[stn], usen & 1, abort_flag, hdr) ||
+                  !mbar_wait(&sm.v_full[stn], usen & 1, abort_flag, hdr)) {
+                ok = false;
+                continue;
+              }
+              tc_fence_after();
+            }
+            mma_k128(tmem + 256 * x, smem_u32(sm.q[x]), kBlk128, smem_u32(sm.k[stn]), kBlk64,
+                     idesc_s);
+            mma_k128(tmem + 256 * x + 64, smem_u32(sm.dout[x]), kBlk128, smem_u32(sm.v[stn]),
+                     kBlk64, idesc_s);
+            mma_commit(&sm.s_full[x]);
+            if (x == 1) {
+              mma_commit(&sm.v_empty[stn]);
+              if (jj + 2 == it.n_kv) mma_commit(&sm.qdo_empty);
+            }
+          }
+        }
+        if (!ok) break;
+        kv_count += it.n_kv;
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + dQ epilogue
+    const int x = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;                          // TMEM lane = query row
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t s_tm = tmem + lane_base + 256 * x;
+    const uint32_t dp_tm = s_tm + 64;
+    const uint32_t dq_tm = s_tm + 128;
+    const float sl2 = p.scale * kLog2e;
+    uint32_t it_count = 0, sc = 0, oc = 0;
+    bool ok = true;
+    while (ok) {
+      const uint32_t slot = it_count & 1;
+      if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+      const QItem it = sm.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+      ++it_count;
+      if (it.n_kv < 0) break;
+      const int h = it.h0 + x;
+      const int64_t row = (int64_t)it.qtile * 128 + r;
+      const bool valid = row < T;
+      int lo = 0, hi = 0;                                    // visible keys [lo, hi)
+      float lse2r = 0.f, deltar = 0.f;
+      if (valid) {
+        const int b = doc_of(p.cu, p.ndoc, row);
+        lo = __ldg(p.cu + b);
+        hi = p.causal ? (int)row + 1 : __ldg(p.cu + b + 1);
+        lse2r = __ldg(a.lse2 + (int64_t)h * a.Tp + row);
+        deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
+      }
+      for (int jj = 0; jj < it.n_kv && ok; ++jj) {
+        if (!mbar_wait(&sm.s_full[x], sc & 1, abort_flag, hdr)) { ok = false; break; }
+        ++sc;
+        tc_fence_after();
+        const int key0 = (it.j_lo + jj) * SUB;
+        const int aa = lo - key0;
+        const uint32_t span = (uint32_t)(hi - lo);
+        const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + SUB <= hi);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(s_tm + c * 32, s);
+          tmem_ld32(dp_tm + c * 32, dp);
+          tmem_wait_ld();
+          uint32_t dk[16];
+          if (full_w) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lse2r));
+              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2r));
+              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - deltar),
+                                  p1 * (__uint_as_float(dp[2 * e + 1]) - deltar));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = c * 32 + 2 * e;
+              const bool v0 = (uint32_t)(col - aa) < span;
+              const bool v1 = (uint32_t)(col + 1 - aa) < span;
+              const float p0 = ex2(v0 ? fmaf(__uint_as_float(s[2 * e]), sl2, -lse2r) : -INFINITY);
+              const float p1 =
+                  ex2(v1 ? fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2r) : -INFINITY);
+              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - deltar : 0.f;
+              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - deltar : 0.f;
+              dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
+            }
+          }
+          tmem_st16(s_tm + c * 16, dk);       // dS over S (columns already read)
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[x]);
+      }
+      if (!ok) break;
+      // epilogue: dQ = scale * accumulated dS K, written once in bf16
+      __nv_bfloat16* dst = a.dq + (row * p.Hq + h) * HD;
+      if (it.n_kv > 0) {
+        if (!mbar_wait(&sm.o_full[x], oc & 1, abort_flag, hdr)) break;
+        ++oc;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(dq_tm + c * 32, v);
+          tmem_wait_ld();
+          if (valid) store_row32_bf16(dst + c * 32, v, p.scale);
+        }
+      } else if (valid) {
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ host
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
@@ -510,12 +828,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+// [rows, cols] bf16 row-major; box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -524,42 +843,54 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 
 }  // namespace
 
+bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
+  return io_dtype == NSP_BF16 && d == HD && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
+}
+
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
-                               const BwdWsLayout& L, char* ws, cudaStream_t s, bool* launched) {
-  *launched = false;
-  if (p.io_dtype != NSP_BF16 || p.d != HD || p.q_len <= 0) return cudaSuccess;
+                               const BwdWsLayout& L, char* ws, cudaStream_t s) {
   const int64_t T = p.q_len;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!make_map(&mq, p.q, T, (int64_t)p.Hq * HD) || !make_map(&mdo, dout, T, (int64_t)p.Hq * HD) ||
-      !make_map(&mk, p.k, T, (int64_t)p.Hkv * HD) || !make_map(&mv, p.v, T, (int64_t)p.Hkv * HD))
-    return cudaSuccess;
-  *launched = true;
+  CUtensorMap mq128, mdo128, mk128, mv128, mq64, mdo64, mk64, mv64;
+  const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
+  if (!make_map(&mq128, p.q, T, qc, 128) || !make_map(&mdo128, dout, T, qc, 128) ||
+      !make_map(&mk128, p.k, T, kc, 128) || !make_map(&mv128, p.v, T, kc, 128) ||
+      !make_map(&mq64, p.q, T, qc, 64) || !make_map(&mdo64, dout, T, qc, 64) ||
+      !make_map(&mk64, p.k, T, kc, 64) || !make_map(&mv64, p.v, T, kc, 64))
+    return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * HD, s);
-  if (e != cudaSuccess) return e;
-  e = launch_bwd_delta(out, dout, lse, delta, lse2, T, L.Tp, p.Hq, HD, p.io_dtype, p.hdr, s);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes);
+  cudaError_t e = launch_bwd_delta(out, dout, lse, delta, lse2, T, L.Tp, p.Hq, HD, p.io_dtype,
+                                   p.hdr, s);
   if (e != cudaSuccess) return e;
   BwdArgs a;
   a.p = p;
   a.lse2 = lse2;
   a.delta = delta;
   a.Tp = L.Tp;
-  a.dq_acc = dq_acc;
+  a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
   a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
   a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+  a.qtiles = reinterpret_cast<const int2*>(ws + L.qtiles);
+  a.qorder = reinterpret_cast<const int*>(ws + L.qorder);
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);
   a.korder = reinterpret_cast<const int*>(ws + L.korder);
-  attn_bwd_tc_kernel<<<num_sms(), kThreads, kSmemBytes, s>>>(mq, mk, mv, mdo, a);
+  const int grid = num_sms();
+  constexpr size_t kv_bytes = smem_bytes<SmemKV>();
+  constexpr size_t q_bytes = smem_bytes<SmemQ>();
+  e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kv_bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)q_bytes);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kv_bytes, s>>>(mq64, mdo64, mk128, mv128, a);
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_dq_convert(dq_acc, dq, T * p.Hq * HD, p.io_dtype, p.hdr, s);
+  attn_bwd_dq_tc_kernel<<<grid, kThreads, q_bytes, s>>>(mq128, mdo128, mk64, mv64, a);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace nsp

@@ -15,7 +15,7 @@ struct WsHeader {
   int32_t counter;      // dynamic work-fetch counter (reset by the prep kernel)
   int32_t n_items;      // number of scheduled work items
   int32_t max_cost;     // largest per-q-tile KV-tile count
-  int32_t counter2;     // second work counter (backward)
+  int32_t counter2;     // second work counter (backward dK/dV)
   int32_t n_items2;
   int32_t pad[58];      // header is 256 bytes
 };
@@ -48,32 +48,40 @@ inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
   return L;
 }
 
-// Backward workspace: header, forward-style schedule for query tiles and a
-// schedule for key tiles, delta and lse * log2(e) [Hq, Tp] f32 (rows padded
-// to Tp = whole 128-row tiles, padding zeroed), dq accumulator [T, Hq, d] f32.
+// Backward workspace: header; schedule of 128-row query tiles listing 64-key
+// sub-tiles (dQ kernel) and of 128-key tiles listing 64-row query sub-tiles
+// (dK/dV kernel); delta and lse * log2(e) [Hq, Tp] f32 (rows padded to whole
+// 128-row tiles, padding zeroed); and, for the CUDA-core path only, a
+// float32 dq accumulator [T, Hq, d].
+constexpr int kBwdSub = 64;        // sub-tile of the backward kernels
+
 struct BwdWsLayout {
-  FwdWsLayout q;       // query-tile schedule (shares the header)
-  size_t ktiles;       // int2 [n_kvtiles]: first/last query tile that sees each key tile
-  size_t korder;       // int32 [n_kvtiles]
-  size_t khist;        // int32 [n_qtiles + 2]
-  size_t delta;        // float [Hq, Tp]
-  size_t lse2;         // float [Hq, Tp]
-  size_t dq_acc;       // float [T, Hq, d]
+  size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_sub + 2]
+  size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_sub + 2]
+  size_t delta;                    // float [Hq, Tp]
+  size_t lse2;                     // float [Hq, Tp]
+  size_t dq_acc;                   // float [T, Hq, d] (CUDA-core path)
   size_t total;
-  int64_t Tp;
+  int64_t Tp, n_qtiles, n_ktiles, n_sub;
 };
 
-inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d) {
+inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d, bool need_dq_acc) {
   BwdWsLayout L;
-  L.q = fwd_ws_layout(T, T);
-  size_t off = L.q.total;
-  L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.q.n_kvtiles, 256);
-  L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.q.n_kvtiles, 256);
-  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.q.n_qtiles + 2), 256);
-  L.Tp = L.q.n_qtiles * kTileM;
+  L.n_qtiles = ceil_div(T, kTileM);
+  L.n_ktiles = ceil_div(T, kTileN);
+  L.n_sub = ceil_div(T, kBwdSub);
+  L.Tp = L.n_qtiles * kTileM;
+  size_t off = sizeof(WsHeader);
+  L.qtiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_qtiles, 256);
+  L.qorder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_qtiles, 256);
+  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_sub + 2), 256);
+  L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_ktiles, 256);
+  L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_ktiles, 256);
+  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_sub + 2), 256);
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.lse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
-  L.dq_acc = off; off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
+  L.dq_acc = off;
+  if (need_dq_acc) off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
   L.total = off;
   return L;
 }
@@ -94,17 +102,20 @@ struct AttnProblem {
 // ---- launchers implemented in the .cu files (return cudaError_t) ----
 cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                 cudaStream_t s);
-cudaError_t launch_bwd_key_schedule(const AttnProblem& p, const BwdWsLayout& L, char* ws,
-                                    cudaStream_t s);
+cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
+                                 cudaStream_t s);
 cudaError_t launch_attn_fwd_simt(const AttnProblem& p, cudaStream_t s);
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                cudaStream_t s, bool* launched);
 cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const void* dout,
                                  const float* lse, void* dq, void* dk, void* dv,
                                  const BwdWsLayout& L, char* ws, cudaStream_t s);
+// True when the tensor-core backward takes this problem (bf16, d = 128,
+// an even number of query heads per KV head).
+bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv);
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
-                               const BwdWsLayout& L, char* ws, cudaStream_t s, bool* launched);
+                               const BwdWsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
                              float* lse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
                              WsHeader* hdr, cudaStream_t s);

@@ -12,9 +12,11 @@
 // mirrors SAP's regional load balancing (same section) on one GPU.
 //
 // Mode 0 (forward / backward dQ view): tile i covers query rows
-//   [q_start + 128 i, ...) and lists KV tiles j (keys [kv_start + 128 j, ...)).
+//   [q_start + 128 i, ...) and lists the key sub-tiles j (keys
+//   [kv_start + gran j, ...), gran = 128 forward, 64 backward) its rows see.
 // Mode 1 (backward dK/dV view): tile j covers keys [128 j, ...) of the whole
-//   stream and lists the query tiles whose rows can see any of those keys.
+//   stream and lists the query sub-tiles (rows [gran i, ...)) whose rows can
+//   see any of those keys.
 //
 // One block of 1024 threads; the first mode-0 launch of a call validates
 // cu_seqlens and resets the workspace status word.
@@ -37,6 +39,7 @@ struct SchedArgs {
   int32_t* hist;       // n_buckets ints
   int32_t n_tiles;     // tiles to schedule
   int32_t n_buckets;   // max cost + 1 (cost = number of listed tiles)
+  int32_t gran;        // granularity (rows or keys) of the listed tiles
   WsHeader* hdr;
   int32_t second;      // write counters into counter2 / n_items2
 };
@@ -86,8 +89,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
       const int64_t lo = max((int64_t)a.cu[b0], a.kv_start);
       const int64_t hi = min(a.causal ? r1 + 1 : (int64_t)a.cu[b1 + 1], kv_end);  // exclusive
       if (hi > lo) {
-        lo_t = (int)((lo - a.kv_start) / kTileN);
-        hi_t = (int)((hi - 1 - a.kv_start) / kTileN);
+        lo_t = (int)((lo - a.kv_start) / a.gran);
+        hi_t = (int)((hi - 1 - a.kv_start) / a.gran);
       }
     } else {
       const int64_t k0 = (int64_t)i * kTileN;
@@ -95,8 +98,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
       const int b0 = doc_of(a.cu, a.ndoc, k0), b1 = doc_of(a.cu, a.ndoc, k1);
       const int64_t lo = a.causal ? k0 : (int64_t)a.cu[b0];
       const int64_t hi = (int64_t)a.cu[b1 + 1];                // exclusive
-      lo_t = (int)(lo / kTileM);
-      hi_t = (int)((hi - 1) / kTileM);
+      lo_t = (int)(lo / a.gran);
+      hi_t = (int)((hi - 1) / a.gran);
     }
     a.tiles[i] = make_int2(lo_t, hi_t);
     const int cost = hi_t - lo_t + 1;
@@ -144,6 +147,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
 cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                 cudaStream_t s) {
   SchedArgs a;
+  a.gran = kTileN;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
   a.causal = p.causal; a.mode = 0; a.validate = 1;
@@ -157,17 +161,29 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_key_schedule(const AttnProblem& p, const BwdWsLayout& L, char* ws,
-                                    cudaStream_t s) {
+cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
+                                 cudaStream_t s) {
+  // query tiles of 128 rows listing 64-key sub-tiles (validates cu_seqlens)
   SchedArgs a;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = 0; a.q_len = p.q_len; a.kv_start = 0; a.kv_len = p.kv_len;
-  a.causal = p.causal; a.mode = 1; a.validate = 0;
+  a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub;
+  a.tiles = reinterpret_cast<int2*>(ws + L.qtiles);
+  a.order = reinterpret_cast<int32_t*>(ws + L.qorder);
+  a.hist = reinterpret_cast<int32_t*>(ws + L.qhist);
+  a.n_tiles = (int32_t)L.n_qtiles;
+  a.n_buckets = (int32_t)L.n_sub + 2;
+  a.hdr = p.hdr; a.second = 0;
+  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // key tiles of 128 keys listing 64-row query sub-tiles
+  a.mode = 1; a.validate = 0;
   a.tiles = reinterpret_cast<int2*>(ws + L.ktiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.korder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.khist);
-  a.n_tiles = (int32_t)L.q.n_kvtiles;
-  a.n_buckets = (int32_t)L.q.n_qtiles + 2;
+  a.n_tiles = (int32_t)L.n_ktiles;
+  a.n_buckets = (int32_t)L.n_sub + 2;
   a.hdr = p.hdr; a.second = 1;
   schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
   return cudaGetLastError();

@@ -38,7 +38,7 @@ _SIGNATURES = {
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
     "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                     _i32, _i32, _f32, _i32, _i32, _vp, _i32, _vp, _vp, _vp]),
-    "nsp_attn_bwd_workspace_size": (_sz, [_i64, _i32, _i32, _i32]),
+    "nsp_attn_bwd_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32]),
     "nsp_attn_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
                             _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_bwd_validate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
@@ -123,8 +123,8 @@ def nsp_attn_fwd_workspace_size(q_len: int, kv_len: int, Hq: int, Hkv: int, d: i
     return int(load().nsp_attn_fwd_workspace_size(q_len, kv_len, Hq, Hkv, d))
 
 
-def nsp_attn_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int) -> int:
-    return int(load().nsp_attn_bwd_workspace_size(T, Hq, Hkv, d))
+def nsp_attn_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int, io_dtype: int = NSP_BF16) -> int:
+    return int(load().nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, int(io_dtype)))
 
 
 def nsp_attn_fwd(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq, Hkv, d,
@@ -221,8 +221,8 @@ def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, works
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
-        workspace = torch.empty(nsp_attn_bwd_workspace_size(T, Hq, Hkv, d), dtype=torch.uint8,
-                                device=q.device)
+        workspace = torch.empty(nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, _dtype(q)),
+                                dtype=torch.uint8, device=q.device)
     nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, d,
                  scale, causal, dq, dk, dv, workspace, stream)
     return dq, dk, dv
