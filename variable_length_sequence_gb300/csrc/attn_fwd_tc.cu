@@ -15,14 +15,16 @@
 // into shared memory feeds two 128x128x128 QK^T and two PV products.  A
 // persistent grid of one CTA per SM takes items from an atomic counter.
 //
-// CTA roles (320 threads):
+// CTA roles (384 threads, three warpgroups):
 //   warps 0-3  softmax for head h0 (TMEM lanes 0-127, one query row each)
 //   warps 4-7  softmax for head h0+1
 //   warp 8     TMA producer and work fetch
 //   warp 9     TMEM allocation and the single MMA-issuing thread
-// The softmax reads each S row from TMEM twice (row maximum first, then
-// exponentials 32 columns at a time), which keeps it within the 168
-// registers a thread gets when 10 warps share the four SM sub-partitions.
+//   warps 10-11 idle (they complete the control warpgroup)
+// Registers: launched at 168 per thread (384 x 168 = 64512); inside its role
+// branch the control warpgroup gives back to 112 and each softmax warpgroup
+// grows to 192 (256 x 192 + 128 x 112 = 63488), enough to hold a whole
+// 128-column S row so S is read from TMEM once per tile.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
 // P (bf16, two per 32-bit cell) is written over the first 64 columns of S
 // and read from TMEM by the PV product.  The tensor core alternates
@@ -46,7 +48,8 @@ using namespace tc;
 
 constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int NSTAGE = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 192, kRegsControl = 112;
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr uint32_t kColBlockBytes = 128 * 64 * 2;        // 128 rows x 64 bf16 (one swizzle span)
 constexpr uint32_t kTileBytes = 2 * kColBlockBytes;      // 128 x 128 bf16
@@ -200,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
   const int n_items = hdr->n_items * n_pairs;
 
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -344,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv_count += it.n_kv;
       }
     }
-  } else if (warp < 8) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -388,34 +395,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a = lo - key0;
         const uint32_t span = (uint32_t)(hi - lo);
         const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + BN <= hi);
-        // pass 1: row maximum of the visible scores (two TMEM loads per wait)
-        float mt = -INFINITY;
+        // S row -> registers (one TMEM round trip); masked columns -> -inf
+        uint32_t sr[4][32];
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t sa[32], sb[32];
-          tmem_ld32(s_tm + (2 * c2) * 32, sa);
-          tmem_ld32(s_tm + (2 * c2 + 1) * 32, sb);
-          tmem_wait_ld();
-          if (full_w) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, sr[c]);
+        tmem_wait_ld();
+        if (!full_w) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              mt = fmaxf(mt, fmaxf(__uint_as_float(sa[i]), __uint_as_float(sb[i])));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int ca = 2 * c2 * 32 + i, cb = ca + 32;
-              const float xa = (uint32_t)(ca - a) < span ? __uint_as_float(sa[i]) : -INFINITY;
-              const float xb = (uint32_t)(cb - a) < span ? __uint_as_float(sb[i]) : -INFINITY;
-              mt = fmaxf(mt, fmaxf(xa, xb));
-            }
-          }
+              if ((uint32_t)(c * 32 + i - a) >= span) sr[c][i] = 0xff800000u;   // -inf
         }
+        // row maximum: 8 independent chains, then a small tree
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          mx[u] = fmaxf(__uint_as_float(sr[0][u]), __uint_as_float(sr[0][u + 8]));
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          mx[u] = fmaxf(mx[u], fmaxf(__uint_as_float(sr[0][u + 16]), __uint_as_float(sr[0][u + 24])));
+#pragma unroll
+        for (int c = 1; c < 4; ++c)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mx[u] = fmaxf(fmaxf(mx[u], fmaxf(__uint_as_float(sr[c][u]), __uint_as_float(sr[c][u + 8]))),
+                          fmaxf(__uint_as_float(sr[c][u + 16]), __uint_as_float(sr[c][u + 24])));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m, mt * sl2);
-        // Rescale the running output only when the maximum grew a lot.
+        // the running output is rescaled only when the maximum grew a lot
         const bool need = (m != -INFINITY) && (m_new > m + kRescaleThreshold);
+        const float corr = need ? ex2(m - m_new) : 1.f;
+        if (need || m == -INFINITY) m = m_new;
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        // p = 2^(s * scale * log2 e - m) from registers, bf16 P over S, row sum
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -mb));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -mb));
+            ls[i & 3] += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_tm + c * 16, pk);
+        }
+        l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (__any_sync(0xffffffffu, need)) {
-          const float corr = need ? ex2(m - m_new) : 1.f;
-          l *= corr;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t orow[32];
@@ -424,45 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * corr);
             tmem_st32(o_tm + c * 32, orow);
-          }
-          tmem_wait_st();
-        }
-        if (need || m == -INFINITY) m = m_new;
-        const float mb = (m == -INFINITY) ? 0.f : m;
-        // pass 2: p = 2^(s * scale * log2 e - m), row sum, bf16 P over S
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t sr[2][32];
-          tmem_ld32(s_tm + (2 * c2) * 32, sr[0]);
-          tmem_ld32(s_tm + (2 * c2 + 1) * 32, sr[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = 2 * c2 + h2;
-            uint32_t pk[16];
-            float ls = 0.f;
-            if (full_w) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[h2][2 * i]), sl2, -mb));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[h2][2 * i + 1]), sl2, -mb));
-                ls += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int col = c * 32 + 2 * i;
-                const float x0 = fmaf(__uint_as_float(sr[h2][2 * i]), sl2, -mb);
-                const float x1 = fmaf(__uint_as_float(sr[h2][2 * i + 1]), sl2, -mb);
-                const float p0 = ex2((uint32_t)(col - a) < span ? x0 : -INFINITY);
-                const float p1 = ex2((uint32_t)(col + 1 - a) < span ? x1 : -INFINITY);
-                ls += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-            }
-            l += ls;
-            tmem_st16(s_tm + c * 16, pk);
           }
         }
         tmem_wait_st();
