@@ -9,32 +9,37 @@
 // with delta = rowsum(dOut * out) and lse * log2(e) prepared by
 // bwd_delta_kernel in padded [Hq, Tp] rows.
 //
+// Both kernels use 128 x 128 x 128 products only, and issue them from two
+// threads (two tcgen05 streams): one M = 128 MMA stream keeps only about
+// half of an SM's tensor core busy, two independent streams keep most of it
+// busy.
+//
 // dK/dV kernel (key-stationary).  Work item: one 128-key tile of one KV
-// head.  It walks every 64-row query sub-tile that can see the keys, for
-// the query heads of the group taken two at a time; the two heads are two
-// chains that ping-pong on the tensor core (one chain's softmax overlaps
-// the other chain's MMAs) and accumulate into the same dV and dK in TMEM:
-//   S^T  = K Q^T      (M = 128 keys, N = 64 queries)   TMEM [128X, 128X+64)
-//   dP^T = V dOut^T                                     TMEM [128X+64, 128X+128)
-//   P^T and dS^T (bf16) are written back over S^T and dP^T by the softmax
-//   dV  += P^T dOut   (A = P^T from TMEM, B = dOut MN-major)   TMEM [256, 384)
-//   dK  += dS^T Q     (A = dS^T from TMEM, B = Q MN-major)     TMEM [384, 512)
-// dK and dV are written once per item, in bf16.
+// head; it walks every (query head of the group, 128-row query tile that
+// can see the keys) pair.  TMEM: S^T [0,128), dP^T [128,256), dV [256,384),
+// dK [384,512).  Stream 1 issues S^T = K Q^T and dP^T = V dOut^T; the
+// softmax warpgroups turn them into P^T (bf16, written back over S^T) and
+// dS^T (bf16, written to shared memory in a 128-byte-swizzled layout);
+// stream 2 issues dV += P^T dOut (A from TMEM) and dK += dS^T Q (A from
+// shared memory).  Stream 1 issues the next dP^T as soon as the softmax has
+// read dP^T and the next S^T as soon as dV has read P^T, so both streams
+// work at once.  dK and dV are written once per item, in bf16.
 //
-// dQ kernel (query-stationary, the shape of the forward).  Work item: one
-// 128-row query tile for a pair of query heads of one KV group; it walks the
-// 64-key sub-tiles the rows can see; the two heads ping-pong:
-//   S  = Q K^T        (M = 128 queries, N = 64 keys)   TMEM [256X, 256X+64)
-//   dP = dOut V^T                                       TMEM [256X+64, 256X+128)
-//   dS (bf16) is written back over S
-//   dQ += dS K        (A = dS from TMEM, B = K MN-major)   TMEM [256X+128, 256X+256)
-// dQ is scaled and written once per item, in bf16.
+// dQ kernel (query-stationary).  Work item: one 128-row query tile of one
+// query head; it walks the 128-key tiles its rows can see.  TMEM: S
+// double-buffered [0,128) and [128,256), dP [256,384), dQ [384,512).
+// Stream 1 issues S = Q K^T (into the free S buffer, while the softmax is
+// still on the other one) and dP = dOut V^T; the softmax writes
+// dS = P (dP - delta) (bf16) back over S; stream 2 issues dQ += dS K (A from
+// TMEM).  dQ is scaled and written once per item, in bf16.
 //
-// Roles (320 threads): warps 0-3 run chain / head 0, warps 4-7 chain / head
-// 1 (one TMEM lane each), warp 8 is the TMA producer and work fetcher, warp
-// 9 allocates TMEM and one of its threads issues every MMA.  Masking is one
-// unsigned compare per element against the row's (or key's) visible
-// interval, skipped for fully visible chunks.  All waits are bounded.
+// Roles (352 threads): warps 0-3 and 4-7 are the softmax / epilogue
+// warpgroups (one TMEM lane each; they split the 128 columns of each tile
+// in halves), warp 8 is the TMA producer and work fetcher, warp 9 allocates
+// TMEM and one of its threads issues stream 1, one thread of warp 10 issues
+// stream 2.  Masking is one unsigned compare per element against the row's
+// (or key's) visible interval, skipped for fully visible chunks.  All waits
+// are bounded.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -45,42 +50,40 @@ namespace {
 using namespace tc;
 
 constexpr int HD = 128;
-constexpr int SUB = kBwdSub;                          // 64
-constexpr int kThreads = 320;
-constexpr int kWarpProducer = 8, kWarpMma = 9;
-constexpr uint32_t kBlk128 = 128 * 64 * 2;            // 128 rows x 64 bf16 column block
-constexpr uint32_t kBlk64 = 64 * 64 * 2;              // 64 rows x 64 bf16 column block
-constexpr uint32_t kTile128 = 2 * kBlk128;            // 128 x 128 bf16
-constexpr uint32_t kTile64 = 2 * kBlk64;              // 64 x 128 bf16
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 8, kWarpMma1 = 9, kWarpMma2 = 10;
+constexpr uint32_t kBlk = 128 * 64 * 2;               // 128 rows x 64 bf16 column block
+constexpr uint32_t kTile = 2 * kBlk;                   // 128 x 128 bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kSmemLimit = 232448;
 
-// ---------------------------------------------------------------- MMA helpers
+constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);   // A, B K-major
+constexpr uint32_t kIdescKM = idesc_bf16_f32(128, 128, true, false);    // B MN-major
 
-// D = A B^T, A and B K-major (128-byte swizzle), K = 128 (head dim).
-// a_blk / b_blk: byte distance between the two 64-wide column blocks.
-__device__ __forceinline__ void mma_k128(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_blk,
-                                         uint32_t b_saddr, uint32_t b_blk, uint32_t idesc) {
+// D = A B^T, A and B K-major 128 x 128 tiles (128-byte swizzle), K = 128.
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
+                                       bool accumulate) {
   const uint64_t ad = smem_desc_sw128(a_saddr, 16, 1024);
   const uint64_t bd = smem_desc_sw128(b_saddr, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t ao = ((kk >> 2) * a_blk + (kk & 3) * 32) >> 4;
-    const uint32_t bo = ((kk >> 2) * b_blk + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, ad + ao, bd + bo, idesc, kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, ad + off, bd + off, kIdescKK, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
-// D (+)= A[tmem] B, K = 64 (4 steps of 16, 8 TMEM columns each); B is
-// MN-major with K along its rows (16 rows = 2048 B per step) and its two
-// 64-wide N blocks b_blk bytes apart.
-__device__ __forceinline__ void mma_tk64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
-                                         uint32_t b_blk, uint32_t idesc, bool accumulate) {
-  const uint64_t bd = smem_desc_sw128(b_saddr, b_blk, 1024);
+// D (+)= A B, A from TMEM (bf16 pairs; K = 128 in two 64-halves at columns
+// a_tmem + [0,32) and a_tmem + [64,96)), B MN-major in shared memory (K
+// along its rows, 16 rows = 2048 B per step; N blocks 16 KB apart).
+__device__ __forceinline__ void mma_t_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
+                                            bool accumulate) {
+  const uint64_t bd = smem_desc_sw128(b_saddr, kBlk, 1024);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, bd + ((kk * 2048) >> 4), idesc,
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t a_col = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+    mma_ts(d_tmem, a_tmem + a_col, bd + ((kk * 2048) >> 4), kIdescKM,
            (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
@@ -129,31 +132,29 @@ struct BwdArgs {
   __nv_bfloat16* dq;      // [T, Hq, d]
   __nv_bfloat16* dk;      // [T, Hkv, d]
   __nv_bfloat16* dv;
-  const int2* qtiles;     // per 128-row query tile: first/last 64-key sub-tile
+  const int2* qtiles;     // per 128-row query tile: first/last 128-key tile
   const int* qorder;
-  const int2* ktiles;     // per 128-key tile: first/last 64-row query sub-tile
+  const int2* ktiles;     // per 128-key tile: first/last 128-row query tile
   const int* korder;
 };
 
 // ================================================================ dK / dV
 
-constexpr int KV_NS = 2;
-
 struct KvItem {
-  int ktile, g, i_lo, n_q, steps, pad[3];   // steps = (G / 2) * n_q; -1 stops
+  int ktile, g, i_lo, n_q, steps, pad[3];   // steps = G * n_q; -1 stops
 };
 
 struct __align__(1024) SmemKV {
-  uint8_t k[kTile128];
-  uint8_t v[kTile128];
-  uint8_t q[2][KV_NS][kTile64];
-  uint8_t dout[2][KV_NS][kTile64];
-  float lse2[2][KV_NS][SUB];
-  float delta[2][KV_NS][SUB];
+  uint8_t k[kTile];
+  uint8_t v[kTile];
+  uint8_t q[2][kTile];
+  uint8_t dout[2][kTile];
+  uint8_t ds[kTile];            // dS^T, [q-block][key][64 q], 128-byte swizzle
+  float lse2[2][128];
+  float delta[2][128];
   uint64_t kv_full, kv_empty;
-  uint64_t qdo_full[2][KV_NS], qdo_empty[2][KV_NS];
-  uint64_t s_full[2], p_full[2];
-  uint64_t dkv_full, dkv_empty;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t s_full, p_full, dv_done, dk_done, dkv_full, dkv_empty;
   uint64_t item_full[2], item_empty[2];
   KvItem items[2];
   uint32_t tmem_base;
@@ -162,10 +163,10 @@ struct __align__(1024) SmemKV {
 static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q64,
-                            const __grid_constant__ CUtensorMap tm_do64,
-                            const __grid_constant__ CUtensorMap tm_k128,
-                            const __grid_constant__ CUtensorMap tm_v128, const BwdArgs a) {
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_do,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
@@ -178,30 +179,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    for (int x = 0; x < 2; ++x) {
-      for (int s = 0; s < KV_NS; ++s) {
-        mbar_init(&sm.qdo_full[x][s], 1);
-        mbar_init(&sm.qdo_empty[x][s], 1);
-      }
-      mbar_init(&sm.s_full[x], 1);
-      mbar_init(&sm.p_full[x], 128);
-      mbar_init(&sm.item_full[x], 1);
-      mbar_init(&sm.item_empty[x], 1 + 8);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.qdo_full[s], 1);
+      mbar_init(&sm.qdo_empty[s], 1);
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], 2 + 8);
     }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 256);
+    mbar_init(&sm.dv_done, 1);
+    mbar_init(&sm.dk_done, 1);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, 256);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma1) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
   if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&tm_q64);
-    tma_prefetch_desc(&tm_do64);
-    tma_prefetch_desc(&tm_k128);
-    tma_prefetch_desc(&tm_v128);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -210,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
   const int G = p.Hq / p.Hkv;
-  const int npair = G >> 1;
   const int64_t T = p.q_len;
   const int n_items = hdr->n_items2 * p.Hkv;
 
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           it.g = idx - (idx / p.Hkv) * p.Hkv;
           it.i_lo = tr.x;
           it.n_q = tr.y - tr.x + 1;
-          it.steps = npair * it.n_q;
+          it.steps = G * it.n_q;
         }
         const uint32_t slot = it_count & 1;
         if (it_count >= 2 &&
@@ -246,58 +246,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile128);
+        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
-          tma_load_2d(sm.k + cb * kBlk128, &tm_k128, &sm.kv_full, it.g * HD + cb * 64,
-                      it.ktile * 128);
-          tma_load_2d(sm.v + cb * kBlk128, &tm_v128, &sm.kv_full, it.g * HD + cb * 64,
-                      it.ktile * 128);
+          tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
+          tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
         }
         ++kv_count;
-        for (int n = 0; n < it.steps && ok; ++n) {
-          const int pair = n / it.n_q;
-          const int i = it.i_lo + (n - pair * it.n_q);
-          const uint32_t st = qc % KV_NS, use = qc / KV_NS;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!ok) continue;
-            const int h = it.g * G + 2 * pair + x;
-            if (use >= 1 &&
-                !mbar_wait(&sm.qdo_empty[x][st], (use - 1) & 1, abort_flag, hdr)) {
-              ok = false;
-              continue;
-            }
-            mbar_arrive_expect_tx(&sm.qdo_full[x][st], 2 * kTile64 + 2 * SUB * sizeof(float));
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-              tma_load_2d(sm.q[x][st] + cb * kBlk64, &tm_q64, &sm.qdo_full[x][st],
-                          h * HD + cb * 64, i * SUB);
-              tma_load_2d(sm.dout[x][st] + cb * kBlk64, &tm_do64, &sm.qdo_full[x][st],
-                          h * HD + cb * 64, i * SUB);
-            }
-            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * SUB;
-            bulk_load(sm.lse2[x][st], a.lse2 + row, SUB * sizeof(float), &sm.qdo_full[x][st]);
-            bulk_load(sm.delta[x][st], a.delta + row, SUB * sizeof(float), &sm.qdo_full[x][st]);
+        for (int n = 0; n < it.steps; ++n) {
+          const int hh = n / it.n_q;
+          const int h = it.g * G + hh;
+          const int i = it.i_lo + (n - hh * it.n_q);
+          const uint32_t st = qc & 1, use = qc >> 1;
+          if (use >= 1 && !mbar_wait(&sm.qdo_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
           }
-          if (ok) ++qc;
+          mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kTile + 2 * 128 * sizeof(float));
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+            tma_load_2d(sm.q[st] + cb * kBlk, &tm_q, &sm.qdo_full[st], h * HD + cb * 64, i * 128);
+            tma_load_2d(sm.dout[st] + cb * kBlk, &tm_do, &sm.qdo_full[st], h * HD + cb * 64,
+                        i * 128);
+          }
+          const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
+          bulk_load(sm.lse2[st], a.lse2 + row, 128 * sizeof(float), &sm.qdo_full[st]);
+          bulk_load(sm.delta[st], a.delta + row, 128 * sizeof(float), &sm.qdo_full[st]);
+          ++qc;
         }
       }
       if (!ok) {
         // abort: every copy issued so far completes on its stage barrier
         if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
-        for (uint32_t j = (qc > KV_NS ? qc - KV_NS : 0); j <= qc; ++j)
-          for (int x = 0; x < 2; ++x) drain_wait(&sm.qdo_full[x][j % KV_NS], (j / KV_NS) & 1);
+        for (uint32_t j = (qc > 2 ? qc - 2 : 0); j < qc; ++j)
+          drain_wait(&sm.qdo_full[j & 1], (j >> 1) & 1);
       }
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMma1) {
+    // ------------------------------------------------------------ stream 1: S^T, dP^T
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, SUB, false, false);   // S^T, dP^T
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, true, false);   // dV, dK
       const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v);
       uint32_t it_count = 0, items_done = 0, qc = 0;
-      uint32_t pc[2] = {0, 0};
       bool ok = true;
       while (ok) {
         const uint32_t slot = it_count & 1;
@@ -307,72 +296,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it_count;
         if (it.steps < 0) break;
         if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
-        for (int n = 0; n < it.steps && ok; ++n) {
-          const uint32_t st = qc % KV_NS;
-          if (n == 0) {
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              if (!ok) continue;
-              if (!mbar_wait(&sm.qdo_full[x][st], (qc / KV_NS) & 1, abort_flag, hdr)) {
-                ok = false;
-                continue;
-              }
-              tc_fence_after();
-              mma_k128(tmem + 128 * x, k_s, kBlk128, smem_u32(sm.q[x][st]), kBlk64, idesc_s);
-              mma_k128(tmem + 128 * x + 64, v_s, kBlk128, smem_u32(sm.dout[x][st]), kBlk64,
-                       idesc_s);
-              mma_commit(&sm.s_full[x]);
-            }
-            if (!ok) break;
+        for (int n = 0; n < it.steps; ++n) {
+          const uint32_t st = qc & 1;
+          if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+          // dP^T region is free once the softmax read the previous dP^T
+          if (qc >= 1 && !mbar_wait(&sm.p_full, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+          tc_fence_after();
+          mma_kk(tmem + 128, v_s, smem_u32(sm.dout[st]), false);       // dP^T = V dOut^T
+          // S^T region holds the previous P^T until dV has read it
+          if (qc >= 1 && !mbar_wait(&sm.dv_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+          tc_fence_after();
+          mma_kk(tmem + 0, k_s, smem_u32(sm.q[st]), false);            // S^T = K Q^T
+          mma_commit(&sm.s_full);
+          ++qc;
+        }
+        if (!ok) break;
+        mma_commit(&sm.kv_empty);
+        ++items_done;
+      }
+    }
+  } else if (warp == kWarpMma2) {
+    // ------------------------------------------------------------ stream 2: dV, dK
+    if (lane == 0) {
+      const uint32_t ds_s = smem_u32(sm.ds);
+      uint32_t it_count = 0, items_done = 0, qc = 0;
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it_count & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        const KvItem it = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++it_count;
+        if (it.steps < 0) break;
+        for (int n = 0; n < it.steps; ++n) {
+          const uint32_t st = qc & 1;
+          if (!mbar_wait(&sm.p_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+          if (n == 0 && items_done > 0 &&
+              !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const bool acc = n > 0;
+          mma_t_split(tmem + 256, tmem + 0, smem_u32(sm.dout[st]), acc);   // dV += P^T dOut
+          mma_commit(&sm.dv_done);
+          {
+            // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
+            const uint64_t ad = smem_desc_sw128(ds_s, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(smem_u32(sm.q[st]), kBlk, 1024);
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!ok) continue;
-            if (!mbar_wait(&sm.p_full[x], pc[x] & 1, abort_flag, hdr)) { ok = false; continue; }
-            ++pc[x];
-            const bool first = (n == 0 && x == 0);
-            if (first && items_done > 0 &&
-                !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
-              ok = false;
-              continue;
-            }
-            tc_fence_after();
-            mma_tk64(tmem + 256, tmem + 128 * x, smem_u32(sm.dout[x][st]), kBlk64, idesc_acc,
-                     !first);
-            mma_tk64(tmem + 384, tmem + 128 * x + 64, smem_u32(sm.q[x][st]), kBlk64, idesc_acc,
-                     !first);
-            mma_commit(&sm.qdo_empty[x][st]);
-            if (n + 1 < it.steps) {
-              const uint32_t stn = (qc + 1) % KV_NS;
-              if (!mbar_wait(&sm.qdo_full[x][stn], ((qc + 1) / KV_NS) & 1, abort_flag, hdr)) {
-                ok = false;
-                continue;
-              }
-              tc_fence_after();
-              mma_k128(tmem + 128 * x, k_s, kBlk128, smem_u32(sm.q[x][stn]), kBlk64, idesc_s);
-              mma_k128(tmem + 128 * x + 64, v_s, kBlk128, smem_u32(sm.dout[x][stn]), kBlk64,
-                       idesc_s);
-              mma_commit(&sm.s_full[x]);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t aoff = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+              mma_ss(tmem + 384, ad + aoff, bd + ((kk * 2048) >> 4), kIdescKM,
+                     (acc || kk > 0) ? 1u : 0u);
             }
           }
-          if (ok) ++qc;
+          mma_commit(&sm.dk_done);
+          mma_commit(&sm.qdo_empty[st]);
+          ++qc;
         }
         if (!ok) break;
         mma_commit(&sm.dkv_full);
-        mma_commit(&sm.kv_empty);
         ++items_done;
       }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + dK/dV epilogue
-    const int x = warp >> 2;
+    const int wg = warp >> 2;                             // query columns 64 wg .. 64 wg + 63
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                          // TMEM lane = key row
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + 128 * x;
-    const uint32_t dp_tm = s_tm + 64;
     const float sl2 = p.scale * kLog2e;
-    uint32_t it_count = 0, items_done = 0, qc = 0, sc = 0;
+    const uint32_t ds_row = smem_u32(sm.ds) + wg * kBlk + r * 128;
+    uint32_t it_count = 0, items_done = 0, qc = 0;
     bool ok = true;
     while (ok) {
       const uint32_t slot = it_count & 1;
@@ -389,60 +385,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         qlo = p.causal ? key : (int64_t)__ldg(p.cu + b);
         qhi = (int64_t)__ldg(p.cu + b + 1);
       }
-      for (int n = 0; n < it.steps && ok; ++n) {
-        const int pair = n / it.n_q;
-        const int64_t q0 = (int64_t)(it.i_lo + (n - pair * it.n_q)) * SUB;
-        const uint32_t st = qc % KV_NS;
-        if (!mbar_wait(&sm.qdo_full[x][st], (qc / KV_NS) & 1, abort_flag, hdr)) { ok = false; break; }
-        if (!mbar_wait(&sm.s_full[x], sc & 1, abort_flag, hdr)) { ok = false; break; }
-        ++sc;
+      for (int n = 0; n < it.steps; ++n) {
+        const int hh = n / it.n_q;
+        const int64_t q0 = (int64_t)(it.i_lo + (n - hh * it.n_q)) * 128;
+        const uint32_t st = qc & 1;
+        if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+        // the dS^T buffer is free once dK has read the previous one
+        if (qc >= 1 && !mbar_wait(&sm.dk_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
-        const float* lse2s = sm.lse2[x][st];
-        const float* deltas = sm.delta[x][st];
+        const float* lse2s = sm.lse2[st];
+        const float* deltas = sm.delta[st];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          const int col0 = wg * 64 + c * 32;
           uint32_t s[32], dp[32];
-          tmem_ld32(s_tm + c * 32, s);
-          tmem_ld32(dp_tm + c * 32, dp);
+          tmem_ld32(tmem + lane_base + 0 + col0, s);
+          tmem_ld32(tmem + lane_base + 128 + col0, dp);
           tmem_wait_ld();
-          const int64_t qg0 = q0 + c * 32;
+          const int64_t qg0 = q0 + col0;
           const int loc = (int)min(max(qlo - qg0, (int64_t)0), (int64_t)32);
           const int hic = (int)min(max(qhi - qg0, (int64_t)0), (int64_t)32);
           const uint32_t span = (uint32_t)(hic - loc);
           const bool full_w = __all_sync(0xffffffffu, loc == 0 && hic == 32);
           uint32_t pk[16], dk[16];
+          float lv[32], dv[32];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2s + col0 + 4 * e4);
+            const float4 d4 = *reinterpret_cast<const float4*>(deltas + col0 + 4 * e4);
+            lv[4 * e4] = l4.x; lv[4 * e4 + 1] = l4.y; lv[4 * e4 + 2] = l4.z; lv[4 * e4 + 3] = l4.w;
+            dv[4 * e4] = d4.x; dv[4 * e4 + 1] = d4.y; dv[4 * e4 + 2] = d4.z; dv[4 * e4 + 3] = d4.w;
+          }
           if (full_w) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int cc = c * 32 + 2 * e;
-              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]));
-              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2s[cc + 1]));
+              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lv[2 * e]));
+              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lv[2 * e + 1]));
               pk[e] = pack_bf16x2(p0, p1);
-              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - deltas[cc]),
-                                  p1 * (__uint_as_float(dp[2 * e + 1]) - deltas[cc + 1]));
+              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - dv[2 * e]),
+                                  p1 * (__uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1]));
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int cc = c * 32 + 2 * e;
               const bool v0 = (uint32_t)(2 * e - loc) < span;
               const bool v1 = (uint32_t)(2 * e + 1 - loc) < span;
-              const float x0 = fmaf(__uint_as_float(s[2 * e]), sl2, -lse2s[cc]);
-              const float x1 = fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2s[cc + 1]);
-              const float p0 = ex2(v0 ? x0 : -INFINITY);
-              const float p1 = ex2(v1 ? x1 : -INFINITY);
-              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - deltas[cc] : 0.f;
-              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - deltas[cc + 1] : 0.f;
+              const float p0 =
+                  ex2(v0 ? fmaf(__uint_as_float(s[2 * e]), sl2, -lv[2 * e]) : -INFINITY);
+              const float p1 =
+                  ex2(v1 ? fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lv[2 * e + 1]) : -INFINITY);
+              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - dv[2 * e] : 0.f;
+              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1] : 0.f;
               pk[e] = pack_bf16x2(p0, p1);
               dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
             }
           }
-          tmem_st16(s_tm + c * 16, pk);       // P^T over S^T (columns already read)
-          tmem_st16(dp_tm + c * 16, dk);      // dS^T over dP^T
+          tmem_st16(tmem + lane_base + wg * 64 + c * 16, pk);   // P^T over read S^T columns
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int chunk = c * 4 + u;                        // 8 query columns per 16 bytes
+            st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
+                         dk[4 * u + 2], dk[4 * u + 3]);
+          }
         }
         tmem_wait_st();
+        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.p_full[x]);
+        mbar_arrive(&sm.p_full);
         ++qc;
       }
       if (!ok) break;
@@ -450,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sm.dkv_full, items_done & 1, abort_flag, hdr)) break;
       tc_fence_after();
       {
-        const uint32_t col = x == 0 ? 256u : 384u;
-        const float scale = x == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = (x == 0 ? a.dv : a.dk) + (key * p.Hkv + it.g) * HD;
+        const uint32_t col = wg == 0 ? 256u : 384u;
+        const float scale = wg == 0 ? 1.f : p.scale;
+        __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + (key * p.Hkv + it.g) * HD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
@@ -469,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -477,20 +487,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ dQ
 
-constexpr int Q_NS = 3;
+constexpr int Q_NS = 2;
 
 struct QItem {
-  int qtile, h0, g, j_lo, n_kv, pad[3];     // n_kv 64-key sub-tiles; -1 stops
+  int qtile, h, g, j_lo, n_kv, pad[3];     // n_kv 128-key tiles; -1 stops
 };
 
 struct __align__(1024) SmemQ {
-  uint8_t q[2][kTile128];
-  uint8_t dout[2][kTile128];
-  uint8_t k[Q_NS][kTile64];
-  uint8_t v[Q_NS][kTile64];
-  uint64_t qdo_full, qdo_empty;
+  uint8_t q[kTile];
+  uint8_t dout[kTile];
+  uint8_t k[Q_NS][kTile];
+  uint8_t v[Q_NS][kTile];
+  uint64_t q_full, q_empty;
   uint64_t k_full[Q_NS], k_empty[Q_NS], v_full[Q_NS], v_empty[Q_NS];
-  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t s_full, p_full[2], dq_done[2], o_full, epi_done;
   uint64_t item_full[2], item_empty[2];
   QItem items[2];
   uint32_t tmem_base;
@@ -499,10 +509,10 @@ struct __align__(1024) SmemQ {
 static_assert(sizeof(SmemQ) <= kSmemLimit, "dQ tile set exceeds shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q128,
-                          const __grid_constant__ CUtensorMap tm_do128,
-                          const __grid_constant__ CUtensorMap tm_k64,
-                          const __grid_constant__ CUtensorMap tm_v64, const BwdArgs a) {
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_do,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
@@ -513,33 +523,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.qdo_full, 1);
-    mbar_init(&sm.qdo_empty, 1);
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < Q_NS; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 2);          // S (stream 1) and dQ (stream 2) read K
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&sm.s_full[x], 1);
-      mbar_init(&sm.p_full[x], 128);
-      mbar_init(&sm.o_full[x], 1);
-      mbar_init(&sm.item_full[x], 1);
-      mbar_init(&sm.item_empty[x], 1 + 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.p_full[b], 256);
+      mbar_init(&sm.dq_done[b], 1);
+      mbar_init(&sm.item_full[b], 1);
+      mbar_init(&sm.item_empty[b], 2 + 8);
     }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.epi_done, 256);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma1) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
   if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&tm_q128);
-    tma_prefetch_desc(&tm_do128);
-    tma_prefetch_desc(&tm_k64);
-    tma_prefetch_desc(&tm_v64);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -547,10 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
-  const int n_pairs = p.Hq >> 1;
   const int G = p.Hq / p.Hkv;
   const int64_t T = p.q_len;
-  const int n_items = hdr->n_items * n_pairs;
+  const int n_items = hdr->n_items * p.Hq;
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -560,14 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok) {
         const int idx = atomicAdd(&hdr->counter, 1);
         QItem it;
-        it.qtile = 0; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
+        it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
         if (idx < n_items) {
-          const int qt = a.qorder[idx / n_pairs];
-          const int pair = idx - (idx / n_pairs) * n_pairs;
+          const int qt = a.qorder[idx / p.Hq];
           const int2 tr = a.qtiles[qt];
           it.qtile = qt;
-          it.h0 = 2 * pair;
-          it.g = (2 * pair) / G;
+          it.h = idx - (idx / p.Hq) * p.Hq;
+          it.g = it.h / G;
           it.j_lo = tr.x;
           it.n_kv = tr.y - tr.x + 1;
         }
@@ -584,59 +594,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it.n_kv < 0) break;
           continue;
         }
-        if (q_count >= 1 && !mbar_wait(&sm.qdo_empty, (q_count - 1) & 1, abort_flag, hdr)) {
+        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, abort_flag, hdr)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.qdo_full, 4 * kTile128);
+        mbar_arrive_expect_tx(&sm.q_full, 2 * kTile);
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            tma_load_2d(sm.q[x] + cb * kBlk128, &tm_q128, &sm.qdo_full, (it.h0 + x) * HD + cb * 64,
-                        it.qtile * 128);
-            tma_load_2d(sm.dout[x] + cb * kBlk128, &tm_do128, &sm.qdo_full,
-                        (it.h0 + x) * HD + cb * 64, it.qtile * 128);
-          }
+        for (int cb = 0; cb < 2; ++cb) {
+          tma_load_2d(sm.q + cb * kBlk, &tm_q, &sm.q_full, it.h * HD + cb * 64, it.qtile * 128);
+          tma_load_2d(sm.dout + cb * kBlk, &tm_do, &sm.q_full, it.h * HD + cb * 64,
+                      it.qtile * 128);
+        }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = kv_count % Q_NS, use = kv_count / Q_NS;
-          const int key0 = (it.j_lo + jj) * SUB;
+          const int key0 = (it.j_lo + jj) * 128;
           if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.k_full[st], kTile64);
+          mbar_arrive_expect_tx(&sm.k_full[st], kTile);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.k[st] + cb * kBlk64, &tm_k64, &sm.k_full[st], it.g * HD + cb * 64, key0);
+            tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.k_full[st], it.g * HD + cb * 64, key0);
           if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
             drain_wait(&sm.k_full[st], use & 1);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.v_full[st], kTile64);
+          mbar_arrive_expect_tx(&sm.v_full[st], kTile);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.v[st] + cb * kBlk64, &tm_v64, &sm.v_full[st], it.g * HD + cb * 64, key0);
+            tma_load_2d(sm.v[st] + cb * kBlk, &tm_v, &sm.v_full[st], it.g * HD + cb * 64, key0);
           ++kv_count;
         }
       }
       if (!ok) {
-        if (q_count >= 1) drain_wait(&sm.qdo_full, (q_count - 1) & 1);
+        if (q_count >= 1) drain_wait(&sm.q_full, (q_count - 1) & 1);
         for (uint32_t j = (kv_count > Q_NS ? kv_count - Q_NS : 0); j < kv_count; ++j) {
           drain_wait(&sm.k_full[j % Q_NS], (j / Q_NS) & 1);
           drain_wait(&sm.v_full[j % Q_NS], (j / Q_NS) & 1);
         }
       }
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMma1) {
+    // ------------------------------------------------------------ stream 1: S, dP
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, SUB, false, false);   // S, dP
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, false);    // dQ
-      uint32_t it_count = 0, q_count = 0, kv_count = 0;
-      uint32_t pc[2] = {0, 0};
+      const uint32_t q_s = smem_u32(sm.q), do_s = smem_u32(sm.dout);
+      uint32_t it_count = 0, q_count = 0, jc = 0;
       bool ok = true;
       while (ok) {
         const uint32_t slot = it_count & 1;
@@ -646,75 +651,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++it_count;
         if (it.n_kv < 0) break;
         if (it.n_kv == 0) continue;
-        if (!mbar_wait(&sm.qdo_full, q_count & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.q_full, q_count & 1, abort_flag, hdr)) break;
         ++q_count;
-        {
-          const uint32_t st = kv_count % Q_NS, use = kv_count / Q_NS;
-          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) break;
-          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) break;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = jc % Q_NS, use = jc / Q_NS, b = jc & 1;
+          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+          // S buffer b is free once dQ has read the dS written over it two tiles ago
+          if (jc >= 2 && !mbar_wait(&sm.dq_done[b], ((jc - 2) >> 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            mma_k128(tmem + 256 * x, smem_u32(sm.q[x]), kBlk128, smem_u32(sm.k[st]), kBlk64,
-                     idesc_s);
-            mma_k128(tmem + 256 * x + 64, smem_u32(sm.dout[x]), kBlk128, smem_u32(sm.v[st]),
-                     kBlk64, idesc_s);
-            mma_commit(&sm.s_full[x]);
+          mma_kk(tmem + 128 * b, q_s, smem_u32(sm.k[st]), false);        // S = Q K^T
+          mma_commit(&sm.k_empty[st]);
+          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+          // dP region is free once the softmax read the previous dP
+          if (jc >= 1 &&
+              !mbar_wait(&sm.p_full[(jc - 1) & 1], ((jc - 1) >> 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          mma_kk(tmem + 256, do_s, smem_u32(sm.v[st]), false);           // dP = dOut V^T
+          mma_commit(&sm.s_full);
           mma_commit(&sm.v_empty[st]);
-          if (it.n_kv == 1) mma_commit(&sm.qdo_empty);
+          if (jj + 1 == it.n_kv) mma_commit(&sm.q_empty);
+          ++jc;
         }
-        for (int jj = 0; jj < it.n_kv && ok; ++jj) {
-          const uint32_t st = (kv_count + jj) % Q_NS;
-          const bool has_next = jj + 1 < it.n_kv;
-          const uint32_t stn = (kv_count + jj + 1) % Q_NS, usen = (kv_count + jj + 1) / Q_NS;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!ok) continue;
-            if (!mbar_wait(&sm.p_full[x], pc[x] & 1, abort_flag, hdr)) { ok = false; continue; }
-            ++pc[x];
-            tc_fence_after();
-            mma_tk64(tmem + 256 * x + 128, tmem + 256 * x, smem_u32(sm.k[st]), kBlk64, idesc_dq,
-                     jj > 0);
-            if (x == 1) mma_commit(&sm.k_empty[st]);
-            if (!has_next) {
-              mma_commit(&sm.o_full[x]);
-              continue;
-            }
-            if (x == 0) {
-              if (!mbar_wait(&sm.k_full[stn], usen & 1, abort_flag, hdr) ||
-                  !mbar_wait(&sm.v_full[stn], usen & 1, abort_flag, hdr)) {
-                ok = false;
-                continue;
-              }
-              tc_fence_after();
-            }
-            mma_k128(tmem + 256 * x, smem_u32(sm.q[x]), kBlk128, smem_u32(sm.k[stn]), kBlk64,
-                     idesc_s);
-            mma_k128(tmem + 256 * x + 64, smem_u32(sm.dout[x]), kBlk128, smem_u32(sm.v[stn]),
-                     kBlk64, idesc_s);
-            mma_commit(&sm.s_full[x]);
-            if (x == 1) {
-              mma_commit(&sm.v_empty[stn]);
-              if (jj + 2 == it.n_kv) mma_commit(&sm.qdo_empty);
-            }
+      }
+    }
+  } else if (warp == kWarpMma2) {
+    // ------------------------------------------------------------ stream 2: dQ
+    if (lane == 0) {
+      uint32_t it_count = 0, items_done = 0, jc = 0;
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it_count & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        const QItem it = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++it_count;
+        if (it.n_kv < 0) break;
+        if (it.n_kv == 0) continue;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = jc % Q_NS, b = jc & 1;
+          if (!mbar_wait(&sm.p_full[b], (jc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+          if (jj == 0 && items_done > 0 &&
+              !mbar_wait(&sm.epi_done, (items_done - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          mma_t_split(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]), jj > 0);   // dQ += dS K
+          mma_commit(&sm.dq_done[b]);
+          mma_commit(&sm.k_empty[st]);
+          ++jc;
         }
         if (!ok) break;
-        kv_count += it.n_kv;
+        mma_commit(&sm.o_full);
+        ++items_done;
       }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + dQ epilogue
-    const int x = warp >> 2;
+    const int wg = warp >> 2;                             // key columns 64 wg .. 64 wg + 63
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                          // TMEM lane = query row
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t s_tm = tmem + lane_base + 256 * x;
-    const uint32_t dp_tm = s_tm + 64;
-    const uint32_t dq_tm = s_tm + 128;
     const float sl2 = p.scale * kLog2e;
-    uint32_t it_count = 0, sc = 0, oc = 0;
+    uint32_t it_count = 0, items_done = 0, jc = 0;
     bool ok = true;
     while (ok) {
       const uint32_t slot = it_count & 1;
@@ -724,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.n_kv < 0) break;
-      const int h = it.h0 + x;
+      const int h = it.h;
       const int64_t row = (int64_t)it.qtile * 128 + r;
       const bool valid = row < T;
       int lo = 0, hi = 0;                                    // visible keys [lo, hi)
@@ -736,14 +741,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse2r = __ldg(a.lse2 + (int64_t)h * a.Tp + row);
         deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
       }
-      for (int jj = 0; jj < it.n_kv && ok; ++jj) {
-        if (!mbar_wait(&sm.s_full[x], sc & 1, abort_flag, hdr)) { ok = false; break; }
-        ++sc;
+      for (int jj = 0; jj < it.n_kv; ++jj) {
+        const uint32_t b = jc & 1;
+        if (!mbar_wait(&sm.s_full, jc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
-        const int key0 = (it.j_lo + jj) * SUB;
+        const int key0 = (it.j_lo + jj) * 128 + wg * 64;
         const int aa = lo - key0;
         const uint32_t span = (uint32_t)(hi - lo);
-        const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + SUB <= hi);
+        const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + 64 <= hi);
+        const uint32_t s_tm = tmem + lane_base + 128 * b + wg * 64;
+        const uint32_t dp_tm = tmem + lane_base + 256 + wg * 64;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t s[32], dp[32];
@@ -777,35 +784,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&sm.p_full[x]);
+        mbar_arrive(&sm.p_full[b]);
+        ++jc;
       }
       if (!ok) break;
-      // epilogue: dQ = scale * accumulated dS K, written once in bf16
-      __nv_bfloat16* dst = a.dq + (row * p.Hq + h) * HD;
+      // epilogue: dQ = scale * accumulated dS K, written once in bf16 (my half of d)
+      __nv_bfloat16* dst = a.dq + (row * p.Hq + h) * HD + wg * 64;
       if (it.n_kv > 0) {
-        if (!mbar_wait(&sm.o_full[x], oc & 1, abort_flag, hdr)) break;
-        ++oc;
+        if (!mbar_wait(&sm.o_full, items_done & 1, abort_flag, hdr)) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(dq_tm + c * 32, v);
+          tmem_ld32(tmem + lane_base + 384 + wg * 64 + c * 32, v);
           tmem_wait_ld();
           if (valid) store_row32_bf16(dst + c * 32, v, p.scale);
         }
+        tc_fence_before();
+        mbar_arrive(&sm.epi_done);
+        ++items_done;
       } else if (valid) {
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
+        for (int c = 0; c < 2; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -828,13 +838,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows, cols] bf16 row-major; box = 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+// [rows, cols] bf16 row-major; box = 64 columns x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -844,19 +854,17 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint
 }  // namespace
 
 bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
-  return io_dtype == NSP_BF16 && d == HD && Hkv > 0 && Hq % Hkv == 0 && (Hq / Hkv) % 2 == 0;
+  return io_dtype == NSP_BF16 && d == HD && Hkv > 0 && Hq % Hkv == 0;
 }
 
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
                                const BwdWsLayout& L, char* ws, cudaStream_t s) {
   const int64_t T = p.q_len;
-  CUtensorMap mq128, mdo128, mk128, mv128, mq64, mdo64, mk64, mv64;
+  CUtensorMap mq, mdo, mk, mv;
   const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
-  if (!make_map(&mq128, p.q, T, qc, 128) || !make_map(&mdo128, dout, T, qc, 128) ||
-      !make_map(&mk128, p.k, T, kc, 128) || !make_map(&mv128, p.v, T, kc, 128) ||
-      !make_map(&mq64, p.q, T, qc, 64) || !make_map(&mdo64, dout, T, qc, 64) ||
-      !make_map(&mk64, p.k, T, kc, 64) || !make_map(&mv64, p.v, T, kc, 64))
+  if (!make_map(&mq, p.q, T, qc) || !make_map(&mdo, dout, T, qc) ||
+      !make_map(&mk, p.k, T, kc) || !make_map(&mv, p.v, T, kc))
     return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
@@ -884,11 +892,11 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)q_bytes);
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kv_bytes, s>>>(mq64, mdo64, mk128, mv128, a);
+  attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kv_bytes, s>>>(mq, mdo, mk, mv, a);
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<<<grid, kThreads, q_bytes, s>>>(mq128, mdo128, mk64, mv64, a);
+  attn_bwd_dq_tc_kernel<<<grid, kThreads, q_bytes, s>>>(mq, mdo, mk, mv, a);
   count_launches(1);
   return cudaGetLastError();
 }

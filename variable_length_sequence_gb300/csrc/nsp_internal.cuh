@@ -48,12 +48,12 @@ inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
   return L;
 }
 
-// Backward workspace: header; schedule of 128-row query tiles listing 64-key
-// sub-tiles (dQ kernel) and of 128-key tiles listing 64-row query sub-tiles
+// Backward workspace: header; schedule of 128-row query tiles listing
+// 128-key tiles (dQ kernel) and of 128-key tiles listing 128-row query tiles
 // (dK/dV kernel); delta and lse * log2(e) [Hq, Tp] f32 (rows padded to whole
 // 128-row tiles, padding zeroed); and, for the CUDA-core path only, a
 // float32 dq accumulator [T, Hq, d].
-constexpr int kBwdSub = 64;        // sub-tile of the backward kernels
+constexpr int kBwdSub = 128;       // tile granularity listed by the backward schedules
 
 struct BwdWsLayout {
   size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_sub + 2]
