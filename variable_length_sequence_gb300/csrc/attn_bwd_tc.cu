@@ -6,7 +6,7 @@
 // lse instead of storing them (the recomputation NSP Sec. 2.3 discusses):
 //   P = exp(scale Q K^T - lse),  dP = dOut V^T,  dS = P (dP - delta),
 //   dV = P^T dOut,  dK = scale dS^T Q,  dQ = scale dS K,
-// with delta = rowsum(dOut * out) and lse * log2(e) prepared by
+// with delta = rowsum(dOut * out) and -lse * log2(e) prepared by
 // bwd_delta_kernel in padded [Hq, Tp] rows.
 //
 // Both kernels use 128 x 128 x 128 products only, and issue them from two
@@ -16,28 +16,36 @@
 //
 // dK/dV kernel (key-stationary).  Work item: one 128-key tile of one KV
 // head; it walks every (query head of the group, 128-row query tile that
-// can see the keys) pair.  TMEM: S^T [0,128), dP^T [128,256), dV [256,384),
-// dK [384,512).  Stream 1 issues S^T = K Q^T and dP^T = V dOut^T; the
-// softmax warpgroups turn them into P^T (bf16, written back over S^T) and
-// dS^T (bf16, written to shared memory in a 128-byte-swizzled layout);
-// stream 2 issues dV += P^T dOut (A from TMEM) and dK += dS^T Q (A from
-// shared memory).  Stream 1 issues the next dP^T as soon as the softmax has
-// read dP^T and the next S^T as soon as dV has read P^T, so both streams
-// work at once.  dK and dV are written once per item, in bf16.
+// can see the keys) pair.  TMEM: two 128-column score regions [0,256) that
+// swap roles every step (step qc puts S^T in region qc & 1 and dP^T in the
+// other), dV [256,384), dK [384,512).  Stream 1 issues S^T = K Q^T and
+// dP^T = V dOut^T; the softmax warpgroups read S^T, write P^T (bf16) back
+// over it, then read dP^T and write dS^T (bf16) to shared memory in a
+// 128-byte-swizzled layout; stream 2 issues dV += P^T dOut (A from TMEM) and
+// dK += dS^T Q (A from shared memory).  The next S^T goes into the region
+// the softmax has just read dP^T from, and the next dP^T into the region
+// whose P^T dV has consumed, so stream 1 works on step qc + 1 while the
+// softmax and stream 2 are on step qc.  dK and dV are written once per item,
+// in bf16.
 //
 // dQ kernel (query-stationary).  Work item: one 128-row query tile of one
 // query head; it walks the 128-key tiles its rows can see.  TMEM: S
 // double-buffered [0,128) and [128,256), dP [256,384), dQ [384,512).
 // Stream 1 issues S = Q K^T (into the free S buffer, while the softmax is
-// still on the other one) and dP = dOut V^T; the softmax writes
-// dS = P (dP - delta) (bf16) back over S; stream 2 issues dQ += dS K (A from
-// TMEM).  dQ is scaled and written once per item, in bf16.
+// still on the other one); dP = dOut V^T is issued by stream 1 for even and
+// by stream 2 for odd tiles of an item, so that both streams carry three
+// products per two tiles; the softmax frees dP as soon as it has read it and
+// writes dS = P (dP - delta) (bf16) back over S; stream 2 issues
+// dQ += dS K (A from TMEM).  K tiles have three shared-memory stages (they
+// are read until dQ of their tile is done), V tiles two.  dQ is scaled and
+// written once per item, in bf16.
 //
-// Roles (352 threads): warps 0-3 and 4-7 are the softmax / epilogue
-// warpgroups (one TMEM lane each; they split the 128 columns of each tile
-// in halves), warp 8 is the TMA producer and work fetcher, warp 9 allocates
-// TMEM and one of its threads issues stream 1, one thread of warp 10 issues
-// stream 2.  Masking is one unsigned compare per element against the row's
+// Roles: warps 0-3 and 4-7 are the softmax / epilogue warpgroups (one TMEM
+// lane each; they split the 128 columns of each tile in halves), warp 8 is
+// the TMA producer and work fetcher, warp 9 allocates TMEM and one of its
+// threads issues stream 1, one thread of warp 10 issues stream 2.  The dK/dV
+// kernel adds an idle warp 11 so that its control warpgroup can hand
+// registers to the softmax warpgroups (setmaxnreg).  Masking is one unsigned compare per element against the row's
 // (or key's) visible interval, skipped for fully visible chunks.  All waits
 // are bounded.
 #include <cudaTypedefs.h>
@@ -50,7 +58,11 @@ namespace {
 using namespace tc;
 
 constexpr int HD = 128;
-constexpr int kThreads = 352;
+constexpr int kThreads = 352;                        // dQ kernel
+constexpr int kKvThreads = 640;                      // dK/dV kernel: 16 softmax warps + 4
+constexpr int kKvSoftmaxWarps = 16;
+constexpr int kKvWarpProducer = 16, kKvWarpMma1 = 17, kKvWarpMma2 = 18;   // warp 19 idle
+constexpr int kKvRegsControl = 64, kKvRegsSoftmax = 104;   // 128 x 64 + 512 x 104 = 640 x 96
 constexpr int kWarpProducer = 8, kWarpMma1 = 9, kWarpMma2 = 10;
 constexpr uint32_t kBlk = 128 * 64 * 2;               // 128 rows x 64 bf16 column block
 constexpr uint32_t kTile = 2 * kBlk;                   // 128 x 128 bf16
@@ -72,15 +84,19 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32
   }
 }
 
-// D (+)= A B, A from TMEM (bf16 pairs; K = 128 in two 64-halves at columns
-// a_tmem + [0,32) and a_tmem + [64,96)), B MN-major in shared memory (K
-// along its rows, 16 rows = 2048 B per step; N blocks 16 KB apart).
+// D (+)= A B, A from TMEM, B MN-major in shared memory (K along its rows,
+// 16 rows = 2048 B per step; N blocks 16 KB apart).  A holds bf16 pairs
+// written by the softmax warps in groups of QPG K-columns: group j sits at
+// TMEM columns a_tmem + j QPG + [0, QPG / 2), so K-step kk (16 columns, 8
+// TMEM columns) starts at (kk / (QPG / 16)) QPG + (kk % (QPG / 16)) 8.
+template <int QPG>
 __device__ __forceinline__ void mma_t_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
                                             bool accumulate) {
+  constexpr int kSteps = QPG / 16;
   const uint64_t bd = smem_desc_sw128(b_saddr, kBlk, 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t a_col = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+    const uint32_t a_col = (kk / kSteps) * QPG + (kk % kSteps) * 8;
     mma_ts(d_tmem, a_tmem + a_col, bd + ((kk * 2048) >> 4), kIdescKM,
            (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -126,7 +142,7 @@ constexpr size_t smem_bytes() {
 
 struct BwdArgs {
   AttnProblem p;
-  const float* lse2;      // [Hq, Tp] lse * log2(e)
+  const float* nlse2;     // [Hq, Tp] -lse * log2(e)
   const float* delta;     // [Hq, Tp]
   int64_t Tp;
   __nv_bfloat16* dq;      // [T, Hq, d]
@@ -150,11 +166,13 @@ struct __align__(1024) SmemKV {
   uint8_t q[2][kTile];
   uint8_t dout[2][kTile];
   uint8_t ds[kTile];            // dS^T, [q-block][key][64 q], 128-byte swizzle
-  float lse2[2][128];
-  float delta[2][128];
+  float nlse2[2][128];           // loaded with Q
+  float delta[2][128];          // loaded with Q
   uint64_t kv_full, kv_empty;
-  uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full, p_full, dv_done, dk_done, dkv_full, dkv_empty;
+  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t s_full, dp_full, dp_free, ds_ready, dk_done;
+  uint64_t p_ready[2], dv_done[2];
+  uint64_t dkv_full, dkv_empty;
   uint64_t item_full[2], item_empty[2];
   KvItem items[2];
   uint32_t tmem_base;
@@ -162,7 +180,7 @@ struct __align__(1024) SmemKV {
 };
 static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memory");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_k,
@@ -180,25 +198,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.qdo_full[s], 1);
-      mbar_init(&sm.qdo_empty[s], 1);
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);          // dK (stream 2) is the last reader of Q
+      mbar_init(&sm.do_full[s], 1);
+      mbar_init(&sm.do_empty[s], 2);         // dP^T (stream 1) and dV (stream 2) read dOut
+      mbar_init(&sm.p_ready[s], kKvSoftmaxWarps);
+      mbar_init(&sm.dv_done[s], 1);
       mbar_init(&sm.item_full[s], 1);
-      mbar_init(&sm.item_empty[s], 2 + 8);
+      mbar_init(&sm.item_empty[s], 2 + kKvSoftmaxWarps);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 256);
-    mbar_init(&sm.dv_done, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.dp_free, kKvSoftmaxWarps);
+    mbar_init(&sm.ds_ready, kKvSoftmaxWarps);
     mbar_init(&sm.dk_done, 1);
     mbar_init(&sm.dkv_full, 1);
-    mbar_init(&sm.dkv_empty, 256);
+    mbar_init(&sm.dkv_empty, kKvSoftmaxWarps);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma1) {
+  if (warp == kKvWarpMma1) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == kWarpProducer && lane == 0) {
+  if (warp == kKvWarpProducer && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_k);
@@ -214,160 +237,187 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t T = p.q_len;
   const int n_items = hdr->n_items2 * p.Hkv;
 
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t it_count = 0, kv_count = 0, qc = 0;
-      bool ok = true;
-      while (ok) {
-        const int idx = atomicAdd(&hdr->counter2, 1);
-        KvItem it;
-        it.ktile = 0; it.g = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
-        if (idx < n_items) {
-          const int kt = a.korder[idx / p.Hkv];
-          const int2 tr = a.ktiles[kt];
-          it.ktile = kt;
-          it.g = idx - (idx / p.Hkv) * p.Hkv;
-          it.i_lo = tr.x;
-          it.n_q = tr.y - tr.x + 1;
-          it.steps = G * it.n_q;
-        }
-        const uint32_t slot = it_count & 1;
-        if (it_count >= 2 &&
-            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
-          ok = false;
-          break;
-        }
-        sm.items[slot] = it;
-        mbar_arrive(&sm.item_full[slot]);
-        ++it_count;
-        if (it.steps < 0) break;
-        if (kv_count >= 1 && !mbar_wait(&sm.kv_empty, (kv_count - 1) & 1, abort_flag, hdr)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-          tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
-          tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
-        }
-        ++kv_count;
-        for (int n = 0; n < it.steps; ++n) {
-          const int hh = n / it.n_q;
-          const int h = it.g * G + hh;
-          const int i = it.i_lo + (n - hh * it.n_q);
-          const uint32_t st = qc & 1, use = qc >> 1;
-          if (use >= 1 && !mbar_wait(&sm.qdo_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+  if (warp >= 16) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kKvRegsControl));
+    if (warp == kKvWarpProducer) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        uint32_t it_count = 0, kv_count = 0, q_count = 0, do_count = 0;
+        bool ok = true;
+        while (ok) {
+          const int idx = atomicAdd(&hdr->counter2, 1);
+          KvItem it;
+          it.ktile = 0; it.g = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
+          if (idx < n_items) {
+            const int kt = a.korder[idx / p.Hkv];
+            const int2 tr = a.ktiles[kt];
+            it.ktile = kt;
+            it.g = idx - (idx / p.Hkv) * p.Hkv;
+            it.i_lo = tr.x;
+            it.n_q = tr.y - tr.x + 1;
+            it.steps = G * it.n_q;
+          }
+          const uint32_t slot = it_count & 1;
+          if (it_count >= 2 &&
+              !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kTile + 2 * 128 * sizeof(float));
+          sm.items[slot] = it;
+          mbar_arrive(&sm.item_full[slot]);
+          ++it_count;
+          if (it.steps < 0) break;
+          if (kv_count >= 1 && !mbar_wait(&sm.kv_empty, (kv_count - 1) & 1, abort_flag, hdr)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
-            tma_load_2d(sm.q[st] + cb * kBlk, &tm_q, &sm.qdo_full[st], h * HD + cb * 64, i * 128);
-            tma_load_2d(sm.dout[st] + cb * kBlk, &tm_do, &sm.qdo_full[st], h * HD + cb * 64,
-                        i * 128);
+            tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
+            tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
           }
-          const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
-          bulk_load(sm.lse2[st], a.lse2 + row, 128 * sizeof(float), &sm.qdo_full[st]);
-          bulk_load(sm.delta[st], a.delta + row, 128 * sizeof(float), &sm.qdo_full[st]);
-          ++qc;
-        }
-      }
-      if (!ok) {
-        // abort: every copy issued so far completes on its stage barrier
-        if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
-        for (uint32_t j = (qc > 2 ? qc - 2 : 0); j < qc; ++j)
-          drain_wait(&sm.qdo_full[j & 1], (j >> 1) & 1);
-      }
-    }
-  } else if (warp == kWarpMma1) {
-    // ------------------------------------------------------------ stream 1: S^T, dP^T
-    if (lane == 0) {
-      const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v);
-      uint32_t it_count = 0, items_done = 0, qc = 0;
-      bool ok = true;
-      while (ok) {
-        const uint32_t slot = it_count & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
-        const KvItem it = sm.items[slot];
-        mbar_arrive(&sm.item_empty[slot]);
-        ++it_count;
-        if (it.steps < 0) break;
-        if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
-        for (int n = 0; n < it.steps; ++n) {
-          const uint32_t st = qc & 1;
-          if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
-          // dP^T region is free once the softmax read the previous dP^T
-          if (qc >= 1 && !mbar_wait(&sm.p_full, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
-          tc_fence_after();
-          mma_kk(tmem + 128, v_s, smem_u32(sm.dout[st]), false);       // dP^T = V dOut^T
-          // S^T region holds the previous P^T until dV has read it
-          if (qc >= 1 && !mbar_wait(&sm.dv_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
-          tc_fence_after();
-          mma_kk(tmem + 0, k_s, smem_u32(sm.q[st]), false);            // S^T = K Q^T
-          mma_commit(&sm.s_full);
-          ++qc;
-        }
-        if (!ok) break;
-        mma_commit(&sm.kv_empty);
-        ++items_done;
-      }
-    }
-  } else if (warp == kWarpMma2) {
-    // ------------------------------------------------------------ stream 2: dV, dK
-    if (lane == 0) {
-      const uint32_t ds_s = smem_u32(sm.ds);
-      uint32_t it_count = 0, items_done = 0, qc = 0;
-      bool ok = true;
-      while (ok) {
-        const uint32_t slot = it_count & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
-        const KvItem it = sm.items[slot];
-        mbar_arrive(&sm.item_empty[slot]);
-        ++it_count;
-        if (it.steps < 0) break;
-        for (int n = 0; n < it.steps; ++n) {
-          const uint32_t st = qc & 1;
-          if (!mbar_wait(&sm.p_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
-          if (n == 0 && items_done > 0 &&
-              !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool acc = n > 0;
-          mma_t_split(tmem + 256, tmem + 0, smem_u32(sm.dout[st]), acc);   // dV += P^T dOut
-          mma_commit(&sm.dv_done);
-          {
-            // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
-            const uint64_t ad = smem_desc_sw128(ds_s, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(smem_u32(sm.q[st]), kBlk, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t aoff = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
-              mma_ss(tmem + 384, ad + aoff, bd + ((kk * 2048) >> 4), kIdescKM,
-                     (acc || kk > 0) ? 1u : 0u);
+          ++kv_count;
+          for (int n = 0; n < it.steps; ++n) {
+            const int hh = n / it.n_q;
+            const int h = it.g * G + hh;
+            const int i = it.i_lo + (n - hh * it.n_q);
+            const uint32_t st = q_count & 1, use = q_count >> 1;
+            if (use >= 1 && !mbar_wait(&sm.q_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
             }
+            mbar_arrive_expect_tx(&sm.q_full[st], kTile + 2 * 128 * sizeof(float));
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d(sm.q[st] + cb * kBlk, &tm_q, &sm.q_full[st], h * HD + cb * 64, i * 128);
+            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
+            bulk_load(sm.nlse2[st], a.nlse2 + row, 128 * sizeof(float), &sm.q_full[st]);
+            bulk_load(sm.delta[st], a.delta + row, 128 * sizeof(float), &sm.q_full[st]);
+            ++q_count;
+            if (use >= 1 && !mbar_wait(&sm.do_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.do_full[st], kTile);
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d(sm.dout[st] + cb * kBlk, &tm_do, &sm.do_full[st], h * HD + cb * 64,
+                          i * 128);
+            ++do_count;
           }
-          mma_commit(&sm.dk_done);
-          mma_commit(&sm.qdo_empty[st]);
-          ++qc;
         }
-        if (!ok) break;
-        mma_commit(&sm.dkv_full);
-        ++items_done;
+        if (!ok) {
+          // abort: every copy issued so far completes on its stage barrier
+          if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
+          for (uint32_t j = (q_count > 2 ? q_count - 2 : 0); j < q_count; ++j)
+            drain_wait(&sm.q_full[j & 1], (j >> 1) & 1);
+          for (uint32_t j = (do_count > 2 ? do_count - 2 : 0); j < do_count; ++j)
+            drain_wait(&sm.do_full[j & 1], (j >> 1) & 1);
+        }
+      }
+    } else if (warp == kKvWarpMma1) {
+      // ------------------------------------------------------------ stream 1: S^T, dP^T
+      // Step qc puts S^T in region qc & 1 and dP^T in the other one; the two
+      // regions swap roles every step.
+      if (lane == 0) {
+        const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v);
+        uint32_t it_count = 0, items_done = 0, qc = 0;
+        bool ok = true;
+        while (ok) {
+          const uint32_t slot = it_count & 1;
+          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+          const KvItem it = sm.items[slot];
+          mbar_arrive(&sm.item_empty[slot]);
+          ++it_count;
+          if (it.steps < 0) break;
+          if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
+          for (int n = 0; n < it.steps; ++n) {
+            const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
+            if (!mbar_wait(&sm.q_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            // region rb held the previous dP^T: free once the softmax has read it
+            if (qc >= 1 && !mbar_wait(&sm.dp_free, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+            tc_fence_after();
+            mma_kk(tmem + 128 * rb, k_s, smem_u32(sm.q[st]), false);          // S^T = K Q^T
+            mma_commit(&sm.s_full);
+            if (!mbar_wait(&sm.do_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            // region rb ^ 1 held the previous P^T: free once dV has read it
+            if (qc >= 1 && !mbar_wait(&sm.dv_done[rb ^ 1], ((qc - 1) >> 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_kk(tmem + 128 * (rb ^ 1), v_s, smem_u32(sm.dout[st]), false);  // dP^T = V dOut^T
+            mma_commit(&sm.dp_full);
+            mma_commit(&sm.do_empty[st]);
+            ++qc;
+          }
+          if (!ok) break;
+          mma_commit(&sm.kv_empty);
+          ++items_done;
+        }
+      }
+    } else if (warp == kKvWarpMma2) {
+      // ------------------------------------------------------------ stream 2: dV, dK
+      if (lane == 0) {
+        const uint32_t ds_s = smem_u32(sm.ds);
+        uint32_t it_count = 0, items_done = 0, qc = 0;
+        bool ok = true;
+        while (ok) {
+          const uint32_t slot = it_count & 1;
+          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+          const KvItem it = sm.items[slot];
+          mbar_arrive(&sm.item_empty[slot]);
+          ++it_count;
+          if (it.steps < 0) break;
+          for (int n = 0; n < it.steps; ++n) {
+            const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
+            if (!mbar_wait(&sm.p_ready[rb], use & 1, abort_flag, hdr)) { ok = false; break; }
+            if (n == 0 && items_done > 0 &&
+                !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&sm.do_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            tc_fence_after();
+            const bool acc = n > 0;
+            mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.dout[st]), acc);   // dV += P^T dOut
+            mma_commit(&sm.dv_done[rb]);
+            mma_commit(&sm.do_empty[st]);
+            if (!mbar_wait(&sm.ds_ready, qc & 1, abort_flag, hdr)) { ok = false; break; }
+            tc_fence_after();
+            {
+              // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
+              const uint64_t ad = smem_desc_sw128(ds_s, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(smem_u32(sm.q[st]), kBlk, 1024);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t aoff = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+                mma_ss(tmem + 384, ad + aoff, bd + ((kk * 2048) >> 4), kIdescKM,
+                       (acc || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&sm.dk_done);
+            mma_commit(&sm.q_empty[st]);
+            ++qc;
+          }
+          if (!ok) break;
+          mma_commit(&sm.dkv_full);
+          ++items_done;
+        }
       }
     }
-  } else if (warp < 8) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kKvRegsSoftmax));
     // ------------------------------------------------------------ softmax + dK/dV epilogue
-    const int wg = warp >> 2;                             // query columns 64 wg .. 64 wg + 63
+    const int cg = warp >> 2;                             // query columns 32 cg .. 32 cg + 31
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                          // TMEM lane = key row
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale * kLog2e;
-    const uint32_t ds_row = smem_u32(sm.ds) + wg * kBlk + r * 128;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    // this thread's dS^T row: query block cg / 2, 16-byte chunks 4 (cg & 1) .. + 3
+    const uint32_t ds_row = smem_u32(sm.ds) + (cg >> 1) * kBlk + r * 128;
     uint32_t it_count = 0, items_done = 0, qc = 0;
     bool ok = true;
     while (ok) {
@@ -387,84 +437,109 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int n = 0; n < it.steps; ++n) {
         const int hh = n / it.n_q;
-        const int64_t q0 = (int64_t)(it.i_lo + (n - hh * it.n_q)) * 128;
-        const uint32_t st = qc & 1;
-        if (!mbar_wait(&sm.qdo_full[st], (qc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        const int64_t q0 = (int64_t)(it.i_lo + (n - hh * it.n_q)) * 128 + cg * 32;
+        const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
+        const uint32_t s_tm = tmem + lane_base + 128 * rb + cg * 32;
+        const uint32_t dp_tm = tmem + lane_base + 128 * (rb ^ 1) + cg * 32;
+        if (!mbar_wait(&sm.q_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
         if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
-        // the dS^T buffer is free once dK has read the previous one
-        if (qc >= 1 && !mbar_wait(&sm.dk_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
-        const float* lse2s = sm.lse2[st];
-        const float* deltas = sm.delta[st];
+        uint32_t x[32];
+        tmem_ld32(s_tm, x);
+        tmem_wait_ld();
+        // phase 1: P = exp2(S sl2 - lse2), masked; P^T (bf16) goes back over
+        // the first 16 of the S^T columns this warp has read
+        const ulonglong2* nl = reinterpret_cast<const ulonglong2*>(sm.nlse2[st] + cg * 32);
+        const int loc = (int)min(max(qlo - q0, (int64_t)0), (int64_t)32);
+        const int hic = (int)min(max(qhi - q0, (int64_t)0), (int64_t)32);
+        const uint32_t span = (uint32_t)(hic - loc);
+        const bool full_w = __all_sync(0xffffffffu, loc == 0 && hic == 32);
+        uint64_t pp[16];                                   // P, float pairs
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = wg * 64 + c * 32;
-          uint32_t s[32], dp[32];
-          tmem_ld32(tmem + lane_base + 0 + col0, s);
-          tmem_ld32(tmem + lane_base + 128 + col0, dp);
-          tmem_wait_ld();
-          const int64_t qg0 = q0 + col0;
-          const int loc = (int)min(max(qlo - qg0, (int64_t)0), (int64_t)32);
-          const int hic = (int)min(max(qhi - qg0, (int64_t)0), (int64_t)32);
-          const uint32_t span = (uint32_t)(hic - loc);
-          const bool full_w = __all_sync(0xffffffffu, loc == 0 && hic == 32);
-          uint32_t pk[16], dk[16];
-          float lv[32], dv[32];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const ulonglong2 l = nl[e4];
+          pp[2 * e4] = f2_fma(f2_pack(__uint_as_float(x[4 * e4]), __uint_as_float(x[4 * e4 + 1])),
+                              sl2x2, l.x);
+          pp[2 * e4 + 1] = f2_fma(
+              f2_pack(__uint_as_float(x[4 * e4 + 2]), __uint_as_float(x[4 * e4 + 3])), sl2x2, l.y);
+        }
+        if (full_w) {
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2s + col0 + 4 * e4);
-            const float4 d4 = *reinterpret_cast<const float4*>(deltas + col0 + 4 * e4);
-            lv[4 * e4] = l4.x; lv[4 * e4 + 1] = l4.y; lv[4 * e4 + 2] = l4.z; lv[4 * e4 + 3] = l4.w;
-            dv[4 * e4] = d4.x; dv[4 * e4 + 1] = d4.y; dv[4 * e4 + 2] = d4.z; dv[4 * e4 + 3] = d4.w;
+          for (int e = 0; e < 16; ++e) {
+            float u0, u1;
+            f2_unpack(pp[e], u0, u1);
+            u0 = ex2(u0);
+            u1 = ex2(u1);
+            pp[e] = f2_pack(u0, u1);
+            pk[e] = pack_bf16x2(u0, u1);
           }
-          if (full_w) {
+        } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lv[2 * e]));
-              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lv[2 * e + 1]));
-              pk[e] = pack_bf16x2(p0, p1);
-              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - dv[2 * e]),
-                                  p1 * (__uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1]));
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const bool v0 = (uint32_t)(2 * e - loc) < span;
-              const bool v1 = (uint32_t)(2 * e + 1 - loc) < span;
-              const float p0 =
-                  ex2(v0 ? fmaf(__uint_as_float(s[2 * e]), sl2, -lv[2 * e]) : -INFINITY);
-              const float p1 =
-                  ex2(v1 ? fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lv[2 * e + 1]) : -INFINITY);
-              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - dv[2 * e] : 0.f;
-              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1] : 0.f;
-              pk[e] = pack_bf16x2(p0, p1);
-              dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
-            }
-          }
-          tmem_st16(tmem + lane_base + wg * 64 + c * 16, pk);   // P^T over read S^T columns
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = c * 4 + u;                        // 8 query columns per 16 bytes
-            st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
-                         dk[4 * u + 2], dk[4 * u + 3]);
+          for (int e = 0; e < 16; ++e) {
+            float u0, u1;
+            f2_unpack(pp[e], u0, u1);
+            u0 = ex2((uint32_t)(2 * e - loc) < span ? u0 : -INFINITY);
+            u1 = ex2((uint32_t)(2 * e + 1 - loc) < span ? u1 : -INFINITY);
+            pp[e] = f2_pack(u0, u1);
+            pk[e] = pack_bf16x2(u0, u1);
           }
         }
+        tmem_st16(s_tm, pk);
         tmem_wait_st();
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[rb]);
+        // phase 2: dS = P (dP - delta); masked P is zero, so dS is too
+        if (!mbar_wait(&sm.dp_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld32(dp_tm, x);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.dp_free);
+        // the dS^T buffer is free once dK has read the previous one
+        if (qc >= 1 && !mbar_wait(&sm.dk_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        const ulonglong2* dl = reinterpret_cast<const ulonglong2*>(sm.delta[st] + cg * 32);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const ulonglong2 dd = dl[e4];
+          const uint64_t s0 = f2_mul(
+              pp[2 * e4],
+              f2_sub(f2_pack(__uint_as_float(x[4 * e4]), __uint_as_float(x[4 * e4 + 1])), dd.x));
+          const uint64_t s1 = f2_mul(
+              pp[2 * e4 + 1],
+              f2_sub(f2_pack(__uint_as_float(x[4 * e4 + 2]), __uint_as_float(x[4 * e4 + 3])), dd.y));
+          float a0, a1, b0, b1;
+          f2_unpack(s0, a0, a1);
+          f2_unpack(s1, b0, b1);
+          dk[2 * e4] = pack_bf16x2(a0, a1);
+          dk[2 * e4 + 1] = pack_bf16x2(b0, b1);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (cg & 1) * 4 + u;                 // 8 query columns per 16 bytes
+          st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2],
+                       dk[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ds_ready);
         ++qc;
       }
       if (!ok) break;
-      // item epilogue: dV (warps 0-3) and dK (warps 4-7), TMEM lane = key row
+      // item epilogue: warps of column groups 0-1 write dV, 2-3 write dK (64
+      // columns each), TMEM lane = key row
       if (!mbar_wait(&sm.dkv_full, items_done & 1, abort_flag, hdr)) break;
       tc_fence_after();
       {
-        const uint32_t col = wg == 0 ? 256u : 384u;
-        const float scale = wg == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = (wg == 0 ? a.dv : a.dk) + (key * p.Hkv + it.g) * HD;
+        const bool is_dk = cg >= 2;
+        const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
+        const float scale = is_dk ? p.scale : 1.f;
+        __nv_bfloat16* dst = (is_dk ? a.dk : a.dv) + (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + col + c * 32, v);
           tmem_wait_ld();
@@ -472,14 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm.dkv_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.dkv_empty);
       ++items_done;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma1) {
+  if (warp == kKvWarpMma1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -487,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================ dQ
 
-constexpr int Q_NS = 2;
+constexpr int K_NS = 3;   // K tiles are read until dQ of their tile is done: one more stage
+constexpr int V_NS = 2;
 
 struct QItem {
   int qtile, h, g, j_lo, n_kv, pad[3];     // n_kv 128-key tiles; -1 stops
@@ -496,17 +573,32 @@ struct QItem {
 struct __align__(1024) SmemQ {
   uint8_t q[kTile];
   uint8_t dout[kTile];
-  uint8_t k[Q_NS][kTile];
-  uint8_t v[Q_NS][kTile];
+  uint8_t k[K_NS][kTile];
+  uint8_t v[V_NS][kTile];
   uint64_t q_full, q_empty;
-  uint64_t k_full[Q_NS], k_empty[Q_NS], v_full[Q_NS], v_empty[Q_NS];
-  uint64_t s_full, p_full[2], dq_done[2], o_full, epi_done;
+  uint64_t k_full[K_NS], k_empty[K_NS], v_full[V_NS], v_empty[V_NS];
+  uint64_t s_full[2], p_full[2], dq_done[2];
+  uint64_t dp_full, dp_free, o_full, epi_done;
   uint64_t item_full[2], item_empty[2];
   QItem items[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(SmemQ) <= kSmemLimit, "dQ tile set exceeds shared memory");
+
+// dP = dOut V^T for tile jc (any stream): dP region free once the softmax
+// has read the previous dP.
+__device__ __forceinline__ bool issue_dp(SmemQ& sm, uint32_t tmem, uint32_t jc,
+                                         volatile int* abort_flag, WsHeader* hdr) {
+  const uint32_t vst = jc % V_NS, vuse = jc / V_NS;
+  if (!mbar_wait(&sm.v_full[vst], vuse & 1, abort_flag, hdr)) return false;
+  if (jc >= 1 && !mbar_wait(&sm.dp_free, (jc - 1) & 1, abort_flag, hdr)) return false;
+  tc_fence_after();
+  mma_kk(tmem + 256, smem_u32(sm.dout), smem_u32(sm.v[vst]), false);
+  mma_commit(&sm.dp_full);
+  mma_commit(&sm.v_empty[vst]);
+  return true;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -524,20 +616,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
-    for (int s = 0; s < Q_NS; ++s) {
+    mbar_init(&sm.q_empty, 2);               // both streams read Q or dOut
+    for (int s = 0; s < K_NS; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 2);          // S (stream 1) and dQ (stream 2) read K
+    }
+    for (int s = 0; s < V_NS; ++s) {
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);          // dP, issued by one of the streams
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_full[b], 256);
       mbar_init(&sm.dq_done[b], 1);
       mbar_init(&sm.item_full[b], 1);
       mbar_init(&sm.item_empty[b], 2 + 8);
     }
-    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.dp_free, 256);
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.epi_done, 256);
     sm.abort_flag = 0;
@@ -566,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t it_count = 0, q_count = 0, kv_count = 0;
+      uint32_t it_count = 0, q_count = 0, k_count = 0, v_count = 0;
       bool ok = true;
       while (ok) {
         const int idx = atomicAdd(&hdr->counter, 1);
@@ -607,40 +703,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
-          const uint32_t st = kv_count % Q_NS, use = kv_count / Q_NS;
           const int key0 = (it.j_lo + jj) * 128;
-          if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.k_full[st], kTile);
+          {
+            const uint32_t st = k_count % K_NS, use = k_count / K_NS;
+            if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.k_full[st], kTile);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.k_full[st], it.g * HD + cb * 64, key0);
-          if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
-            drain_wait(&sm.k_full[st], use & 1);
-            ok = false;
-            break;
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.k_full[st], it.g * HD + cb * 64, key0);
+            ++k_count;
           }
-          mbar_arrive_expect_tx(&sm.v_full[st], kTile);
+          {
+            const uint32_t st = v_count % V_NS, use = v_count / V_NS;
+            if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.v_full[st], kTile);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.v[st] + cb * kBlk, &tm_v, &sm.v_full[st], it.g * HD + cb * 64, key0);
-          ++kv_count;
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d(sm.v[st] + cb * kBlk, &tm_v, &sm.v_full[st], it.g * HD + cb * 64, key0);
+            ++v_count;
+          }
         }
       }
       if (!ok) {
         if (q_count >= 1) drain_wait(&sm.q_full, (q_count - 1) & 1);
-        for (uint32_t j = (kv_count > Q_NS ? kv_count - Q_NS : 0); j < kv_count; ++j) {
-          drain_wait(&sm.k_full[j % Q_NS], (j / Q_NS) & 1);
-          drain_wait(&sm.v_full[j % Q_NS], (j / Q_NS) & 1);
-        }
+        for (uint32_t j = (k_count > K_NS ? k_count - K_NS : 0); j < k_count; ++j)
+          drain_wait(&sm.k_full[j % K_NS], (j / K_NS) & 1);
+        for (uint32_t j = (v_count > V_NS ? v_count - V_NS : 0); j < v_count; ++j)
+          drain_wait(&sm.v_full[j % V_NS], (j / V_NS) & 1);
       }
     }
   } else if (warp == kWarpMma1) {
-    // ------------------------------------------------------------ stream 1: S, dP
+    // ------------------------------------------------------------ stream 1: S, dP of even tiles
     if (lane == 0) {
-      const uint32_t q_s = smem_u32(sm.q), do_s = smem_u32(sm.dout);
+      const uint32_t q_s = smem_u32(sm.q);
       uint32_t it_count = 0, q_count = 0, jc = 0;
       bool ok = true;
       while (ok) {
@@ -654,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sm.q_full, q_count & 1, abort_flag, hdr)) break;
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
-          const uint32_t st = jc % Q_NS, use = jc / Q_NS, b = jc & 1;
+          const uint32_t st = jc % K_NS, use = jc / K_NS, b = jc & 1;
           if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
           // S buffer b is free once dQ has read the dS written over it two tiles ago
           if (jc >= 2 && !mbar_wait(&sm.dq_done[b], ((jc - 2) >> 1) & 1, abort_flag, hdr)) {
@@ -663,25 +764,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           mma_kk(tmem + 128 * b, q_s, smem_u32(sm.k[st]), false);        // S = Q K^T
+          mma_commit(&sm.s_full[b]);
           mma_commit(&sm.k_empty[st]);
-          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
-          // dP region is free once the softmax read the previous dP
-          if (jc >= 1 &&
-              !mbar_wait(&sm.p_full[(jc - 1) & 1], ((jc - 1) >> 1) & 1, abort_flag, hdr)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          mma_kk(tmem + 256, do_s, smem_u32(sm.v[st]), false);           // dP = dOut V^T
-          mma_commit(&sm.s_full);
-          mma_commit(&sm.v_empty[st]);
-          if (jj + 1 == it.n_kv) mma_commit(&sm.q_empty);
+          if ((jj & 1) == 0 && !issue_dp(sm, tmem, jc, abort_flag, hdr)) { ok = false; break; }
           ++jc;
         }
+        if (!ok) break;
+        mma_commit(&sm.q_empty);
       }
     }
   } else if (warp == kWarpMma2) {
-    // ------------------------------------------------------------ stream 2: dQ
+    // ------------------------------------------------------------ stream 2: dP of odd tiles, dQ
     if (lane == 0) {
       uint32_t it_count = 0, items_done = 0, jc = 0;
       bool ok = true;
@@ -694,7 +787,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.n_kv < 0) break;
         if (it.n_kv == 0) continue;
         for (int jj = 0; jj < it.n_kv; ++jj) {
-          const uint32_t st = jc % Q_NS, b = jc & 1;
+          const uint32_t st = jc % K_NS, b = jc & 1;
+          // dP of the next tile when its in-item index is odd: it is due
+          // before this tile's dQ (the softmax frees dP mid-tile)
+          if (((jj + 1) & 1) == 1 && jj + 1 < it.n_kv &&
+              !issue_dp(sm, tmem, jc + 1, abort_flag, hdr)) {
+            ok = false;
+            break;
+          }
           if (!mbar_wait(&sm.p_full[b], (jc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
           if (jj == 0 && items_done > 0 &&
               !mbar_wait(&sm.epi_done, (items_done - 1) & 1, abort_flag, hdr)) {
@@ -702,12 +802,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_t_split(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]), jj > 0);   // dQ += dS K
+          mma_t_split<64>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]), jj > 0);   // dQ += dS K
           mma_commit(&sm.dq_done[b]);
           mma_commit(&sm.k_empty[st]);
           ++jc;
         }
         if (!ok) break;
+        mma_commit(&sm.q_empty);
         mma_commit(&sm.o_full);
         ++items_done;
       }
@@ -733,52 +834,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row = (int64_t)it.qtile * 128 + r;
       const bool valid = row < T;
       int lo = 0, hi = 0;                                    // visible keys [lo, hi)
-      float lse2r = 0.f, deltar = 0.f;
+      float nlse2r = 0.f, deltar = 0.f;
       if (valid) {
         const int b = doc_of(p.cu, p.ndoc, row);
         lo = __ldg(p.cu + b);
         hi = p.causal ? (int)row + 1 : __ldg(p.cu + b + 1);
-        lse2r = __ldg(a.lse2 + (int64_t)h * a.Tp + row);
+        nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + row);
         deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
       }
       for (int jj = 0; jj < it.n_kv; ++jj) {
         const uint32_t b = jc & 1;
-        if (!mbar_wait(&sm.s_full, jc & 1, abort_flag, hdr)) { ok = false; break; }
+        const uint32_t s_tm = tmem + lane_base + 128 * b + wg * 64;
+        const uint32_t dp_tm = tmem + lane_base + 256 + wg * 64;
+        if (!mbar_wait(&sm.s_full[b], (jc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
+        // phase 1: P = exp2(S sl2 - nlse2), masked to the row's visible keys
+        uint32_t pf[64];
+        tmem_ld32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(pf));
+        tmem_ld32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(pf + 32));
+        tmem_wait_ld();
         const int key0 = (it.j_lo + jj) * 128 + wg * 64;
         const int aa = lo - key0;
         const uint32_t span = (uint32_t)(hi - lo);
         const bool full_w = __all_sync(0xffffffffu, lo <= key0 && key0 + 64 <= hi);
-        const uint32_t s_tm = tmem + lane_base + 128 * b + wg * 64;
-        const uint32_t dp_tm = tmem + lane_base + 256 + wg * 64;
+        if (full_w) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            pf[e] = __float_as_uint(ex2(fmaf(__uint_as_float(pf[e]), sl2, nlse2r)));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const bool vis = (uint32_t)(e - aa) < span;
+            pf[e] = __float_as_uint(
+                ex2(vis ? fmaf(__uint_as_float(pf[e]), sl2, nlse2r) : -INFINITY));
+          }
+        }
+        // phase 2: dS = P (dP - delta) in bf16 over S (masked P is zero)
+        if (!mbar_wait(&sm.dp_full, jc & 1, abort_flag, hdr)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dp[64];
+        tmem_ld32(dp_tm, *reinterpret_cast<uint32_t(*)[32]>(dp));
+        tmem_ld32(dp_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(dp + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&sm.dp_free);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(s_tm + c * 32, s);
-          tmem_ld32(dp_tm + c * 32, dp);
-          tmem_wait_ld();
           uint32_t dk[16];
-          if (full_w) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -lse2r));
-              const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2r));
-              dk[e] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * e]) - deltar),
-                                  p1 * (__uint_as_float(dp[2 * e + 1]) - deltar));
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = c * 32 + 2 * e;
-              const bool v0 = (uint32_t)(col - aa) < span;
-              const bool v1 = (uint32_t)(col + 1 - aa) < span;
-              const float p0 = ex2(v0 ? fmaf(__uint_as_float(s[2 * e]), sl2, -lse2r) : -INFINITY);
-              const float p1 =
-                  ex2(v1 ? fmaf(__uint_as_float(s[2 * e + 1]), sl2, -lse2r) : -INFINITY);
-              const float d0 = v0 ? __uint_as_float(dp[2 * e]) - deltar : 0.f;
-              const float d1 = v1 ? __uint_as_float(dp[2 * e + 1]) - deltar : 0.f;
-              dk[e] = pack_bf16x2(p0 * d0, p1 * d1);
-            }
+          for (int e = 0; e < 16; ++e) {
+            const int i0 = c * 32 + 2 * e;
+            dk[e] = pack_bf16x2(__uint_as_float(pf[i0]) * (__uint_as_float(dp[i0]) - deltar),
+                                __uint_as_float(pf[i0 + 1]) *
+                                    (__uint_as_float(dp[i0 + 1]) - deltar));
           }
           tmem_st16(s_tm + c * 16, dk);       // dS over S (columns already read)
         }
@@ -867,13 +975,13 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
       !make_map(&mk, p.k, T, kc) || !make_map(&mv, p.v, T, kc))
     return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
-  float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-  cudaError_t e = launch_bwd_delta(out, dout, lse, delta, lse2, T, L.Tp, p.Hq, HD, p.io_dtype,
+  float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
+  cudaError_t e = launch_bwd_delta(out, dout, lse, delta, nlse2, T, L.Tp, p.Hq, HD, p.io_dtype,
                                    p.hdr, s);
   if (e != cudaSuccess) return e;
   BwdArgs a;
   a.p = p;
-  a.lse2 = lse2;
+  a.nlse2 = nlse2;
   a.delta = delta;
   a.Tp = L.Tp;
   a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
@@ -892,7 +1000,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)q_bytes);
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<<<grid, kThreads, kv_bytes, s>>>(mq, mdo, mk, mv, a);
+  attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kv_bytes, s>>>(mq, mdo, mk, mv, a);
   count_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

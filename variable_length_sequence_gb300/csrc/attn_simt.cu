@@ -292,7 +292,7 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
   if (e != cudaSuccess) return e;
-  e = launch_bwd_delta(out, dout, lse, delta, reinterpret_cast<float*>(ws + L.lse2), T, L.Tp,
+  e = launch_bwd_delta(out, dout, lse, delta, reinterpret_cast<float*>(ws + L.nlse2), T, L.Tp,
                        p.Hq, D, p.io_dtype, p.hdr, s);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(BwdSmem<D>);

@@ -27,7 +27,7 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&x)[4]) {
   x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
 }
 
-// delta[h, t] = <dout[t, h, :], out[t, h, :]> and lse2[h, t] = lse[h, t] log2(e),
+// delta[h, t] = <dout[t, h, :], out[t, h, :]> and nlse2[h, t] = -lse[h, t] log2(e),
 // both with row stride Tp (rows padded to whole tiles, padding set to 0);
 // TPR threads share one (t, h) row.
 template <typename TI, int D>
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
                                                         const TI* __restrict__ dout,
                                                         const float* __restrict__ lse,
                                                         float* __restrict__ delta,
-                                                        float* __restrict__ lse2, int64_t T,
+                                                        float* __restrict__ nlse2, int64_t T,
                                                         int64_t Tp, int Hq, const WsHeader* hdr) {
   constexpr int VEC = 16 / sizeof(TI);
   constexpr int TPR = D / VEC;                  // 16 (bf16, d=128) ... 32 (f32, d=128)
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
       const int64_t t = rr / Hq;
       const int h = (int)(rr - t * Hq);
       delta[(int64_t)h * Tp + t] = acc;
-      lse2[(int64_t)h * Tp + t] = lse[(int64_t)h * T + t] * 1.4426950408889634f;
+      nlse2[(int64_t)h * Tp + t] = lse[(int64_t)h * T + t] * -1.4426950408889634f;
     }
   }
   // zero the padding columns [T, Tp) of every head row
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
   for (int64_t e = gtid; e < pad * Hq; e += nthreads) {
     const int64_t h = e / pad, t = T + e % pad;
     delta[h * Tp + t] = 0.f;
-    lse2[h * Tp + t] = 0.f;
+    nlse2[h * Tp + t] = 0.f;
   }
 }
 
@@ -101,27 +101,27 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }  // namespace
 
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
-                             float* lse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
+                             float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
                              WsHeader* hdr, cudaStream_t s) {
   const int blocks = num_sms() * 8;
   if (io_dtype == NSP_BF16) {
     if (d == 128)
       bwd_delta_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, s>>>(
           reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, lse2, T, Tp, Hq, hdr);
+          lse, delta, nlse2, T, Tp, Hq, hdr);
     else
       bwd_delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(
           reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, lse2, T, Tp, Hq, hdr);
+          lse, delta, nlse2, T, Tp, Hq, hdr);
   } else {
     if (d == 128)
       bwd_delta_kernel<float, 128><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
                                                          reinterpret_cast<const float*>(dout),
-                                                         lse, delta, lse2, T, Tp, Hq, hdr);
+                                                         lse, delta, nlse2, T, Tp, Hq, hdr);
     else
       bwd_delta_kernel<float, 64><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
                                                         reinterpret_cast<const float*>(dout),
-                                                        lse, delta, lse2, T, Tp, Hq, hdr);
+                                                        lse, delta, nlse2, T, Tp, Hq, hdr);
   }
   count_launches(1);
   return cudaGetLastError();

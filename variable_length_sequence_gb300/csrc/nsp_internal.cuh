@@ -59,7 +59,7 @@ struct BwdWsLayout {
   size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_sub + 2]
   size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_sub + 2]
   size_t delta;                    // float [Hq, Tp]
-  size_t lse2;                     // float [Hq, Tp]
+  size_t nlse2;                     // float [Hq, Tp]
   size_t dq_acc;                   // float [T, Hq, d] (CUDA-core path)
   size_t total;
   int64_t Tp, n_qtiles, n_ktiles, n_sub;
@@ -79,7 +79,7 @@ inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d, bool need_dq_
   L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_ktiles, 256);
   L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_sub + 2), 256);
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
-  L.lse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
+  L.nlse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off;
   if (need_dq_acc) off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
   L.total = off;
@@ -117,7 +117,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
                                const float* lse, void* dq, void* dk, void* dv,
                                const BwdWsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
-                             float* lse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
+                             float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
                              WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n, int io_dtype,
                               WsHeader* hdr, cudaStream_t s);
