@@ -49,6 +49,9 @@ CONFIG_ID = 2
 RING_SHARDS = 8
 PERMUTE_GROUPS = 8
 L2_FLUSH_BYTES = 256 << 20
+# ncu DRAM read + write bytes of one main-forward launch of this workload
+# (365.7 MB + 230.4 MB), taken on the current forward kernel.
+FWD_LAUNCH_DRAM_BYTES = 596.1e6
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -110,14 +113,15 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []           # (arrival time, csv line)
         self.t = None
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -126,7 +130,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The timed region, in time.perf_counter() seconds: only samples that
+        arrive inside it (plus one sampling interval) are reported."""
+        self.window = (t0, t1 + 0.06)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -140,7 +149,9 @@ class ClockSampler:
             self.t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if self.window is not None and not (self.window[0] <= t <= self.window[1]):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -310,6 +321,9 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     nlegs = len(Problem.LEGS)
 
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    clocks.start()                          # nvidia-smi takes a while to start sampling
     for _ in range(args.warmup):
         flush.zero_()
         prob.step(stream)
@@ -320,12 +334,9 @@ def run_ours(args, world, rank, local):
                for _ in range(K)]
     leg_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(nlegs)] for _ in range(K)]
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
     launches0 = nsp.nsp_kernel_launches()
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()                       # L2 flush, outside the timed region
@@ -334,7 +345,9 @@ def run_ours(args, world, rank, local):
         step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    wall = time.perf_counter() - wall0
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
+    clocks.mark(wall0, wall1)
     clk = clocks.stop()
     launches = nsp.nsp_kernel_launches() - launches0
 
@@ -360,17 +373,22 @@ def run_ours(args, world, rank, local):
     }
     for k in ("fwd", "bwd", "ring_partials"):
         leg_stats[k]["frac_bf16"] = leg_stats[k]["tflops"] / peaks["bf16_tflops"]
-    dom = max(Problem.LEGS, key=lambda k: legs[k])
-    if dom in ("merge", "permute"):
-        ach = leg_stats[dom]["gbs"]
-        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None}
-    else:
-        ach = leg_stats[dom]["tflops"]
-        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None}
+    # Roofline of the kernel with the largest share of the step's GPU time
+    # (an ncu launch list of this step: the attention forward kernel, main
+    # forward plus ring partials), on its main-forward launch: useful FLOP of
+    # that launch / its duration, timed with CUDA events on the launching
+    # stream (the duration includes the small tile-schedule kernel of the call).
+    ach = leg_stats["fwd"]["tflops"]
+    roof = {"bound": "tensor", "kernel": "attn_fwd_tc_kernel (main forward launch)",
+            "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"],
+            # DRAM bytes (read + write) of this launch from one ncu capture of
+            # the bench workload (dram__bytes_read.sum + dram__bytes_write.sum);
+            # compulsory bytes (Q, K, V, out, lse) are 607 MB.
+            "traffic": FWD_LAUNCH_DRAM_BYTES,
+            "traffic_unit": "bytes per launch",
+            "algorithmic_flop": prob.fwd_flop}
     roof["peak_source"] = peaks["source"] + " (burst)"
-    roof["note"] = "duration = the whole C-ABI call (its small schedule kernels included)"
 
     e2e = run_e2e(args, prob, nsp, w, device, stream, world)
 
@@ -509,7 +527,7 @@ def run_reference(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
