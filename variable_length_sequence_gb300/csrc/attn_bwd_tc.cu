@@ -410,14 +410,23 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kKvRegsSoftmax));
     // ------------------------------------------------------------ softmax + dK/dV epilogue
-    const int cg = warp >> 2;                             // query columns 32 cg .. 32 cg + 31
+    // Warp (cg, wq) covers TMEM lane quadrant wq (32 keys) and query columns
+    // 32 cg .. 32 cg + 31.  Scores are read as 16-lane fragments (16x256b,
+    // two loads per quadrant): thread t holds key rows wq 32 + t/4 + 8 i
+    // (i = 0..3) at columns 8 j + 2 (t % 4) + {0, 1} (j = 0..3), so it needs
+    // the lse and delta of 8 columns only, read as 4 float pairs each.
+    // Register x[16 h + 4 j + 2 e + u] is row 16 h + 8 e + t/4, column
+    // 8 j + 2 (t % 4) + u; fragment row index i = 2 h + e.
+    const int cg = warp >> 2;
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;                          // TMEM lane = key row
+    const int r = wq * 32 + lane;                          // epilogue: TMEM lane = key row
+    const int tr = lane >> 2, tc2 = 2 * (lane & 3);
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale * kLog2e;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    // this thread's dS^T row: query block cg / 2, 16-byte chunks 4 (cg & 1) .. + 3
-    const uint32_t ds_row = smem_u32(sm.ds) + (cg >> 1) * kBlk + r * 128;
+    // dS^T tile: query block cg / 2, 16-byte chunks 4 (cg & 1) + j, swizzled
+    // by key & 7 (= tr for every fragment row)
+    const uint32_t ds_base = smem_u32(sm.ds) + (cg >> 1) * kBlk + (wq * 32 + tr) * 128 + 2 * tc2;
     uint32_t it_count = 0, items_done = 0, qc = 0;
     bool ok = true;
     while (ok) {
@@ -428,16 +437,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.steps < 0) break;
-      const int64_t key = (int64_t)it.ktile * 128 + r;
-      int64_t qlo = 0, qhi = 0;                             // queries that see this key
-      if (key < T) {
-        const int b = doc_of(p.cu, p.ndoc, key);
-        qlo = p.causal ? key : (int64_t)__ldg(p.cu + b);
-        qhi = (int64_t)__ldg(p.cu + b + 1);
+      int qlo[4], qhi[4];                                   // queries that see fragment row i
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t key = (int64_t)it.ktile * 128 + wq * 32 + tr + 8 * i;
+        qlo[i] = 0;
+        qhi[i] = 0;
+        if (key < T) {
+          const int b = doc_of(p.cu, p.ndoc, key);
+          qlo[i] = p.causal ? (int)key : __ldg(p.cu + b);
+          qhi[i] = __ldg(p.cu + b + 1);
+        }
       }
       for (int n = 0; n < it.steps; ++n) {
         const int hh = n / it.n_q;
-        const int64_t q0 = (int64_t)(it.i_lo + (n - hh * it.n_q)) * 128 + cg * 32;
+        const int q0 = (it.i_lo + (n - hh * it.n_q)) * 128 + cg * 32;
         const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
         const uint32_t s_tm = tmem + lane_base + 128 * rb + cg * 32;
         const uint32_t dp_tm = tmem + lane_base + 128 * (rb ^ 1) + cg * 32;
@@ -445,47 +459,63 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
         uint32_t x[32];
-        tmem_ld32(s_tm, x);
+        tmem_ld16x256_x4(s_tm, x);
+        tmem_ld16x256_x4(s_tm + (16u << 16), x + 16);
+        uint64_t nl[4];                                     // -lse log2(e) column pairs
+        {
+          const float* src = sm.nlse2[st] + cg * 32 + tc2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) nl[j] = *reinterpret_cast<const uint64_t*>(src + 8 * j);
+        }
+        int loc[4];
+        uint32_t span[4];
+        bool full = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          loc[i] = min(max(qlo[i] - q0, 0), 32);
+          const int hic = min(max(qhi[i] - q0, 0), 32);
+          span[i] = (uint32_t)(hic - loc[i]);
+          full = full && loc[i] == 0 && hic == 32;
+        }
+        const bool full_w = __all_sync(0xffffffffu, full);
         tmem_wait_ld();
-        // phase 1: P = exp2(S sl2 - lse2), masked; P^T (bf16) goes back over
-        // the first 16 of the S^T columns this warp has read
-        const ulonglong2* nl = reinterpret_cast<const ulonglong2*>(sm.nlse2[st] + cg * 32);
-        const int loc = (int)min(max(qlo - q0, (int64_t)0), (int64_t)32);
-        const int hic = (int)min(max(qhi - q0, (int64_t)0), (int64_t)32);
-        const uint32_t span = (uint32_t)(hic - loc);
-        const bool full_w = __all_sync(0xffffffffu, loc == 0 && hic == 32);
+        // phase 1: P = exp2(S sl2 - lse2), masked; P^T (bf16 pairs) goes back
+        // over the first 16 of the S^T columns this warp has read
         uint64_t pp[16];                                   // P, float pairs
         uint32_t pk[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const ulonglong2 l = nl[e4];
-          pp[2 * e4] = f2_fma(f2_pack(__uint_as_float(x[4 * e4]), __uint_as_float(x[4 * e4 + 1])),
-                              sl2x2, l.x);
-          pp[2 * e4 + 1] = f2_fma(
-              f2_pack(__uint_as_float(x[4 * e4 + 2]), __uint_as_float(x[4 * e4 + 3])), sl2x2, l.y);
+        for (int k = 0; k < 16; ++k) {
+          const int j = (k >> 1) & 3;
+          pp[k] = f2_fma(f2_pack(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])),
+                         sl2x2, nl[j]);
         }
         if (full_w) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int k = 0; k < 16; ++k) {
             float u0, u1;
-            f2_unpack(pp[e], u0, u1);
+            f2_unpack(pp[k], u0, u1);
             u0 = ex2(u0);
             u1 = ex2(u1);
-            pp[e] = f2_pack(u0, u1);
-            pk[e] = pack_bf16x2(u0, u1);
+            pp[k] = f2_pack(u0, u1);
+            pk[k] = pack_bf16x2(u0, u1);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int k = 0; k < 16; ++k) {
+            const int i = 2 * (k >> 3) + (k & 1);          // fragment row
+            const int col = 8 * ((k >> 1) & 3) + tc2;
             float u0, u1;
-            f2_unpack(pp[e], u0, u1);
-            u0 = ex2((uint32_t)(2 * e - loc) < span ? u0 : -INFINITY);
-            u1 = ex2((uint32_t)(2 * e + 1 - loc) < span ? u1 : -INFINITY);
-            pp[e] = f2_pack(u0, u1);
-            pk[e] = pack_bf16x2(u0, u1);
+            f2_unpack(pp[k], u0, u1);
+            u0 = ex2((uint32_t)(col - loc[i]) < span[i] ? u0 : -INFINITY);
+            u1 = ex2((uint32_t)(col + 1 - loc[i]) < span[i] ? u1 : -INFINITY);
+            pp[k] = f2_pack(u0, u1);
+            pk[k] = pack_bf16x2(u0, u1);
           }
         }
-        tmem_st16(s_tm, pk);
+        // pk[8 h + 2 j + e] is (row 16 h + 8 e + t/4, packed column 4 j + t % 4):
+        // the 16x128b register order
+        tmem_st16x128_x4(s_tm, pk);
+        tmem_st16x128_x4(s_tm + (16u << 16), pk + 8);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -493,35 +523,31 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // phase 2: dS = P (dP - delta); masked P is zero, so dS is too
         if (!mbar_wait(&sm.dp_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
-        tmem_ld32(dp_tm, x);
+        tmem_ld16x256_x4(dp_tm, x);
+        tmem_ld16x256_x4(dp_tm + (16u << 16), x + 16);
+        uint64_t dd[4];                                     // delta column pairs
+        {
+          const float* src = sm.delta[st] + cg * 32 + tc2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dd[j] = *reinterpret_cast<const uint64_t*>(src + 8 * j);
+        }
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.dp_free);
         // the dS^T buffer is free once dK has read the previous one
         if (qc >= 1 && !mbar_wait(&sm.dk_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
-        const ulonglong2* dl = reinterpret_cast<const ulonglong2*>(sm.delta[st] + cg * 32);
-        uint32_t dk[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const ulonglong2 dd = dl[e4];
-          const uint64_t s0 = f2_mul(
-              pp[2 * e4],
-              f2_sub(f2_pack(__uint_as_float(x[4 * e4]), __uint_as_float(x[4 * e4 + 1])), dd.x));
-          const uint64_t s1 = f2_mul(
-              pp[2 * e4 + 1],
-              f2_sub(f2_pack(__uint_as_float(x[4 * e4 + 2]), __uint_as_float(x[4 * e4 + 3])), dd.y));
-          float a0, a1, b0, b1;
-          f2_unpack(s0, a0, a1);
-          f2_unpack(s1, b0, b1);
-          dk[2 * e4] = pack_bf16x2(a0, a1);
-          dk[2 * e4 + 1] = pack_bf16x2(b0, b1);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (cg & 1) * 4 + u;                 // 8 query columns per 16 bytes
-          st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2],
-                       dk[4 * u + 3]);
+        for (int k = 0; k < 16; ++k) {
+          const int j = (k >> 1) & 3;
+          const int rowoff = 16 * (k >> 3) + 8 * (k & 1);   // key row - (wq 32 + t/4)
+          const uint64_t s2 =
+              f2_mul(pp[k], f2_sub(f2_pack(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])),
+                                   dd[j]));
+          float a0, a1;
+          f2_unpack(s2, a0, a1);
+          const int chunk = (cg & 1) * 4 + j;               // 8 query columns per 16 bytes
+          st_shared_u32(ds_base + rowoff * 128 + ((chunk ^ tr) << 4), pack_bf16x2(a0, a1));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -534,6 +560,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (!mbar_wait(&sm.dkv_full, items_done & 1, abort_flag, hdr)) break;
       tc_fence_after();
       {
+        const int64_t key = (int64_t)it.ktile * 128 + r;
         const bool is_dk = cg >= 2;
         const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
         const float scale = is_dk ? p.scale : 1.f;
