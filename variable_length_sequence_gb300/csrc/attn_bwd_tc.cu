@@ -163,13 +163,16 @@ struct KvItem {
 struct __align__(1024) SmemKV {
   uint8_t k[kTile];
   uint8_t v[kTile];
-  uint8_t q[2][kTile];
-  uint8_t dout[2][kTile];
+  // Q / dOut pool: Q of step j in slot j % 4, dOut of step j in slot
+  // (j + 2) % 4, both the (j / 2)-th fill of their slot.  Every slot
+  // alternates Q and dOut roles, so Q of step j + 2 lands in the slot that
+  // dOut of step j frees in the middle of step j (after dV), not in the one
+  // Q of step j frees at its end (after dK).
+  uint8_t qd[4][kTile];
   uint8_t ds[kTile];            // dS^T, [q-block][key][64 q], 128-byte swizzle
-  float nlse2[2][128];           // loaded with Q
-  float delta[2][128];          // loaded with Q
+  float vec[4][128];            // -lse log2(e) with a Q tile, delta with a dOut tile
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
+  uint64_t slot_full[4], slot_empty[4];
   uint64_t s_full, dp_full, dp_free, ds_ready, dk_done;
   uint64_t p_ready[2], dv_done[2];
   uint64_t dkv_full, dkv_empty;
@@ -197,11 +200,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&sm.slot_full[s], 1);
+      // one commit from each stream (Q: S^T, dK; dOut: dP^T, dV) and one
+      // arrival per softmax warp (its lse or delta read)
+      mbar_init(&sm.slot_empty[s], 2 + kKvSoftmaxWarps);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.q_full[s], 1);
-      mbar_init(&sm.q_empty[s], 1);          // dK (stream 2) is the last reader of Q
-      mbar_init(&sm.do_full[s], 1);
-      mbar_init(&sm.do_empty[s], 2);         // dP^T (stream 1) and dV (stream 2) read dOut
       mbar_init(&sm.p_ready[s], kKvSoftmaxWarps);
       mbar_init(&sm.dv_done[s], 1);
       mbar_init(&sm.item_full[s], 1);
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (warp == kKvWarpProducer) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        uint32_t it_count = 0, kv_count = 0, q_count = 0, do_count = 0;
+        uint32_t it_count = 0, kv_count = 0, q_count = 0, loads = 0;
         bool ok = true;
         while (ok) {
           const int idx = atomicAdd(&hdr->counter2, 1);
@@ -282,38 +287,44 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const int hh = n / it.n_q;
             const int h = it.g * G + hh;
             const int i = it.i_lo + (n - hh * it.n_q);
-            const uint32_t st = q_count & 1, use = q_count >> 1;
-            if (use >= 1 && !mbar_wait(&sm.q_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            const uint32_t fill = q_count >> 1;             // fill index of both slots
+            const uint32_t sq = q_count & 3, sd = (q_count + 2) & 3;
+            if (q_count >= 2 &&
+                !mbar_wait(&sm.slot_empty[sq], (fill - 1) & 1, abort_flag, hdr)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.q_full[st], kTile + 2 * 128 * sizeof(float));
+            mbar_arrive_expect_tx(&sm.slot_full[sq], kTile + 128 * sizeof(float));
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.q[st] + cb * kBlk, &tm_q, &sm.q_full[st], h * HD + cb * 64, i * 128);
-            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
-            bulk_load(sm.nlse2[st], a.nlse2 + row, 128 * sizeof(float), &sm.q_full[st]);
-            bulk_load(sm.delta[st], a.delta + row, 128 * sizeof(float), &sm.q_full[st]);
-            ++q_count;
-            if (use >= 1 && !mbar_wait(&sm.do_empty[st], (use - 1) & 1, abort_flag, hdr)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&sm.do_full[st], kTile);
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.dout[st] + cb * kBlk, &tm_do, &sm.do_full[st], h * HD + cb * 64,
+              tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], h * HD + cb * 64,
                           i * 128);
-            ++do_count;
+            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
+            bulk_load(sm.vec[sq], a.nlse2 + row, 128 * sizeof(float), &sm.slot_full[sq]);
+            ++loads;
+            if (q_count >= 2 &&
+                !mbar_wait(&sm.slot_empty[sd], (fill - 1) & 1, abort_flag, hdr)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.slot_full[sd], kTile + 128 * sizeof(float));
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d(sm.qd[sd] + cb * kBlk, &tm_do, &sm.slot_full[sd], h * HD + cb * 64,
+                          i * 128);
+            bulk_load(sm.vec[sd], a.delta + row, 128 * sizeof(float), &sm.slot_full[sd]);
+            ++loads;
+            ++q_count;
           }
         }
         if (!ok) {
           // abort: every copy issued so far completes on its stage barrier
           if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
-          for (uint32_t j = (q_count > 2 ? q_count - 2 : 0); j < q_count; ++j)
-            drain_wait(&sm.q_full[j & 1], (j >> 1) & 1);
-          for (uint32_t j = (do_count > 2 ? do_count - 2 : 0); j < do_count; ++j)
-            drain_wait(&sm.do_full[j & 1], (j >> 1) & 1);
+          // load l: step l / 2, Q (l even) or dOut (l odd)
+          for (uint32_t l = (loads > 4 ? loads - 4 : 0); l < loads; ++l) {
+            const uint32_t j = l >> 1;
+            drain_wait(&sm.slot_full[(l & 1) ? ((j + 2) & 3) : (j & 3)], (j >> 1) & 1);
+          }
         }
       }
     } else if (warp == kKvWarpMma1) {
@@ -333,23 +344,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (it.steps < 0) break;
           if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
           for (int n = 0; n < it.steps; ++n) {
-            const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
-            if (!mbar_wait(&sm.q_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
+            if (!mbar_wait(&sm.slot_full[sq], fp, abort_flag, hdr)) { ok = false; break; }
             // region rb held the previous dP^T: free once the softmax has read it
             if (qc >= 1 && !mbar_wait(&sm.dp_free, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
             tc_fence_after();
-            mma_kk(tmem + 128 * rb, k_s, smem_u32(sm.q[st]), false);          // S^T = K Q^T
+            mma_kk(tmem + 128 * rb, k_s, smem_u32(sm.qd[sq]), false);         // S^T = K Q^T
             mma_commit(&sm.s_full);
-            if (!mbar_wait(&sm.do_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            mma_commit(&sm.slot_empty[sq]);
+            if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
             // region rb ^ 1 held the previous P^T: free once dV has read it
             if (qc >= 1 && !mbar_wait(&sm.dv_done[rb ^ 1], ((qc - 1) >> 1) & 1, abort_flag, hdr)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_kk(tmem + 128 * (rb ^ 1), v_s, smem_u32(sm.dout[st]), false);  // dP^T = V dOut^T
+            mma_kk(tmem + 128 * (rb ^ 1), v_s, smem_u32(sm.qd[sd]), false);   // dP^T = V dOut^T
             mma_commit(&sm.dp_full);
-            mma_commit(&sm.do_empty[st]);
+            mma_commit(&sm.slot_empty[sd]);
             ++qc;
           }
           if (!ok) break;
@@ -371,25 +383,25 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           ++it_count;
           if (it.steps < 0) break;
           for (int n = 0; n < it.steps; ++n) {
-            const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
-            if (!mbar_wait(&sm.p_ready[rb], use & 1, abort_flag, hdr)) { ok = false; break; }
+            const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
+            if (!mbar_wait(&sm.p_ready[rb], fp, abort_flag, hdr)) { ok = false; break; }
             if (n == 0 && items_done > 0 &&
                 !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
               ok = false;
               break;
             }
-            if (!mbar_wait(&sm.do_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
             tc_fence_after();
             const bool acc = n > 0;
-            mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.dout[st]), acc);   // dV += P^T dOut
+            mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
             mma_commit(&sm.dv_done[rb]);
-            mma_commit(&sm.do_empty[st]);
+            mma_commit(&sm.slot_empty[sd]);
             if (!mbar_wait(&sm.ds_ready, qc & 1, abort_flag, hdr)) { ok = false; break; }
             tc_fence_after();
             {
               // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
               const uint64_t ad = smem_desc_sw128(ds_s, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(smem_u32(sm.q[st]), kBlk, 1024);
+              const uint64_t bd = smem_desc_sw128(smem_u32(sm.qd[sq]), kBlk, 1024);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t aoff = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
@@ -398,7 +410,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               }
             }
             mma_commit(&sm.dk_done);
-            mma_commit(&sm.q_empty[st]);
+            mma_commit(&sm.slot_empty[sq]);
             ++qc;
           }
           if (!ok) break;
@@ -452,10 +464,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       for (int n = 0; n < it.steps; ++n) {
         const int hh = n / it.n_q;
         const int q0 = (it.i_lo + (n - hh * it.n_q)) * 128 + cg * 32;
-        const uint32_t st = qc & 1, use = qc >> 1, rb = qc & 1;
+        const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
         const uint32_t s_tm = tmem + lane_base + 128 * rb + cg * 32;
         const uint32_t dp_tm = tmem + lane_base + 128 * (rb ^ 1) + cg * 32;
-        if (!mbar_wait(&sm.q_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait(&sm.slot_full[sq], fp, abort_flag, hdr)) { ok = false; break; }
         if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
         uint32_t x[32];
@@ -463,7 +475,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_ld16x256_x4(s_tm + (16u << 16), x + 16);
         uint64_t nl[4];                                     // -lse log2(e) column pairs
         {
-          const float* src = sm.nlse2[st] + cg * 32 + tc2;
+          const float* src = sm.vec[sq] + cg * 32 + tc2;
 #pragma unroll
           for (int j = 0; j < 4; ++j) nl[j] = *reinterpret_cast<const uint64_t*>(src + 8 * j);
         }
@@ -519,15 +531,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_ready[rb]);
+        if (lane == 0) {
+          mbar_arrive(&sm.p_ready[rb]);
+          mbar_arrive(&sm.slot_empty[sq]);                  // lse read
+        }
         // phase 2: dS = P (dP - delta); masked P is zero, so dS is too
+        if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
         if (!mbar_wait(&sm.dp_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
         tc_fence_after();
         tmem_ld16x256_x4(dp_tm, x);
         tmem_ld16x256_x4(dp_tm + (16u << 16), x + 16);
         uint64_t dd[4];                                     // delta column pairs
         {
-          const float* src = sm.delta[st] + cg * 32 + tc2;
+          const float* src = sm.vec[sd] + cg * 32 + tc2;
 #pragma unroll
           for (int j = 0; j < 4; ++j) dd[j] = *reinterpret_cast<const uint64_t*>(src + 8 * j);
         }
@@ -551,7 +567,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ds_ready);
+        if (lane == 0) {
+          mbar_arrive(&sm.ds_ready);
+          mbar_arrive(&sm.slot_empty[sd]);                  // delta consumed
+        }
         ++qc;
       }
       if (!ok) break;
