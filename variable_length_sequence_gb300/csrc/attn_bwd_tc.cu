@@ -115,9 +115,10 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  for (int i = 0; i < 2; ++i)
+    st_global_v8(dst + 16 * i, w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3], w[8 * i + 4],
+                 w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
 }
 
 // 1024-aligned view of dynamic shared memory, or nullptr (error recorded)

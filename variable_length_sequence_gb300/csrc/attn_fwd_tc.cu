@@ -124,7 +124,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Store 32 consecutive output elements of one row (raw float32 bits in v).
+// Store 32 consecutive output elements of one row (raw float32 bits in v),
+// 32 bytes per instruction and lane (whole sectors); dst is 32-byte aligned
+// (rows are 256 or 512 bytes, chunks 64 or 128).
 template <typename TO>
 __device__ __forceinline__ void store_row_chunk(TO* dst, const uint32_t (&v)[32], float scale);
 
@@ -136,20 +138,22 @@ __device__ __forceinline__ void store_row_chunk<__nv_bfloat16>(__nv_bfloat16* ds
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  for (int i = 0; i < 2; ++i)
+    st_global_v8(dst + 16 * i, w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3], w[8 * i + 4],
+                 w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
 }
 
 template <>
 __device__ __forceinline__ void store_row_chunk<float>(float* dst, const uint32_t (&v)[32],
                                                        float scale) {
-  float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    d4[i] = make_float4(__uint_as_float(v[4 * i]) * scale, __uint_as_float(v[4 * i + 1]) * scale,
-                        __uint_as_float(v[4 * i + 2]) * scale,
-                        __uint_as_float(v[4 * i + 3]) * scale);
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__uint_as_float(v[8 * i + k]) * scale);
+    st_global_v8(dst + 8 * i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+  }
 }
 
 template <typename TO>
@@ -467,19 +471,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sm.o_full[t], o_count & 1, abort_flag, hdr)) break;
         ++o_count;
         tc_fence_after();
+        if constexpr (sizeof(TO) == 4) {
+          // float32 rows: read O as 16-lane fragments so that the four lanes
+          // of a row write 32 contiguous bytes and consecutive stores of a
+          // warp continue the same 8 rows; thread t holds rows 8 i + t/4 of
+          // the warp's 32 (i = 0..3)
+          float invr[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t orow[32];
-          tmem_ld32(o_tm + c * 32, orow);
-          tmem_wait_ld();
-          if (valid) store_row_chunk<TO>(dst + c * 32, orow, inv);
+          for (int i = 0; i < 4; ++i) invr[i] = __shfl_sync(0xffffffffu, inv, 8 * i + (lane >> 2));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t x[32];
+            tmem_ld16x256_x4(o_tm + c * 32, x);
+            tmem_ld16x256_x4(o_tm + (16u << 16) + c * 32, x + 16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int i = 2 * (k >> 3) + (k & 1);
+              const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + 8 * i + (lane >> 2);
+              if (grow < p.q_len) {
+                float2* d = reinterpret_cast<float2*>(
+                    out + (grow * p.Hq + h) * HD + c * 32 + 8 * ((k >> 1) & 3) + 2 * (lane & 3));
+                *d = make_float2(__uint_as_float(x[2 * k]) * invr[i],
+                                 __uint_as_float(x[2 * k + 1]) * invr[i]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(o_tm + c * 32, orow);
+            tmem_wait_ld();
+            if (valid) store_row_chunk<TO>(dst + c * 32, orow, inv);
+          }
         }
-      } else if (valid) {
-        uint32_t z[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) store_row_chunk<TO>(dst + c * 32, z, 0.f);
+      } else {
+        // no key of the range is visible to any row of the tile: zero rows,
+        // each written whole by a warp (16-byte lanes, full sectors)
+        constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
+        constexpr int kRowsPerPass = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += kRowsPerPass) {
+          const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + rr + sub;
+          if (grow < p.q_len)
+            reinterpret_cast<uint4*>(out + (grow * p.Hq + h) * HD)[part] = make_uint4(0, 0, 0, 0);
+        }
       }
       if (valid && p.lse != nullptr)
         p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;

@@ -244,6 +244,14 @@ __device__ __forceinline__ void tmem_st16x128_x4(uint32_t taddr, const uint32_t*
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
+// 32-byte store (one whole sector per lane); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5,
+                                             uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a0), "r"(a1),
+               "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
 __device__ __forceinline__ void st_shared_u32(uint32_t saddr, uint32_t a) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(a) : "memory");
 }
