@@ -9,8 +9,9 @@
 //
 // HBM-bound: every partial row is read once (float4 per lane), the merged
 // row written once.  A warp walks 32 consecutive tokens of one head so the
-// lse reads ([H, T] layout) are warp-coalesced and reused from L1; the
-// row-wise weights are computed once per row per warp.
+// lse reads ([H, T] layout) are warp-coalesced and reused from L1; it loads
+// 4 row groups of every partial before combining them, so each lane keeps
+// several independent loads in flight.
 #include "nsp_internal.cuh"
 
 namespace nsp {
@@ -48,7 +49,7 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
 }
 
 template <typename TO>
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(MergePtrs ptrs, int n,
+__global__ void __launch_bounds__(kMergeThreads, 2) lse_merge_kernel(MergePtrs ptrs, int n,
                                                                   int64_t T, int H, int d,
                                                                   TO* __restrict__ out,
                                                                   float* __restrict__ lse_out) {
@@ -73,6 +74,54 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(MergePtrs ptrs
     }
     if (tl < T && lse_out != nullptr) lse_out[(int64_t)h * T + tl] = L;
     const int rows = (int)min((int64_t)32, T - t0);
+    if (32 % d4 == 0) {
+      // 32 / d4 rows per warp load; RB of those loads per partial in flight
+      constexpr int RB = 4;
+      const int rpi = 32 / d4;
+      const int sub = lane / d4, c = lane % d4;
+      for (int r0 = 0; r0 < rows; r0 += RB * rpi) {
+        float4 acc[RB];
+        float Lr[RB];
+        int64_t off[RB];
+        int rr[RB];
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+          rr[k] = r0 + k * rpi + sub;
+          Lr[k] = __shfl_sync(0xffffffffu, L, rr[k] & 31);
+          if (rr[k] >= rows) Lr[k] = -INFINITY;
+          off[k] = ((t0 + rr[k]) * H + h) * (int64_t)d + 4 * c;
+          acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 2
+        for (int i = 0; i < n; ++i) {
+          const float* lsei = ptrs.lse[i] + (int64_t)h * T + t0;
+          const float* oi = ptrs.out[i];
+          float4 o[RB];
+          float li[RB];
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            li[k] = -INFINITY;
+            o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (Lr[k] != -INFINITY) {
+              li[k] = __ldg(lsei + rr[k]);
+              o[k] = ld_stream4(oi + off[k]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < RB; ++k) {
+            const float w = Lr[k] != -INFINITY ? expf(li[k] - Lr[k]) : 0.f;
+            acc[k].x = fmaf(w, o[k].x, acc[k].x);
+            acc[k].y = fmaf(w, o[k].y, acc[k].y);
+            acc[k].z = fmaf(w, o[k].z, acc[k].z);
+            acc[k].w = fmaf(w, o[k].w, acc[k].w);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < RB; ++k)
+          if (rr[k] < rows) st4<TO>(out + off[k], acc[k]);
+      }
+      continue;
+    }
     for (int r = 0; r < rows; ++r) {
       const float Lr = __shfl_sync(0xffffffffu, L, r);
       const int64_t t = t0 + r;
