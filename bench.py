@@ -18,10 +18,13 @@ bf16 inputs, float32 accumulation):
 by the step time; masked work is never counted.  Per-leg times, TFLOP/s and
 GB/s and the roofline of the dominant kernel are reported beside it.
 
-Timing: W warm-up steps, then K steps, each preceded (outside its timed
-region) by an L2 flush (a 256 MiB write, larger than the 129 MB L2), each
-timed with CUDA events on the launching stream; barrier + synchronize on
-both sides; max over ranks.  ``--impl reference`` times the fp64 CPU oracle
+Timing: W warm-up steps; the C-ABI calls of each leg are then recorded once
+as a CUDA graph and replayed (the library allocates nothing and its calls are
+stream-ordered, so a leg's kernels launch back to back); K steps, each
+preceded (outside its timed region) by an L2 flush (a 256 MiB write, larger
+than the 129 MB L2), each timed with CUDA events on the launching stream;
+barrier + synchronize on both sides; max over ranks.  ``gpu_launches`` is
+the library kernels one step records times K.  ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
@@ -296,9 +299,33 @@ class Problem:
         for i, leg in enumerate(self.LEGS):
             if events is not None:
                 events[i][0].record(stream)
-            getattr(self, leg)(stream)
+            if self.graphs is not None:
+                self.graphs[leg].replay()
+            else:
+                getattr(self, leg)(stream)
             if events is not None:
                 events[i][1].record(stream)
+
+    graphs = None
+    launches_per_step = None
+
+    def capture(self, stream):
+        """Record each leg's C-ABI calls once as a CUDA graph (the kernels of a
+        leg then launch back to back on replay).  Returns the number of
+        library kernels one step launches."""
+        self.graphs = {}
+        n0 = self.nsp.nsp_kernel_launches()
+        side = torch.cuda.Stream(stream.device)
+        side.wait_stream(stream)
+        for leg in self.LEGS:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                getattr(self, leg)(side)
+            self.graphs[leg] = g
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        self.launches_per_step = self.nsp.nsp_kernel_launches() - n0
+        return self.launches_per_step
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -328,13 +355,17 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         prob.step(stream)
     torch.cuda.synchronize()
+    launches_per_step = prob.capture(stream)  # legs replayed as CUDA graphs from here on
+    for _ in range(2):
+        flush.zero_()
+        prob.step(stream)
+    torch.cuda.synchronize()
 
     K = args.steps
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
     leg_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(nlegs)] for _ in range(K)]
-    launches0 = nsp.nsp_kernel_launches()
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -349,7 +380,9 @@ def run_ours(args, world, rank, local):
     wall = wall1 - wall0
     clocks.mark(wall0, wall1)
     clk = clocks.stop()
-    launches = nsp.nsp_kernel_launches() - launches0
+    # graph replays do not pass through the library's host launch counter:
+    # the kernels of one step were counted while the graphs were recorded
+    launches = launches_per_step * K
 
     step_ms = [s.elapsed_time(e) for s, e in step_ev]
     leg_ms = np.array([[s.elapsed_time(e) for s, e in legs] for legs in leg_ev])  # [K, nlegs]
@@ -431,7 +464,11 @@ def run_e2e(args, prob, nsp, w, device, stream, world):
     device buffers, a copy-in stream, the compute stream and a copy-out
     stream, so the copies of neighbouring steps overlap a step's compute.
     The time is from the first copy-in to the last copy-out."""
-    probs = (prob, Problem(nsp, w, device))
+    prob2 = Problem(nsp, w, device)
+    prob2.step(stream)                      # warm (lazy buffers), then record its graphs
+    torch.cuda.synchronize()
+    prob2.capture(stream)
+    probs = (prob, prob2)
     host_in = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "dout")}
     host_cu = torch.from_numpy(w.cu_seqlens).pin_memory()
     outs = {n: torch.empty(getattr(prob, n).shape, dtype=getattr(prob, n).dtype).pin_memory()
