@@ -13,19 +13,23 @@
 //
 // Mode 0 (forward / backward dQ view): tile i covers query rows
 //   [q_start + 128 i, ...) and lists the key sub-tiles j (keys
-//   [kv_start + gran j, ...), gran = 128 forward, 64 backward) its rows see.
+//   [kv_start + gran j, ...), gran = 128) its rows see.
 // Mode 1 (backward dK/dV view): tile j covers keys [128 j, ...) of the whole
 //   stream and lists the query sub-tiles (rows [gran i, ...)) whose rows can
 //   see any of those keys.
 //
 // One block of 1024 threads; the first mode-0 launch of a call validates
-// cu_seqlens and resets the workspace status word.
+// cu_seqlens and resets the workspace status word.  The counting-sort
+// histogram lives in shared memory when it fits (it almost always does), and
+// the descending-cost scan is a warp-shuffle scan: the kernel is a handful of
+// block barriers long.
 #include "nsp_internal.cuh"
 
 namespace nsp {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+constexpr int kSmemBuckets = 12 * 1024;    // 48 KB of counting-sort buckets in shared memory
 
 struct SchedArgs {
   const int32_t* cu;
@@ -45,10 +49,12 @@ struct SchedArgs {
 };
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
+  extern __shared__ int s_hist_dyn[];       // n_buckets ints when they fit
   __shared__ int s_bad;
   __shared__ int s_max;
-  __shared__ int s_scan[kSchedThreads];
-  const int tid = threadIdx.x;
+  __shared__ int s_warp[kSchedThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int* const hist = a.n_buckets <= kSmemBuckets ? s_hist_dyn : a.hist;
   if (tid == 0) { s_bad = 0; s_max = 0; }
   __syncthreads();
 
@@ -76,7 +82,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     return;
   }
 
-  for (int i = tid; i < a.n_buckets; i += kSchedThreads) a.hist[i] = 0;
+  for (int i = tid; i < a.n_buckets; i += kSchedThreads) hist[i] = 0;
   __syncthreads();
 
   const int64_t q_end = a.q_start + a.q_len, kv_end = a.kv_start + a.kv_len;
@@ -103,7 +109,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     }
     a.tiles[i] = make_int2(lo_t, hi_t);
     const int cost = hi_t - lo_t + 1;
-    atomicAdd(&a.hist[cost], 1);
+    atomicAdd(&hist[cost], 1);
     atomicMax(&s_max, cost);
   }
   __syncthreads();
@@ -113,33 +119,48 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   const int per = (a.n_buckets + kSchedThreads - 1) / kSchedThreads;
   const int r_begin = tid * per, r_end = min(r_begin + per, a.n_buckets);
   int local = 0;
-  for (int r = r_begin; r < r_end; ++r) local += a.hist[a.n_buckets - 1 - r];
-  s_scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < kSchedThreads; off <<= 1) {
-    const int add = tid >= off ? s_scan[tid - off] : 0;
-    __syncthreads();
-    s_scan[tid] += add;
-    __syncthreads();
+  for (int r = r_begin; r < r_end; ++r) local += hist[a.n_buckets - 1 - r];
+  // block-wide inclusive scan of `local`: within warps, then over warp totals
+  int x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  int run = s_scan[tid] - local;          // exclusive prefix of this thread's run
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  int run = x - local + (wid > 0 ? s_warp[wid - 1] : 0);   // exclusive prefix of my run
   for (int r = r_begin; r < r_end; ++r) {
     const int c = a.n_buckets - 1 - r;
-    const int h = a.hist[c];
-    a.hist[c] = run;
+    const int h = hist[c];
+    hist[c] = run;
     run += h;
   }
   __syncthreads();
 
   for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
     const int2 t = a.tiles[i];
-    const int pos = atomicAdd(&a.hist[t.y - t.x + 1], 1);
+    const int pos = atomicAdd(&hist[t.y - t.x + 1], 1);
     a.order[pos] = i;
   }
   if (tid == 0) {
     if (a.second) { a.hdr->counter2 = 0; a.hdr->n_items2 = a.n_tiles; }
     else { a.hdr->counter = 0; a.hdr->n_items = a.n_tiles; a.hdr->max_cost = s_max; }
   }
+}
+
+size_t sched_smem(const SchedArgs& a) {
+  return a.n_buckets <= kSmemBuckets ? sizeof(int) * (size_t)a.n_buckets : 0;
 }
 
 }  // namespace
@@ -157,13 +178,13 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
   a.n_tiles = (int32_t)L.n_qtiles;
   a.n_buckets = (int32_t)L.n_kvtiles + 2;
   a.hdr = p.hdr; a.second = 0;
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
                                  cudaStream_t s) {
-  // query tiles of 128 rows listing 64-key sub-tiles (validates cu_seqlens)
+  // query tiles of 128 rows listing 128-key tiles (validates cu_seqlens)
   SchedArgs a;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = 0; a.q_len = p.q_len; a.kv_start = 0; a.kv_len = p.kv_len;
@@ -174,10 +195,10 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.n_tiles = (int32_t)L.n_qtiles;
   a.n_buckets = (int32_t)L.n_sub + 2;
   a.hdr = p.hdr; a.second = 0;
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // key tiles of 128 keys listing 64-row query sub-tiles
+  // key tiles of 128 keys listing 128-row query tiles
   a.mode = 1; a.validate = 0;
   a.tiles = reinterpret_cast<int2*>(ws + L.ktiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.korder);
@@ -185,7 +206,7 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.n_tiles = (int32_t)L.n_ktiles;
   a.n_buckets = (int32_t)L.n_sub + 2;
   a.hdr = p.hdr; a.second = 1;
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a); count_launches(1);
+  schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   return cudaGetLastError();
 }
 
