@@ -192,6 +192,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
+  grid_dep_wait();                          // delta and -lse log2(e) of bwd_delta_kernel
+  grid_dep_trigger();                       // the dQ kernel may launch on SMs this one frees
   if (status_bad(hdr)) return;
   SmemKV* smp = smem_view<SmemKV>(smem_raw, hdr);
   if (smp == nullptr) return;
@@ -655,9 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
-  if (status_bad(hdr)) return;
+  // Launched behind the dK/dV kernel, which triggers only after its own
+  // wait: everything this kernel reads (schedules, delta, -lse log2(e)) is
+  // complete.  It reads nothing the dK/dV kernel writes, so it starts on the
+  // SMs that kernel frees and waits for it only before it exits (work after
+  // this call in the stream then also follows the dK/dV kernel).
+  if (status_bad(hdr)) {
+    grid_dep_wait();
+    return;
+  }
   SmemQ* smp = smem_view<SmemQ>(smem_raw, hdr);
-  if (smp == nullptr) return;
+  if (smp == nullptr) {
+    grid_dep_wait();
+    return;
+  }
   SmemQ& sm = *smp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -974,6 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  grid_dep_wait();
 }
 
 // ================================================================ host
@@ -1047,12 +1061,14 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)q_bytes);
   if (e != cudaSuccess) return e;
-  attn_bwd_dkdv_tc_kernel<<<grid, kKvThreads, kv_bytes, s>>>(mq, mdo, mk, mv, a);
+  e = launch_dependent(attn_bwd_dkdv_tc_kernel, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq,
+                       mdo, mk, mv, a);
   count_launches(1);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<<<grid, kThreads, q_bytes, s>>>(mq, mdo, mk, mv, a);
+  e = launch_dependent(attn_bwd_dq_tc_kernel, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo,
+                       mk, mv, a);
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

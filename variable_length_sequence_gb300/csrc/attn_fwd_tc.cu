@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* hdr = p.hdr;
+  grid_dep_wait();                          // the schedule kernel's lists and status
   if (status_bad(hdr)) return;
 
   if (threadIdx.x == 0) {
@@ -569,10 +570,11 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = num_sms();
-  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p,
-                                          reinterpret_cast<const int2*>(ws + L.tiles),
-                                          reinterpret_cast<const int*>(ws + L.order));
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, mq, mk, mv, p,
+                       reinterpret_cast<const int2*>(ws + L.tiles),
+                       reinterpret_cast<const int*>(ws + L.order));
   count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

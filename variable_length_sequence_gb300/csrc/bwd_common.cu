@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
   constexpr int TPR = D / VEC;                  // 16 (bf16, d=128) ... 32 (f32, d=128)
   constexpr int RPW = 32 / TPR;                 // rows per warp step
   static_assert(TPR <= 32 && 32 % TPR == 0, "row split");
+  grid_dep_trigger();                       // the dK/dV kernel may launch (it waits)
   if (status_bad(hdr)) return;
   const int lane = threadIdx.x & 31;
   const int sub = lane / TPR, part = lane % TPR;

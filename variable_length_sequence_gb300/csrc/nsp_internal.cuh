@@ -160,5 +160,32 @@ __device__ __forceinline__ bool status_bad(const WsHeader* hdr) {
   return *((volatile const int32_t*)&hdr->status) != 0;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_dependent may
+// start while the kernel before it in the stream is still running, as soon as
+// every CTA of that kernel has executed grid_dep_trigger() (or exited); it
+// must execute grid_dep_wait() before it reads anything that kernel (or one
+// before it) wrote: the wait returns once that kernel has completed and its
+// writes are visible.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace nsp
 #endif

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   __shared__ int s_warp[kSchedThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int* const hist = a.n_buckets <= kSmemBuckets ? s_hist_dyn : a.hist;
+  grid_dep_trigger();                       // the attention kernel may launch (it waits)
   if (tid == 0) { s_bad = 0; s_max = 0; }
   __syncthreads();
 
