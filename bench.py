@@ -48,7 +48,14 @@ sys.path.insert(0, ROOT)
 from variable_length_sequence_gb300.workloads import CONFIGS, make_workload, shard_bounds  # noqa: E402
 
 METRIC = "varlen attn fwd+bwd useful TFLOP/s & % bf16 peak; merge/permute GB/s % HBM"
-CONFIG_ID = 2
+CONFIG_ID = 2                      # the bench workload; --config 3/4/5 time other configs
+# legs timed per config: config 3 is the ring-style chunked forward plus the
+# permutation; configs 2, 4 and 5 are forward + backward (config 2 also runs
+# the ring legs and the permutation on its own 32768-token stream)
+CONFIG_LEGS = {2: ("fwd", "bwd", "ring_partials", "merge", "permute"),
+               3: ("ring_partials", "merge", "permute"),
+               4: ("fwd", "bwd"),
+               5: ("fwd", "bwd")}
 RING_SHARDS = 8
 PERMUTE_GROUPS = 8
 L2_FLUSH_BYTES = 256 << 20
@@ -198,8 +205,9 @@ def allowed_pairs_blocks(cu: np.ndarray, bounds):
 class Problem:
     """Device-resident inputs, outputs and workspaces of one step."""
 
-    def __init__(self, nsp, w, device):
+    def __init__(self, nsp, w, device, legs=CONFIG_LEGS[CONFIG_ID]):
         self.nsp = nsp
+        self.LEGS = tuple(legs)
         self.w = w
         cfg = w.cfg
         self.T, self.Hq, self.Hkv, self.d = w.T, cfg.Hq, cfg.Hkv, cfg.d
@@ -208,22 +216,24 @@ class Problem:
         self.q = w.q.to(dev)
         self.k = w.k.to(dev)
         self.v = w.v.to(dev)
-        self.dout = w.dout.to(dev)
+        self.dout = w.dout.to(dev) if w.dout is not None else None
         self.cu = torch.from_numpy(w.cu_seqlens).to(dev)
         T, Hq, Hkv, d = self.T, self.Hq, self.Hkv, self.d
         bf = torch.bfloat16
         self.out = torch.empty((T, Hq, d), dtype=bf, device=dev)
         self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-        self.dq = torch.empty_like(self.q)
-        self.dk = torch.empty_like(self.k)
-        self.dv = torch.empty_like(self.v)
+        has_bwd = "bwd" in self.LEGS
+        self.dq = torch.empty_like(self.q) if has_bwd else None
+        self.dk = torch.empty_like(self.k) if has_bwd else None
+        self.dv = torch.empty_like(self.v) if has_bwd else None
         self.ws_f = torch.empty(nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d),
                                 dtype=torch.uint8, device=dev)
-        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, nsp.NSP_BF16),
-                                dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, nsp.NSP_BF16)
+                                if has_bwd else 16, dtype=torch.uint8, device=dev)
         # ring legs
         self.bounds = shard_bounds(T, RING_SHARDS)
-        self.ring_pairs = allowed_pairs_blocks(w.cu_seqlens, self.bounds)
+        self.ring_pairs = (allowed_pairs_blocks(w.cu_seqlens, self.bounds)
+                           if "ring_partials" in self.LEGS else [])
         n = T // RING_SHARDS
         self.part_o = {(qs, ks): torch.empty((n, Hq, d), dtype=torch.float32, device=dev)
                        for qs, ks, _ in self.ring_pairs}
@@ -231,24 +241,30 @@ class Problem:
                        for qs, ks, _ in self.ring_pairs}
         self.ws_r = torch.empty(nsp.nsp_attn_fwd_workspace_size(n, n, Hq, Hkv, d),
                                 dtype=torch.uint8, device=dev)
-        self.merged_o = torch.empty((T, Hq, d), dtype=bf, device=dev)
+        ring = bool(self.ring_pairs)
+        self.acc_o = torch.empty((T, Hq, d), dtype=torch.float32, device=dev) if ring else None
+        self.acc_l = [torch.empty((Hq, n), dtype=torch.float32, device=dev)
+                      for _ in range(RING_SHARDS)] if ring else None
+        self.merged_o = torch.empty((T, Hq, d), dtype=bf, device=dev) if ring else None
         self.merged_l = torch.empty((Hq, T), dtype=torch.float32, device=dev)
         # permutation
+        perm = "permute" in self.LEGS
         self.perm = torch.empty((PERMUTE_GROUPS, T, Hq // PERMUTE_GROUPS, d), dtype=bf,
-                                device=dev)
-        self.unperm = torch.empty_like(self.q)
+                                device=dev) if perm else None
+        self.unperm = torch.empty_like(self.q) if perm else None
         # work accounting
         self.pairs = nsp.nsp_attn_pairs(w.cu_seqlens, True)
-        self.fwd_flop = 4.0 * d * Hq * self.pairs
-        self.bwd_flop = 10.0 * d * Hq * self.pairs
+        self.fwd_flop = 4.0 * d * Hq * self.pairs if "fwd" in self.LEGS else 0.0
+        self.bwd_flop = 10.0 * d * Hq * self.pairs if has_bwd else 0.0
         self.ring_flop = 4.0 * d * Hq * sum(c for _, _, c in self.ring_pairs)
         nb = lambda t: t.numel() * t.element_size()
         self.merge_bytes = 0
         for qs in range(RING_SHARDS):
             parts = [(a, b) for a, b, _ in self.ring_pairs if a == qs]
             self.merge_bytes += sum(nb(self.part_o[p]) + nb(self.part_l[p]) for p in parts)
-        self.merge_bytes += nb(self.merged_o) + nb(self.merged_l)
-        self.permute_bytes = 2 * (nb(self.q) + nb(self.perm))   # read + write, both ways
+        if ring:
+            self.merge_bytes += nb(self.merged_o) + nb(self.merged_l)
+        self.permute_bytes = 2 * (nb(self.q) + nb(self.perm)) if perm else 0  # read + write, both ways
 
     # individual legs -------------------------------------------------------------
     def fwd(self, stream):
@@ -279,6 +295,24 @@ class Problem:
                                    [self.part_l[p] for p in keys],
                                    self.merged_o[qa:qa + n], self.merged_l_view(qs), stream)
 
+    def ring_accumulate(self, stream):
+        """The ring legs with the merge fused into the attention epilogue: per
+        query shard the first block is a plain float32 partial (it writes the
+        running result), every later block is merged into it in place by
+        nsp_attn_fwd_accumulate.  Result: float32 out and lse per shard."""
+        n = self.T // RING_SHARDS
+        started = set()
+        for qs, ks, _ in self.ring_pairs:
+            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
+            args = (self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n], self.cu,
+                    len(self.w.lengths), qa, n, ka, n, self.Hq, self.Hkv, self.d, self.scale,
+                    True, self.acc_o[qa:qa + n], self.acc_l[qs], self.ws_r, stream)
+            if qs in started:
+                self.nsp.nsp_attn_fwd_accumulate(*args)
+            else:
+                self.nsp.nsp_attn_fwd(*args)
+                started.add(qs)
+
     def merged_l_view(self, qs):
         # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
         if not hasattr(self, "_ml"):
@@ -292,8 +326,6 @@ class Problem:
                                       PERMUTE_GROUPS, False, stream)
         self.nsp.nsp_seq2head_permute(self.perm, self.unperm, self.T, self.Hq, self.d,
                                       PERMUTE_GROUPS, True, stream)
-
-    LEGS = ("fwd", "bwd", "ring_partials", "merge", "permute")
 
     def step(self, stream, events=None):
         for i, leg in enumerate(self.LEGS):
@@ -309,7 +341,7 @@ class Problem:
     graphs = None
     launches_per_step = None
 
-    def capture(self, stream):
+    def capture(self, stream, legs=None):
         """Record each leg's C-ABI calls once as a CUDA graph (the kernels of a
         leg then launch back to back on replay).  Returns the number of
         library kernels one step launches."""
@@ -317,7 +349,7 @@ class Problem:
         n0 = self.nsp.nsp_kernel_launches()
         side = torch.cuda.Stream(stream.device)
         side.wait_stream(stream)
-        for leg in self.LEGS:
+        for leg in legs or self.LEGS:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
                 getattr(self, leg)(side)
@@ -342,11 +374,12 @@ def run_ours(args, world, rank, local):
     barrier(world)
     nsp.load()
 
-    w = make_workload(CONFIG_ID)
-    prob = Problem(nsp, w, device)
+    cid = args.config
+    w = make_workload(cid)
+    prob = Problem(nsp, w, device, CONFIG_LEGS[cid])
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    nlegs = len(Problem.LEGS)
+    nlegs = len(prob.LEGS)
 
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
@@ -392,41 +425,54 @@ def run_ours(args, world, rank, local):
     value = reduce_sum(useful * K, world, device) / (total_ms * 1e-3) / 1e12
 
     peaks = measured_peaks()
-    legs = dict(zip(Problem.LEGS, leg_ms.mean(0).tolist()))
-    leg_stats = {
-        "fwd": {"ms": legs["fwd"], "tflops": prob.fwd_flop / legs["fwd"] / 1e9},
-        "bwd": {"ms": legs["bwd"], "tflops": prob.bwd_flop / legs["bwd"] / 1e9},
-        "ring_partials": {"ms": legs["ring_partials"],
-                          "tflops": prob.ring_flop / legs["ring_partials"] / 1e9,
-                          "pairs": len(prob.ring_pairs)},
-        "merge": {"ms": legs["merge"], "gbs": prob.merge_bytes / legs["merge"] / 1e6,
-                  "frac_hbm": prob.merge_bytes / legs["merge"] / 1e6 / peaks["hbm_gbs"]},
-        "permute": {"ms": legs["permute"], "gbs": prob.permute_bytes / legs["permute"] / 1e6,
-                    "frac_hbm": prob.permute_bytes / legs["permute"] / 1e6 / peaks["hbm_gbs"]},
-    }
-    for k in ("fwd", "bwd", "ring_partials"):
-        leg_stats[k]["frac_bf16"] = leg_stats[k]["tflops"] / peaks["bf16_tflops"]
+    legs = dict(zip(prob.LEGS, leg_ms.mean(0).tolist()))
+    leg_stats = {}
+    for k, flop in (("fwd", prob.fwd_flop), ("bwd", prob.bwd_flop),
+                    ("ring_partials", prob.ring_flop)):
+        if k in legs:
+            leg_stats[k] = {"ms": legs[k], "tflops": flop / legs[k] / 1e9}
+            leg_stats[k]["frac_bf16"] = leg_stats[k]["tflops"] / peaks["bf16_tflops"]
+    if "ring_partials" in legs:
+        leg_stats["ring_partials"]["pairs"] = len(prob.ring_pairs)
+    for k, nbytes in (("merge", prob.merge_bytes), ("permute", prob.permute_bytes)):
+        if k in legs:
+            leg_stats[k] = {"ms": legs[k], "gbs": nbytes / legs[k] / 1e6,
+                            "frac_hbm": nbytes / legs[k] / 1e6 / peaks["hbm_gbs"]}
+    if "fwd" in legs and "bwd" in legs:
+        fb = (prob.fwd_flop + prob.bwd_flop) / (legs["fwd"] + legs["bwd"]) / 1e9
+        leg_stats["fwd+bwd"] = {"ms": legs["fwd"] + legs["bwd"], "tflops": fb,
+                                "frac_bf16": fb / peaks["bf16_tflops"]}
     # Roofline of the kernel with the largest share of the step's GPU time
     # (an ncu launch list of this step: the attention forward kernel, main
     # forward plus ring partials), on its main-forward launch: useful FLOP of
     # that launch / its duration, timed with CUDA events on the launching
     # stream (the duration includes the small tile-schedule kernel of the call).
-    ach = leg_stats["fwd"]["tflops"]
-    roof = {"bound": "tensor", "kernel": "attn_fwd_tc_kernel (main forward launch)",
+    main_fwd = "fwd" in legs
+    ach = leg_stats["fwd" if main_fwd else "ring_partials"]["tflops"]
+    roof = {"bound": "tensor",
+            "kernel": "attn_fwd_tc_kernel (" + ("main forward launch" if main_fwd
+                                                else "ring partial launches") + ")",
             "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": ach / peaks["bf16_tflops"],
             # DRAM bytes (read + write) of this launch from one ncu capture of
             # the bench workload (dram__bytes_read.sum + dram__bytes_write.sum);
             # compulsory bytes (Q, K, V, out, lse) are 607 MB.
-            "traffic": FWD_LAUNCH_DRAM_BYTES,
+            "traffic": FWD_LAUNCH_DRAM_BYTES if cid == CONFIG_ID else None,
             "traffic_unit": "bytes per launch",
-            "algorithmic_flop": prob.fwd_flop}
+            "algorithmic_flop": prob.fwd_flop if main_fwd else prob.ring_flop}
     roof["peak_source"] = peaks["source"] + " (burst)"
 
-    e2e = run_e2e(args, prob, nsp, w, device, stream, world)
+    extra = None
+    if prob.ring_pairs:
+        extra = time_extra_legs(prob, stream, flush, K, peaks)
+        extra["ring_accumulate"]["partials_plus_merge_ms"] = legs["ring_partials"] + legs["merge"]
+
+    e2e = None
+    if "bwd" in legs:
+        e2e = run_e2e(args, prob, nsp, w, device, stream, world)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and cid == CONFIG_ID:
         cpu = cpu_baseline(w, args.cpu_seconds)
 
     if rank == 0:
@@ -435,15 +481,16 @@ def run_ours(args, world, rank, local):
             "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded; lengths, Q/K/V/dOut N(0,1) rounded to bf16)",
-            "config": {"workload": CONFIGS[CONFIG_ID].name, "tokens": prob.T,
+            "config": {"workload": CONFIGS[cid].name, "tokens": prob.T,
                        "docs": len(w.lengths), "heads_q": prob.Hq, "heads_kv": prob.Hkv,
                        "head_dim": prob.d, "causal": True, "ring_shards": RING_SHARDS,
                        "permute_groups": PERMUTE_GROUPS,
-                       "step": "fwd + bwd + 8-shard ring partials + lse merge + seq<->head permute",
+                       "step": " + ".join(prob.LEGS),
                        "l2": "flushed (256 MiB write) before every timed step",
                        "parallelism": f"replicas x{world}"},
             "useful_flop_per_step": useful,
             "legs": leg_stats,
+            "extra_legs": extra,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -456,6 +503,35 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def time_extra_legs(prob, stream, flush, K, peaks):
+    """Entry points outside the step, timed alone the same way (graph replay,
+    L2 flushed before each timed call, CUDA events on the stream):
+    ring_accumulate, the ring legs with the merge fused into attention."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(stream.device)
+    prob.ring_accumulate(stream)            # warm
+    torch.cuda.synchronize()
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side):
+        prob.ring_accumulate(side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    reps = max(3, min(K, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i in range(reps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    tf = prob.ring_flop / ms / 1e9
+    return {"ring_accumulate": {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+                                "blocks": len(prob.ring_pairs),
+                                "out": "float32 out + lse per shard"}}
+
+
 def run_e2e(args, prob, nsp, w, device, stream, world):
     """Same step through the public API with host buffers: every step copies
     its inputs (q, k, v, dOut, cu_seqlens) in from pinned host memory and its
@@ -464,7 +540,7 @@ def run_e2e(args, prob, nsp, w, device, stream, world):
     device buffers, a copy-in stream, the compute stream and a copy-out
     stream, so the copies of neighbouring steps overlap a step's compute.
     The time is from the first copy-in to the last copy-out."""
-    prob2 = Problem(nsp, w, device)
+    prob2 = Problem(nsp, w, device, prob.LEGS)
     prob2.step(stream)                      # warm (lazy buffers), then record its graphs
     torch.cuda.synchronize()
     prob2.capture(stream)
@@ -549,7 +625,7 @@ def cpu_baseline(w, seconds: float):
     rate, rows, el = cpu_oracle_rate(w, seconds)
     return {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"fp64 numpy oracle forward on {rows} random query rows of "
-                      f"{CONFIGS[CONFIG_ID].name} (all {w.cfg.Hq} heads), {el:.1f} s; "
+                      f"{w.cfg.name} (all {w.cfg.Hq} heads), {el:.1f} s; "
                       "useful FLOP = 4 d Hq x allowed pairs of those rows"}
 
 
@@ -589,6 +665,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", type=int, choices=sorted(CONFIG_LEGS), default=CONFIG_ID,
+                    help="workload (default: config 2, the bench workload)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("bench: --warmup raised to 3 (minimum)", file=sys.stderr)

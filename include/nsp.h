@@ -124,6 +124,39 @@ int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
                               size_t workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * Ring partial accumulated in place: the partial block of nsp_attn_fwd
+ * merged into a running result by the attention epilogue itself.  This is
+ * the ring's online accumulation (HSAP Sec. 2.2.1) with the receive-side
+ * rescale fused into the attention computation, as HSAP's Limitations
+ * section proposes; nsp_lse_merge is the same combine as a separate pass.
+ *
+ * For the query rows [q_start, q_start + q_len) against the keys
+ * [kv_start, kv_start + kv_len) (global token ids, checked against
+ * cu_seqlens exactly as in nsp_attn_fwd) it forms the partial (o_p, lse_p)
+ * and updates, per (row t, head h):
+ *   lse' = log(exp(lse_acc) + exp(lse_p)),
+ *   acc' = exp(lse_acc - lse') acc + exp(lse_p - lse') o_p.
+ * Rows that see no key of the range (lse_p = -inf) are left unchanged.
+ *   q, k, v, cu_seqlens, ndoc, ranges, Hq, Hkv, d, scale, causal, io_dtype,
+ *     workspace: as nsp_attn_fwd (workspace sized by
+ *     nsp_attn_fwd_workspace_size(q_len, kv_len, ...)).
+ *   acc: device float32 [q_len, Hq, d], read and written.
+ *   lse_acc: device float32 [Hq, q_len] (natural log), read and written;
+ *     required.
+ * Start a ring with lse_acc = -inf and acc = 0 everywhere; after the last
+ * block acc holds the attention output and lse_acc its log-sum-exp (a row
+ * that never saw a key keeps acc = 0, lse_acc = -inf).  Blocks may come in
+ * any order.  Errors: as nsp_attn_fwd (with out_dtype = NSP_F32); a NULL
+ * lse_acc is NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                                int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                                int32_t Hkv, int32_t d, float scale, int32_t causal,
+                                int32_t io_dtype, float* acc, float* lse_acc, void* workspace,
+                                size_t workspace_bytes, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * nsp_attn_fwd without a workspace argument.  No page has a counterpart of
  * this entry point: it exists for callers that cannot allocate device
  * memory where they run attention (code inside a custom allocator or

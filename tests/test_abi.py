@@ -116,3 +116,18 @@ def test_attn_pairs_counts_allowed_pairs(lib):
     assert nsp.nsp_attn_pairs(cu, False) == brute_n == 9 + 16 + 1
     with pytest.raises(nsp.NspError):
         nsp.nsp_attn_pairs(np.array([0, 5, 3], dtype=np.int32))
+
+
+def test_accumulate_rejects_on_host(lib):
+    """nsp_attn_fwd_accumulate: lse_acc is required and 16-byte aligned, and
+    the scale must be positive; all three are refused before any launch."""
+    ws = nsp.nsp_attn_fwd_workspace_size(300, 300, 32, 4, 128)
+    f = lib.nsp_attn_fwd_accumulate
+
+    def call(lse, scale=0.088, acc=A + 16384):
+        return f(A, A + 4096, A + 8192, A + 12288, 3, 0, 300, 0, 300, 32, 4, 128, scale, 1,
+                 nsp.NSP_BF16, acc, lse, A + 32768, ws, None)
+    assert call(None) == nsp.NSP_ERR_INVALID
+    assert call(A + (1 << 16) + 4) == nsp.NSP_ERR_ALIGN
+    assert call(A + (1 << 16), scale=0.0) == nsp.NSP_ERR_INVALID
+    assert call(A + (1 << 16), acc=A + 16388) == nsp.NSP_ERR_ALIGN

@@ -128,6 +128,37 @@ int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t*
   return NSP_OK;
 }
 
+int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                                int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                                int32_t Hkv, int32_t d, float scale, int32_t causal,
+                                int32_t io_dtype, float* acc, float* lse_acc, void* workspace,
+                                size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = nsp_attn_fwd_validate(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start,
+                                     kv_len, Hq, Hkv, d, causal, io_dtype, acc, NSP_F32,
+                                     workspace, workspace_bytes);
+  if (st != NSP_OK) return st;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
+  if (q_len > 0 && !lse_acc) return NSP_ERR_INVALID;
+  if (!aligned16(lse_acc)) return NSP_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = NSP_F32; p.out = acc; p.lse = lse_acc;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.accumulate = 1;
+  if (launch_fwd_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (q_len == 0) return NSP_OK;
+  bool launched = false;
+  if (launch_attn_fwd_tc(p, L, ws, s, &launched) != cudaSuccess) return NSP_ERR_CUDA;
+  if (!launched && launch_attn_fwd_simt(p, s) != cudaSuccess) return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
                                    int32_t io_dtype) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;

@@ -477,9 +477,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           // of a row write 32 contiguous bytes and consecutive stores of a
           // warp continue the same 8 rows; thread t holds rows 8 i + t/4 of
           // the warp's 32 (i = 0..3)
-          float invr[4];
+          //
+          // Ring accumulation (acc, lse_acc updated in place): with this
+          // block's lse_p = m + log2 l (log2 units) and the running lse_a,
+          // lse' = log2(2^lse_a + 2^lse_p), acc' = 2^(lse_a - lse') acc +
+          // 2^(m - lse') O, since O / l weighted by 2^(lse_p - lse') is
+          // O 2^(m - lse').  A row seeing no key keeps (acc, lse_a); a row
+          // whose lse_a is -inf is written without reading acc.
+          float wa = 0.f, wp = inv;
+          if (p.accumulate) {
+            wp = 0.f;
+            if (valid && l > 0.f) {
+              float* lse_a = p.lse + (int64_t)h * p.q_len + row;
+              const float lp2 = m + __log2f(l);
+              const float la2 = *lse_a * kLog2e;
+              const float mx = fmaxf(la2, lp2);
+              const float l2 = mx + __log2f(ex2(la2 - mx) + ex2(lp2 - mx));
+              wa = ex2(la2 - l2);
+              wp = ex2(m - l2);
+              *lse_a = l2 * kLn2;
+            }
+          }
+          float war[4], wpr[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) invr[i] = __shfl_sync(0xffffffffu, inv, 8 * i + (lane >> 2));
+          for (int i = 0; i < 4; ++i) {
+            war[i] = __shfl_sync(0xffffffffu, wa, 8 * i + (lane >> 2));
+            wpr[i] = __shfl_sync(0xffffffffu, wp, 8 * i + (lane >> 2));
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t x[32];
@@ -490,11 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
               const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + 8 * i + (lane >> 2);
-              if (grow < p.q_len) {
+              if (grow < p.q_len && !(p.accumulate && wpr[i] == 0.f)) {
                 float2* d = reinterpret_cast<float2*>(
                     out + (grow * p.Hq + h) * HD + c * 32 + 8 * ((k >> 1) & 3) + 2 * (lane & 3));
-                *d = make_float2(__uint_as_float(x[2 * k]) * invr[i],
-                                 __uint_as_float(x[2 * k + 1]) * invr[i]);
+                float2 y = make_float2(__uint_as_float(x[2 * k]) * wpr[i],
+                                       __uint_as_float(x[2 * k + 1]) * wpr[i]);
+                if (war[i] != 0.f) {
+                  const float2 a = *d;
+                  y.x = fmaf(war[i], a.x, y.x);
+                  y.y = fmaf(war[i], a.y, y.y);
+                }
+                *d = y;
               }
             }
           }
@@ -507,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) store_row_chunk<TO>(dst + c * 32, orow, inv);
           }
         }
-      } else {
+      } else if (!p.accumulate) {
         // no key of the range is visible to any row of the tile: zero rows,
         // each written whole by a warp (16-byte lanes, full sectors)
         constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
@@ -520,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(out + (grow * p.Hq + h) * HD)[part] = make_uint4(0, 0, 0, 0);
         }
       }
-      if (valid && p.lse != nullptr)
+      if (valid && p.lse != nullptr && !p.accumulate)
         p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }

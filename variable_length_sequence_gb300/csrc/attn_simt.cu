@@ -139,9 +139,26 @@ __global__ void __launch_bounds__(kFwdThreads) attn_fwd_simt_kernel(AttnProblem 
     m = m_new;
   }
 
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  if (p.accumulate) {
+    // merge this partial into the running result (both threads of the row
+    // read the old lse before the first one writes the new one)
+    const float lp = (valid && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    float la = -INFINITY;
+    if (lp != -INFINITY) la = p.lse[(int64_t)h * p.q_len + row];
+    __syncwarp();
+    if (lp == -INFINITY) return;
+    const float mx = fmaxf(la, lp);
+    const float L = mx + logf(expf(la - mx) + expf(lp - mx));
+    const float wa = expf(la - L), wp = expf(lp - L) * inv;
+    float* A = reinterpret_cast<float*>(p.out) + (row * p.Hq + h) * D + half * DH;
+#pragma unroll
+    for (int c = 0; c < DH; ++c) A[c] = fmaf(wa, A[c], wp * o[c]);
+    if (half == 0) p.lse[(int64_t)h * p.q_len + row] = L;
+    return;
+  }
   if (!valid) return;
   TO* O = reinterpret_cast<TO*>(p.out);
-  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int c = 0; c < DH; ++c) st_out(O + (row * p.Hq + h) * D + half * DH + c, o[c] * inv);
   if (half == 0 && p.lse != nullptr)

@@ -97,6 +97,10 @@ struct AttnProblem {
   int32_t io_dtype, out_dtype;
   void* out; float* lse;
   WsHeader* hdr;
+  // Accumulate into a running ring result instead of writing the partial:
+  // out is then the float32 accumulator and lse its log-sum-exp (both read
+  // and written; rows that see no key of the range are left unchanged).
+  int32_t accumulate = 0;
 };
 
 // ---- launchers implemented in the .cu files (return cudaError_t) ----

@@ -34,6 +34,8 @@ _SIGNATURES = {
     "nsp_attn_fwd_workspace_size": (_sz, [_i64, _i64, _i32, _i32, _i32]),
     "nsp_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32,
                             _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "nsp_attn_fwd_accumulate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
+                                       _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
     "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
@@ -137,6 +139,18 @@ def nsp_attn_fwd(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq
     return _check("nsp_attn_fwd", st)
 
 
+def nsp_attn_fwd_accumulate(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq,
+                            Hkv, d, scale, causal, acc, lse_acc, workspace, stream=None) -> int:
+    st = load().nsp_attn_fwd_accumulate(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(ndoc),
+                                        int(q_start), int(q_len), int(kv_start), int(kv_len),
+                                        int(Hq), int(Hkv), int(d), float(scale),
+                                        int(bool(causal)), _dtype(q), _ptr(acc), _ptr(lse_acc),
+                                        _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
+    return _check("nsp_attn_fwd_accumulate", st)
+
+
 def nsp_attn_fwd_noalloc(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq, Hkv,
                          d, scale, causal, out, lse, device_status=None, stream=None) -> int:
     """nsp_attn_fwd for callers that cannot allocate: no workspace argument
@@ -212,6 +226,28 @@ def attn_fwd(q, k, v, cu_seqlens, scale=None, causal=True, out_dtype=None, q_sta
     nsp_attn_fwd(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, q_start, q_len, kv_start, kv_len,
                  Hq, Hkv, d, scale, causal, out, lse, workspace, stream)
     return out, lse
+
+
+def ring_accumulate_init(q_len, Hq, d, device):
+    """A fresh ring accumulator: acc = 0 [q_len, Hq, d] float32, lse_acc = -inf [Hq, q_len]."""
+    acc = torch.zeros((q_len, Hq, d), dtype=torch.float32, device=device)
+    lse = torch.full((Hq, q_len), float("-inf"), dtype=torch.float32, device=device)
+    return acc, lse
+
+
+def attn_fwd_accumulate(q, k, v, cu_seqlens, acc, lse_acc, scale=None, causal=True, q_start=0,
+                        kv_start=0, workspace=None, stream=None):
+    """Merge the block (q rows from q_start) x (keys from kv_start) into acc/lse_acc in place."""
+    q_len, Hq, d = q.shape
+    kv_len, Hkv, _ = k.shape
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_fwd_workspace_size(q_len, kv_len, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q.device)
+    nsp_attn_fwd_accumulate(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, q_start, q_len,
+                            kv_start, kv_len, Hq, Hkv, d, scale, causal, acc, lse_acc,
+                            workspace, stream)
+    return acc, lse_acc
 
 
 def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, workspace=None,
