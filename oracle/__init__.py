@@ -20,6 +20,9 @@ online softmax, no fusion), citing the page passage it follows:
   computation blocks").
 * ``attention.attn_bwd`` and the sampled variants -- the analytic gradients of
   that definition (the backward pass that recomputation re-runs, NSP Sec. 2.3).
+* ``attention.attn_bwd_block`` -- one ring block's share of those gradients
+  (queries of one range against keys of another, probabilities normalised
+  over the full row; HSAP Sec. 2.2.1 ring InterSP).
 * ``merge.lse_merge`` -- combining partial results over key chunks, the
   "rescale" of ring attention's online accumulation (HSAP Sec. 2.2.1 and
   Limitations).
@@ -32,11 +35,11 @@ against closed forms, invariants, library special cases and finite
 differences; none is "parity unpinned".
 """
 from .attention import (allowed_interval, attn_fwd, attn_fwd_rows, attn_probs,
-                        attn_bwd, attn_bwd_dq_rows, attn_bwd_dkv_rows)
+                        attn_bwd, attn_bwd_block, attn_bwd_dq_rows, attn_bwd_dkv_rows)
 from .merge import lse_merge
 from .permute import seq2head, head2seq
 
 __all__ = [
-    "allowed_interval", "attn_fwd", "attn_fwd_rows", "attn_probs", "attn_bwd",
+    "allowed_interval", "attn_fwd", "attn_fwd_rows", "attn_probs", "attn_bwd", "attn_bwd_block",
     "attn_bwd_dq_rows", "attn_bwd_dkv_rows", "lse_merge", "seq2head", "head2seq",
 ]

@@ -232,3 +232,54 @@ def attn_bwd_dkv_rows(q, k, v, dout, cu_seqlens, scale, causal, key_rows, g):
             dv[kpos] += ps.reshape(n * G, -1).T @ dog.reshape(n * G, -1)
             dk[kpos] += scale * (dSs.reshape(n * G, -1).T @ qg.reshape(n * G, -1))
     return dk, dv
+
+
+def attn_bwd_block(q, k, v, dout, cu_seqlens, scale, causal, q_range, kv_range):
+    """Gradient contributions of one ring block: queries [qa, qb) against keys
+    [ka, kb) (global ids), for the backward of a ring-style InterSP step
+    (HSAP Sec. 2.2.1: the KV blocks circulate, each rank's queries meet every
+    block once; HSAP Sec. 3.2 blocks A1-A5).
+
+    The probabilities are those of the whole row (normalised over the row's
+    full key set, i.e. by the row's global lse) and delta_t = <dOut_t, out_t>
+    uses the row's full output; only the sums are restricted to the block:
+      dq[t - qa] = scale sum_{j in block} dS_tj k_j,
+      dk[j - ka] = scale sum_{t in block, h in grp(g)} dS_tj q_t,
+      dv[j - ka] = sum_{t in block, h in grp(g)} p_tj dOut_t.
+    Summing the blocks of any (query chunking x key chunking) gives
+    ``attn_bwd``.  Returns dq [qb - qa, Hq, d], dk / dv [kb - ka, Hkv, d].
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    qa, qb = q_range
+    ka, kb = kv_range
+    dq = np.zeros((qb - qa, Hq, d))
+    dk = np.zeros((kb - ka, Hkv, d))
+    dv = np.zeros((kb - ka, Hkv, v.shape[2]))
+    rows = np.arange(qa, qb)
+    for b, pos in _docs_of_rows(rows, cu):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        keys = np.arange(lo, hi)                        # the row's full key set
+        sel = (keys >= ka) & (keys < kb)                # the block's keys
+        if not sel.any():
+            continue
+        nb = _rows_per_block(G, len(keys))
+        for s in range(0, len(pos), nb):
+            rb = rows[pos[s:s + nb]]
+            n = len(rb)
+            for g in range(Hkv):
+                hs = slice(g * G, (g + 1) * G)
+                qg, kg, vg, dog = q[rb, hs, :], k[keys, g, :], v[keys, g, :], dout[rb, hs, :]
+                p, _ = _block(qg, kg, rb, keys, scale, causal, lo, hi)
+                o = (p.reshape(n * G, -1) @ vg).reshape(n, G, -1)
+                delta = (dog * o).sum(-1)                                     # [n, G]
+                ps = p[:, :, sel]                                             # block columns
+                dPs = (dog.reshape(n * G, -1) @ vg[sel].T).reshape(n, G, -1)
+                dSs = (ps * (dPs - delta[..., None])).reshape(n * G, -1)
+                kj = keys[sel] - ka
+                dq[rb - qa, hs, :] += scale * (dSs @ kg[sel]).reshape(n, G, -1)
+                dk[kj, g, :] += scale * (dSs.T @ qg.reshape(n * G, -1))
+                dv[kj, g, :] += ps.reshape(n * G, -1).T @ dog.reshape(n * G, -1)
+    return dq, dk, dv

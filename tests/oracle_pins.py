@@ -332,6 +332,80 @@ def pin_bwd_rows_variants(att, mrg, prm):
         np.testing.assert_allclose(dv2, dv[keys, g], atol=1e-13)
 
 
+def _chunks(T, n_cuts, r):
+    cuts = np.unique(np.concatenate([[0, T], r.integers(1, T, n_cuts)]))
+    return [(int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:])]
+
+
+def pin_bwd_blocks_sum_to_whole(att, mrg, prm):
+    """Ring backward: the block contributions of any (query chunking x key
+    chunking), cuts through documents included, add up to the whole-stream
+    gradients (which finite differences and autograd pin)."""
+    lens = [6, 1, 11, 0, 9]
+    cu, q, k, v, dout = _rand(19, lens, 4, 2, 8)
+    T = int(cu[-1])
+    r = _rng(20)
+    for causal in (True, False):
+        dq, dk, dv = att.attn_bwd(q, k, v, dout, cu, 0.35, causal)
+        for nq, nk in ((0, 0), (2, 3), (5, 1)):
+            sq, sk, sv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
+            for qa, qb in _chunks(T, nq, r):
+                for ka, kb in _chunks(T, nk, r):
+                    bq, bk, bv = att.attn_bwd_block(q, k, v, dout, cu, 0.35, causal, (qa, qb),
+                                                    (ka, kb))
+                    sq[qa:qb] += bq
+                    sk[ka:kb] += bk
+                    sv[ka:kb] += bv
+            for a, b in ((sq, dq), (sk, dk), (sv, dv)):
+                np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def pin_bwd_block_autograd(att, mrg, prm):
+    """One block's contributions equal torch autograd (float64) of
+    L = sum(dOut * out) with every score outside the block, and every value
+    row's use outside it, held constant (detached): only the block's terms
+    then carry gradient, and the probabilities stay those of the full row."""
+    lens = [7, 12, 5]
+    Hq, Hkv, d = 4, 2, 8
+    cu, q, k, v, dout = _rand(21, lens, Hq, Hkv, d)
+    T = int(cu[-1])
+    scale = 0.3
+    doc = np.searchsorted(cu, np.arange(T), side="right") - 1
+    for causal in (True, False):
+        for (qa, qb), (ka, kb) in (((3, 20), (5, 15)), ((0, T), (10, 24)), ((9, 24), (0, 9))):
+            Q, K, V = (torch.from_numpy(x).clone().requires_grad_(True) for x in (q, k, v))
+            Ke = K.repeat_interleave(Hq // Hkv, dim=1)            # [T, Hq, d]
+            Ve = V.repeat_interleave(Hq // Hkv, dim=1)
+            t = torch.arange(T)
+            same = torch.from_numpy(doc[:, None] == doc[None, :])
+            allowed = same & (t[None, :] <= t[:, None]) if causal else same
+            blk = (((t >= qa) & (t < qb))[:, None] & ((t >= ka) & (t < kb))[None, :])
+            live = torch.einsum("thd,jhd->htj", Q, Ke) * scale
+            dead = torch.einsum("thd,jhd->htj", Q.detach(), Ke.detach()) * scale
+            S = torch.where(blk[None], live, dead).masked_fill(~allowed[None], float("-inf"))
+            P = torch.softmax(S, dim=-1)                          # [Hq, T, T]
+            Pb = torch.where(blk[None], P, torch.zeros_like(P))
+            out = (torch.einsum("htj,jhd->thd", Pb, Ve)
+                   + torch.einsum("htj,jhd->thd", P - Pb, Ve.detach()))
+            (out * torch.from_numpy(dout)).sum().backward()
+            bq, bk, bv = att.attn_bwd_block(q, k, v, dout, cu, scale, causal, (qa, qb), (ka, kb))
+            np.testing.assert_allclose(bq, Q.grad[qa:qb].numpy(), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(bk, K.grad[ka:kb].numpy(), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(bv, V.grad[ka:kb].numpy(), rtol=0, atol=1e-12)
+            # nothing outside the block moves
+            assert float(Q.grad[:qa].abs().sum() + Q.grad[qb:].abs().sum()) == 0.0
+            assert float(K.grad[:ka].abs().sum() + K.grad[kb:].abs().sum()) == 0.0
+
+
+def pin_bwd_block_empty(att, mrg, prm):
+    """Causal block whose keys all come after its queries: all zeros."""
+    lens = [10, 10]
+    cu, q, k, v, dout = _rand(22, lens, 2, 1, 4)
+    bq, bk, bv = att.attn_bwd_block(q, k, v, dout, cu, 0.5, True, (0, 8), (8, 20))
+    assert not bq.any() and not bk.any() and not bv.any()
+    assert bq.shape == (8, 2, 4) and bk.shape == (12, 1, 4)
+
+
 # --------------------------------------------------------------------------- permutation
 
 

@@ -32,6 +32,19 @@ MUTANTS = [
      "scale dropped in dK"),
     ("attention.py", "dv[keys, g, :] += pf.T @ dog", "dv[keys, g, :] += pf.T @ dog[::-1]",
      "wrong rows of dOut in dV"),
+    ("attention.py", "p, _ = _block(qg, kg, rb, keys, scale, causal, lo, hi)\n"
+     "                o = (p.reshape(n * G, -1) @ vg).reshape(n, G, -1)\n"
+     "                delta = (dog * o).sum(-1)                                     # [n, G]\n"
+     "                ps",
+     "p, _ = _block(qg, kg, rb, keys, scale, causal, max(lo, ka), min(hi, kb))\n"
+     "                o = (p.reshape(n * G, -1) @ vg).reshape(n, G, -1)\n"
+     "                delta = (dog * o).sum(-1)                                     # [n, G]\n"
+     "                ps",
+     "ring block backward normalised over the block's keys only"),
+    ("attention.py", "dk[kj, g, :] += scale * (dSs.T", "dk[kj, g, :] += (dSs.T",
+     "scale dropped in the block dK"),
+    ("attention.py", "kj = keys[sel] - ka", "kj = keys[sel] - lo",
+     "block keys offset by the document start instead of the block start"),
     ("merge.py", "np.exp(L - np.where(empty, 0.0, lse))", "np.exp(L - np.where(empty, 0.0, m))",
      "weights not normalised by the merged lse"),
     ("merge.py", "m_safe + np.log(", "np.log(", "max not added back into merged lse"),
