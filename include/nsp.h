@@ -203,10 +203,10 @@ int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  * dq, dk, dv are written (not accumulated) in io_dtype.  The workspace (at
  * least nsp_attn_bwd_workspace_size bytes for the same T, heads, d and
  * io_dtype) holds the tile schedules, delta and lse * log2(e); its contents
- * need no initialisation.  bf16 with d = 128 and an even Hq / Hkv runs on the
- * tensor cores (dq, dk, dv each written once, deterministic); other shapes run
- * on CUDA cores, whose dq is summed with float atomics in a float32
- * accumulator that the workspace then also holds (last bits may vary).
+ * need no initialisation.  bf16 with d = 128 runs on the tensor cores (dq,
+ * dk, dv each written once, deterministic); other shapes run on CUDA cores,
+ * whose dq is summed with float atomics in a float32 accumulator that the
+ * workspace then also holds (last bits may vary).
  * ---------------------------------------------------------------------- */
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
                                    int32_t io_dtype);
@@ -223,6 +223,48 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
                               int32_t causal, int32_t io_dtype, const void* dq,
                               const void* dk, const void* dv, const void* workspace,
                               size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * Ring-block backward: one (query range, key range) block's share of the
+ * gradients, added into float32 accumulators.  In ring-style InterSP
+ * ([HSAP] Sec. 2.2.1) each rank keeps its query shard and the key/value
+ * blocks circulate; the backward meets every block once, adds the block's
+ * dq into its own accumulator and sends the block's dk/dv contribution on
+ * with the block.  Summing the blocks of any chunking of queries and keys
+ * gives nsp_attn_bwd's gradients.
+ *
+ * For the query rows [q_start, q_start + q_len) and the keys
+ * [kv_start, kv_start + kv_len) (global token ids, checked against
+ * cu_seqlens as in nsp_attn_fwd), with p_tj and delta_t those of the whole
+ * row (lse and out are the row's final results over all its keys):
+ *   dq_acc[t - q_start, h] += scale sum_{j in block} dS_tj k[j, g],
+ *   dk_acc[j - kv_start, g] += scale sum_{t in block, h in g} dS_tj q[t, h],
+ *   dv_acc[j - kv_start, g] += sum_{t in block, h in g} p_tj dout[t, h].
+ *   q, out, dout: device io_dtype [q_len, Hq, d] (the query shard, its final
+ *     attention output and the output gradient).
+ *   lse: device float32 [Hq, q_len], the rows' final log-sum-exp.
+ *   k, v: device io_dtype [kv_len, Hkv, d] (the key/value block).
+ *   dq_acc: device float32 [q_len, Hq, d]; dk_acc, dv_acc: device float32
+ *     [kv_len, Hkv, d]; read and written (start them at zero).
+ *   workspace: device, at least nsp_attn_bwd_accumulate_workspace_size(q_len,
+ *     kv_len, ...) bytes, no initialisation.
+ * Pairs no query of the block can see add nothing; a block with no visible
+ * pair leaves the accumulators unchanged.  bf16 with d = 128 runs on the
+ * tensor cores (each accumulator element read and written once per call);
+ * other shapes run on CUDA cores (dq_acc summed with float atomics).
+ * Errors: as nsp_attn_bwd (NULL or misaligned buffers, bad scalars before
+ * any launch; a bad cu_seqlens through the workspace status word).
+ * ---------------------------------------------------------------------- */
+size_t nsp_attn_bwd_accumulate_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq,
+                                              int32_t Hkv, int32_t d, int32_t io_dtype);
+
+int32_t nsp_attn_bwd_accumulate(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                                int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                                int32_t Hkv, int32_t d, float scale, int32_t causal,
+                                int32_t io_dtype, float* dq_acc, float* dk_acc, float* dv_acc,
+                                void* workspace, size_t workspace_bytes, nsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Log-sum-exp merge of n partials of the same T query rows over disjoint

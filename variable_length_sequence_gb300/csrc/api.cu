@@ -162,7 +162,7 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
                                    int32_t io_dtype) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;
-  return bwd_ws_layout(T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total;
+  return bwd_ws_layout(T, T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total;
 }
 
 int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const void* out,
@@ -182,7 +182,7 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
   for (const void* x : ptrs)
     if (!aligned16(x)) return NSP_ERR_ALIGN;
   if (!workspace ||
-      workspace_bytes < bwd_ws_layout(T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total)
+      workspace_bytes < bwd_ws_layout(T, T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total)
     return NSP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NSP_ERR_ALIGN;
   return NSP_OK;
@@ -200,7 +200,7 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
   const bool tc = bwd_tc_eligible(io_dtype, d, Hq, Hkv);
-  const BwdWsLayout L = bwd_ws_layout(T, Hq, d, !tc);
+  const BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
@@ -211,6 +211,52 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   if (T == 0) return NSP_OK;
   const cudaError_t e = tc ? launch_attn_bwd_tc(p, out, dout, lse, dq, dk, dv, L, ws, s)
                            : launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s);
+  return e == cudaSuccess ? NSP_OK : NSP_ERR_CUDA;
+}
+
+size_t nsp_attn_bwd_accumulate_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq,
+                                              int32_t Hkv, int32_t d, int32_t io_dtype) {
+  (void)Hkv; (void)io_dtype;
+  if (q_len < 0 || kv_len < 0 || Hq < 1 || d < 1) return 0;
+  return bwd_ws_layout(q_len, kv_len, Hq, d, false).total;
+}
+
+int32_t nsp_attn_bwd_accumulate(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t q_start,
+                                int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq,
+                                int32_t Hkv, int32_t d, float scale, int32_t causal,
+                                int32_t io_dtype, float* dq_acc, float* dk_acc, float* dv_acc,
+                                void* workspace, size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = check_common(ndoc, Hq, Hkv, d, causal, io_dtype);
+  if (st != NSP_OK) return st;
+  if (q_start < 0 || q_len < 0 || kv_start < 0 || kv_len < 0) return NSP_ERR_INVALID;
+  if (q_start + q_len > kMaxTokens || kv_start + kv_len > kMaxTokens) return NSP_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
+  if (!cu_seqlens) return NSP_ERR_INVALID;
+  if (q_len > 0 && (!q || !out || !dout || !lse || !dq_acc)) return NSP_ERR_INVALID;
+  if (kv_len > 0 && (!k || !v || !dk_acc || !dv_acc)) return NSP_ERR_INVALID;
+  const void* ptrs[] = {q, k, v, out, dout, lse, cu_seqlens, dq_acc, dk_acc, dv_acc};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return NSP_ERR_ALIGN;
+  const BwdWsLayout L = bwd_ws_layout(q_len, kv_len, Hq, d, false);
+  if (!workspace || workspace_bytes < L.total) return NSP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NSP_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = NSP_F32; p.out = nullptr; p.lse = nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.accumulate = 1;
+  if (q_len == 0 || kv_len == 0) return NSP_OK;        // an empty block adds nothing
+  if (launch_bwd_schedules(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  const cudaError_t e =
+      bwd_tc_eligible(io_dtype, d, Hq, Hkv)
+          ? launch_attn_bwd_tc(p, out, dout, lse, dq_acc, dk_acc, dv_acc, L, ws, s)
+          : launch_attn_bwd_simt(p, out, dout, lse, dq_acc, dk_acc, dv_acc, L, ws, s);
   return e == cudaSuccess ? NSP_OK : NSP_ERR_CUDA;
 }
 

@@ -121,6 +121,21 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
                  w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
 }
 
+// dst[0..31] += scale * v (raw float32 bits), float32 accumulator row chunk
+// (16-byte aligned: rows are 512 bytes, chunks 128).
+__device__ __forceinline__ void add_row32_f32(float* dst, const uint32_t (&v)[32], float scale) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float4 o = d4[i];
+    o.x = fmaf(__uint_as_float(v[4 * i]), scale, o.x);
+    o.y = fmaf(__uint_as_float(v[4 * i + 1]), scale, o.y);
+    o.z = fmaf(__uint_as_float(v[4 * i + 2]), scale, o.z);
+    o.w = fmaf(__uint_as_float(v[4 * i + 3]), scale, o.w);
+    d4[i] = o;
+  }
+}
+
 // 1024-aligned view of dynamic shared memory, or nullptr (error recorded)
 // when the aligned structure would not fit in the launch's allocation.
 template <typename S>
@@ -146,9 +161,12 @@ struct BwdArgs {
   const float* nlse2;     // [Hq, Tp] -lse * log2(e)
   const float* delta;     // [Hq, Tp]
   int64_t Tp;
-  __nv_bfloat16* dq;      // [T, Hq, d]
-  __nv_bfloat16* dk;      // [T, Hkv, d]
+  __nv_bfloat16* dq;      // [q_len, Hq, d]
+  __nv_bfloat16* dk;      // [kv_len, Hkv, d]
   __nv_bfloat16* dv;
+  float* dq_acc;          // ring block (p.accumulate): float32 accumulators, same shapes
+  float* dk_acc;
+  float* dv_acc;
   const int2* qtiles;     // per 128-row query tile: first/last 128-key tile
   const int* qorder;
   const int2* ktiles;     // per 128-key tile: first/last 128-row query tile
@@ -242,7 +260,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
   const int G = p.Hq / p.Hkv;
-  const int64_t T = p.q_len;
+  const int64_t n_keys = p.kv_len;           // keys of the range (row index of K, V, dK, dV)
   const int n_items = hdr->n_items2 * p.Hkv;
 
   if (warp >= 16) {
@@ -275,6 +293,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mbar_arrive(&sm.item_full[slot]);
           ++it_count;
           if (it.steps < 0) break;
+          if (it.steps == 0) continue;            // no query of the range sees these keys
           if (kv_count >= 1 && !mbar_wait(&sm.kv_empty, (kv_count - 1) & 1, abort_flag, hdr)) {
             ok = false;
             break;
@@ -345,6 +364,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mbar_arrive(&sm.item_empty[slot]);
           ++it_count;
           if (it.steps < 0) break;
+          if (it.steps == 0) continue;
           if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
           for (int n = 0; n < it.steps; ++n) {
             const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
@@ -385,6 +405,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mbar_arrive(&sm.item_empty[slot]);
           ++it_count;
           if (it.steps < 0) break;
+          if (it.steps == 0) continue;
           for (int n = 0; n < it.steps; ++n) {
             const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
             if (!mbar_wait(&sm.p_ready[rb], fp, abort_flag, hdr)) { ok = false; break; }
@@ -452,16 +473,35 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.steps < 0) break;
-      int qlo[4], qhi[4];                                   // queries that see fragment row i
+      if (it.steps == 0) {
+        // no query of the range sees these keys: the whole-stream backward
+        // writes zero rows (a ring block adds nothing)
+        if (!p.accumulate) {
+          const int64_t key = (int64_t)it.ktile * 128 + r;
+          __nv_bfloat16* dst = (cg >= 2 ? a.dk : a.dv) + (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
+          uint32_t z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+          if (key < n_keys) {
+            store_row32_bf16(dst, z, 0.f);
+            store_row32_bf16(dst + 32, z, 0.f);
+          }
+        }
+        continue;
+      }
+      int qlo[4], qhi[4];                                   // queries (range-relative) that see fragment row i
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int64_t key = (int64_t)it.ktile * 128 + wq * 32 + tr + 8 * i;
         qlo[i] = 0;
         qhi[i] = 0;
-        if (key < T) {
-          const int b = doc_of(p.cu, p.ndoc, key);
-          qlo[i] = p.causal ? (int)key : __ldg(p.cu + b);
-          qhi[i] = __ldg(p.cu + b + 1);
+        if (key < n_keys) {
+          const int64_t kg = p.kv_start + key;
+          const int b = doc_of(p.cu, p.ndoc, kg);
+          const int64_t glo = p.causal ? kg : (int64_t)__ldg(p.cu + b);
+          const int64_t ghi = __ldg(p.cu + b + 1);
+          qlo[i] = (int)min(max(glo - p.q_start, (int64_t)0), p.q_len);
+          qhi[i] = (int)min(max(ghi - p.q_start, (int64_t)0), p.q_len);
         }
       }
       for (int n = 0; n < it.steps; ++n) {
@@ -586,13 +626,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const bool is_dk = cg >= 2;
         const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
         const float scale = is_dk ? p.scale : 1.f;
-        __nv_bfloat16* dst = (is_dk ? a.dk : a.dv) + (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
+        const int64_t off = (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + col + c * 32, v);
           tmem_wait_ld();
-          if (key < T) store_row32_bf16(dst + c * 32, v, scale);
+          if (key >= n_keys) continue;
+          if (p.accumulate)
+            add_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
+          else
+            store_row32_bf16((is_dk ? a.dk : a.dv) + off + c * 32, v, scale);
         }
       }
       tc_fence_before();
@@ -896,9 +940,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int lo = 0, hi = 0;                                    // visible keys [lo, hi)
       float nlse2r = 0.f, deltar = 0.f;
       if (valid) {
-        const int b = doc_of(p.cu, p.ndoc, row);
-        lo = __ldg(p.cu + b);
-        hi = p.causal ? (int)row + 1 : __ldg(p.cu + b + 1);
+        // visible keys, relative to the key range
+        const int64_t tg = p.q_start + row;
+        const int b = doc_of(p.cu, p.ndoc, tg);
+        const int64_t glo = max((int64_t)__ldg(p.cu + b), p.kv_start);
+        const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1),
+                                p.kv_start + p.kv_len);
+        lo = (int)(glo - p.kv_start);
+        hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
         nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + row);
         deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
       }
@@ -966,12 +1015,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + 384 + wg * 64 + c * 32, v);
           tmem_wait_ld();
-          if (valid) store_row32_bf16(dst + c * 32, v, p.scale);
+          if (!valid) continue;
+          if (p.accumulate)
+            add_row32_f32(a.dq_acc + (row * p.Hq + h) * HD + wg * 64 + c * 32, v, p.scale);
+          else
+            store_row32_bf16(dst + c * 32, v, p.scale);
         }
         tc_fence_before();
         mbar_arrive(&sm.epi_done);
         ++items_done;
-      } else if (valid) {
+      } else if (valid && !p.accumulate) {
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0u;
@@ -1033,7 +1086,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   CUtensorMap mq, mdo, mk, mv;
   const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
   if (!make_map(&mq, p.q, T, qc) || !make_map(&mdo, dout, T, qc) ||
-      !make_map(&mk, p.k, T, kc) || !make_map(&mv, p.v, T, kc))
+      !make_map(&mk, p.k, p.kv_len, kc) || !make_map(&mv, p.v, p.kv_len, kc))
     return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
@@ -1048,6 +1101,9 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   a.dq = reinterpret_cast<__nv_bfloat16*>(dq);
   a.dk = reinterpret_cast<__nv_bfloat16*>(dk);
   a.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+  a.dq_acc = reinterpret_cast<float*>(dq);
+  a.dk_acc = reinterpret_cast<float*>(dk);
+  a.dv_acc = reinterpret_cast<float*>(dv);
   a.qtiles = reinterpret_cast<const int2*>(ws + L.qtiles);
   a.qorder = reinterpret_cast<const int*>(ws + L.qorder);
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);

@@ -388,6 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         lo = (int)(glo - p.kv_start);
         hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
       }
+      // ring accumulation: the running lse is read now and the running
+      // output row is brought into L2, so the epilogue does not wait on DRAM
+      float la_row = -INFINITY;
+      if (p.accumulate && valid && hi > lo) {
+        la_row = p.lse[(int64_t)h * p.q_len + row];
+        const float* arow = reinterpret_cast<const float*>(p.out) + (row * p.Hq + h) * HD;
+#pragma unroll
+        for (int c = 0; c < HD * 4 / 128; ++c) prefetch_l2(arow + c * 32);
+      }
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int jj = 0; jj < it.n_kv; ++jj) {
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid && l > 0.f) {
               float* lse_a = p.lse + (int64_t)h * p.q_len + row;
               const float lp2 = m + __log2f(l);
-              const float la2 = *lse_a * kLog2e;
+              const float la2 = la_row * kLog2e;
               const float mx = fmaxf(la2, lp2);
               const float l2 = mx + __log2f(ex2(la2 - mx) + ex2(lp2 - mx));
               wa = ex2(la2 - l2);

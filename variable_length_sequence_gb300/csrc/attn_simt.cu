@@ -188,7 +188,8 @@ template <typename TI, int D>
 __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
     AttnProblem p, const TI* __restrict__ dout, const float* __restrict__ lse,
     const float* __restrict__ delta, int64_t delta_stride, float* __restrict__ dq_acc,
-    TI* __restrict__ dk, TI* __restrict__ dv) {
+    TI* __restrict__ dk, TI* __restrict__ dv, float* __restrict__ dk_acc32,
+    float* __restrict__ dv_acc32) {
   constexpr int DQ = D / 4;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
@@ -198,11 +199,13 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
   const int j = tid >> 2, qtr = tid & 3;
   const int g = blockIdx.y;
   const int G = p.Hq / p.Hkv;
-  const int64_t T = p.q_len;
+  const int64_t T = p.q_len;                      // query rows of the range
+  const int64_t NK = p.kv_len;                    // keys of the range
   const int64_t key0 = (int64_t)blockIdx.x * kBwdBK;
   const int64_t key = key0 + j;
-  const bool kvalid = key < T;
-  const int64_t key_last = min(key0 + kBwdBK, T) - 1;
+  const int64_t key_g = p.kv_start + key;         // global token id of this thread's key
+  const bool kvalid = key < NK;
+  const int64_t key_last = min(key0 + kBwdBK, NK) - 1;
 
   const TI* Q = reinterpret_cast<const TI*>(p.q);
   const TI* K = reinterpret_cast<const TI*>(p.k);
@@ -219,12 +222,13 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
   for (int e = tid; e < kBwdBK * D; e += kBwdThreads) {
     const int jj = e / D, c = e % D;
     const int64_t kk = key0 + jj;
-    sm.k[jj][c] = kk < T ? ld_in(K + (kk * p.Hkv + g) * D + c) : 0.f;
+    sm.k[jj][c] = kk < NK ? ld_in(K + (kk * p.Hkv + g) * D + c) : 0.f;
   }
-  // Query rows that can see any key of this block.
-  const int b0 = doc_of(p.cu, p.ndoc, key0), b1 = doc_of(p.cu, p.ndoc, key_last);
-  const int64_t r_lo = p.causal ? key0 : (int64_t)p.cu[b0];
-  const int64_t r_hi = (int64_t)p.cu[b1 + 1];
+  // Query rows (relative to the query range) that can see any key of this block.
+  const int64_t k0g = p.kv_start + key0, klg = p.kv_start + key_last;
+  const int b0 = doc_of(p.cu, p.ndoc, k0g), b1 = doc_of(p.cu, p.ndoc, klg);
+  const int64_t r_lo = max(p.causal ? k0g : (int64_t)p.cu[b0], p.q_start) - p.q_start;
+  const int64_t r_hi = min((int64_t)p.cu[b1 + 1], p.q_start + T) - p.q_start;
   const float sl2 = p.scale * kLog2e;
 
   for (int hh = 0; hh < G; ++hh) {
@@ -241,9 +245,10 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
       if (tid < kBwdBM) {
         const int64_t t = t0 + tid;
         if (t < r_hi) {
-          const int b = doc_of(p.cu, p.ndoc, t);
+          const int64_t tg = p.q_start + t;
+          const int b = doc_of(p.cu, p.ndoc, tg);
           sm.lo[tid] = p.cu[b];
-          sm.hi[tid] = p.causal ? t + 1 : (int64_t)p.cu[b + 1];
+          sm.hi[tid] = p.causal ? tg + 1 : (int64_t)p.cu[b + 1];
           sm.lse[tid] = lse[(int64_t)h * T + t];
           sm.delta[tid] = delta[(int64_t)h * delta_stride + t];
         } else {
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         dp += __shfl_xor_sync(0xffffffffu, dp, 1);
         dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-        const bool allowed = kvalid && key >= sm.lo[rr] && key < sm.hi[rr];
+        const bool allowed = kvalid && key_g >= sm.lo[rr] && key_g < sm.hi[rr];
         const float pr = allowed ? exp2f(s * sl2 - sm.lse[rr] * kLog2e) : 0.f;
         const float ds = pr * (dp - sm.delta[rr]);
 #pragma unroll
@@ -286,6 +291,15 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
     }
   }
   if (!kvalid) return;
+  if (p.accumulate) {
+    // ring block: add into the float32 accumulators (one thread per element)
+#pragma unroll
+    for (int c = 0; c < DQ; ++c) {
+      dk_acc32[(key * p.Hkv + g) * D + qtr * DQ + c] += dk_acc[c] * p.scale;
+      dv_acc32[(key * p.Hkv + g) * D + qtr * DQ + c] += dv_acc[c];
+    }
+    return;
+  }
 #pragma unroll
   for (int c = 0; c < DQ; ++c) {
     st_out(dk + (key * p.Hkv + g) * D + qtr * DQ + c, dk_acc[c] * p.scale);
@@ -306,8 +320,11 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
                          char* ws, cudaStream_t s) {
   const int64_t T = p.q_len;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
-  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
-  cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
+  // a ring block adds dQ straight into the caller's float32 accumulator
+  float* dq_acc = p.accumulate ? reinterpret_cast<float*>(dq)
+                               : reinterpret_cast<float*>(ws + L.dq_acc);
+  cudaError_t e = cudaSuccess;
+  if (!p.accumulate) e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
   if (e != cudaSuccess) return e;
   e = launch_bwd_delta(out, dout, lse, delta, reinterpret_cast<float*>(ws + L.nlse2), T, L.Tp,
                        p.Hq, D, p.io_dtype, p.hdr, s);
@@ -316,12 +333,13 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   e = cudaFuncSetAttribute(attn_bwd_dkdv_simt_kernel<TI, D>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)ceil_div(T, kBwdBK), (unsigned)p.Hkv);
+  dim3 grid((unsigned)ceil_div(p.kv_len, kBwdBK), (unsigned)p.Hkv);
   attn_bwd_dkdv_simt_kernel<TI, D><<<grid, kBwdThreads, smem, s>>>(
       p, reinterpret_cast<const TI*>(dout), lse, delta, L.Tp, dq_acc, reinterpret_cast<TI*>(dk),
-      reinterpret_cast<TI*>(dv)); count_launches(1);
+      reinterpret_cast<TI*>(dv), reinterpret_cast<float*>(dk), reinterpret_cast<float*>(dv));
+  count_launches(1);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || p.accumulate) return e;
   return launch_dq_convert(dq_acc, dq, T * p.Hq * D, p.io_dtype, p.hdr, s);
 }
 

@@ -51,37 +51,40 @@ inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
 // Backward workspace: header; schedule of 128-row query tiles listing
 // 128-key tiles (dQ kernel) and of 128-key tiles listing 128-row query tiles
 // (dK/dV kernel); delta and lse * log2(e) [Hq, Tp] f32 (rows padded to whole
-// 128-row tiles, padding zeroed); and, for the CUDA-core path only, a
-// float32 dq accumulator [T, Hq, d].
+// 128-row tiles, padding zeroed); and, for the CUDA-core path of the
+// whole-stream backward only, a float32 dq accumulator [q_len, Hq, d].
+// A ring block (nsp_attn_bwd_accumulate) has q_len query rows and kv_len keys;
+// the whole-stream backward is q_len = kv_len = T.
 constexpr int kBwdSub = 128;       // tile granularity listed by the backward schedules
 
 struct BwdWsLayout {
-  size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_sub + 2]
-  size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_sub + 2]
+  size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_ktiles + 2]
+  size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_qtiles + 2]
   size_t delta;                    // float [Hq, Tp]
   size_t nlse2;                     // float [Hq, Tp]
-  size_t dq_acc;                   // float [T, Hq, d] (CUDA-core path)
+  size_t dq_acc;                   // float [q_len, Hq, d] (CUDA-core path)
   size_t total;
-  int64_t Tp, n_qtiles, n_ktiles, n_sub;
+  int64_t Tp, n_qtiles, n_ktiles;
 };
 
-inline BwdWsLayout bwd_ws_layout(int64_t T, int32_t Hq, int32_t d, bool need_dq_acc) {
+inline BwdWsLayout bwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t d,
+                                 bool need_dq_acc) {
   BwdWsLayout L;
-  L.n_qtiles = ceil_div(T, kTileM);
-  L.n_ktiles = ceil_div(T, kTileN);
-  L.n_sub = ceil_div(T, kBwdSub);
+  L.n_qtiles = ceil_div(q_len, kTileM);
+  L.n_ktiles = ceil_div(kv_len, kTileN);
   L.Tp = L.n_qtiles * kTileM;
   size_t off = sizeof(WsHeader);
   L.qtiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_qtiles, 256);
   L.qorder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_qtiles, 256);
-  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_sub + 2), 256);
+  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_ktiles + 2), 256);
   L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_ktiles, 256);
   L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_ktiles, 256);
-  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_sub + 2), 256);
+  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_qtiles + 2), 256);
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.nlse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off;
-  if (need_dq_acc) off = align_up(off + sizeof(float) * (size_t)T * (size_t)Hq * (size_t)d, 256);
+  if (need_dq_acc)
+    off = align_up(off + sizeof(float) * (size_t)q_len * (size_t)Hq * (size_t)d, 256);
   L.total = off;
   return L;
 }
@@ -97,9 +100,11 @@ struct AttnProblem {
   int32_t io_dtype, out_dtype;
   void* out; float* lse;
   WsHeader* hdr;
-  // Accumulate into a running ring result instead of writing the partial:
-  // out is then the float32 accumulator and lse its log-sum-exp (both read
-  // and written; rows that see no key of the range are left unchanged).
+  // Forward: accumulate into a running ring result instead of writing the
+  // partial: out is then the float32 accumulator and lse its log-sum-exp
+  // (both read and written; rows that see no key of the range are left
+  // unchanged).  Backward: add the block's dq/dk/dv into float32
+  // accumulators instead of writing io-typed gradients.
   int32_t accumulate = 0;
 };
 

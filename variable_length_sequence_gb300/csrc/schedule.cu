@@ -14,9 +14,12 @@
 // Mode 0 (forward / backward dQ view): tile i covers query rows
 //   [q_start + 128 i, ...) and lists the key sub-tiles j (keys
 //   [kv_start + gran j, ...), gran = 128) its rows see.
-// Mode 1 (backward dK/dV view): tile j covers keys [128 j, ...) of the whole
-//   stream and lists the query sub-tiles (rows [gran i, ...)) whose rows can
-//   see any of those keys.
+// Mode 1 (backward dK/dV view): tile j covers keys [kv_start + 128 j, ...)
+//   and lists the query sub-tiles (rows [q_start + gran i, ...)) whose rows
+//   can see any of those keys.
+// A tile that sees nothing of the other range gets the empty list
+// (first = 0, last = -1): it happens only for ring blocks, never for the
+// whole stream (every key and query sees itself).
 //
 // One block of 1024 threads; the first mode-0 launch of a call validates
 // cu_seqlens and resets the workspace status word.  The counting-sort
@@ -100,13 +103,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
         hi_t = (int)((hi - 1 - a.kv_start) / a.gran);
       }
     } else {
-      const int64_t k0 = (int64_t)i * kTileN;
-      const int64_t k1 = min(k0 + kTileN, a.kv_len) - 1;
+      const int64_t k0 = a.kv_start + (int64_t)i * kTileN;
+      const int64_t k1 = min(k0 + kTileN, kv_end) - 1;          // last key of the tile
       const int b0 = doc_of(a.cu, a.ndoc, k0), b1 = doc_of(a.cu, a.ndoc, k1);
-      const int64_t lo = a.causal ? k0 : (int64_t)a.cu[b0];
-      const int64_t hi = (int64_t)a.cu[b1 + 1];                // exclusive
-      lo_t = (int)(lo / a.gran);
-      hi_t = (int)((hi - 1) / a.gran);
+      const int64_t lo = max(a.causal ? k0 : (int64_t)a.cu[b0], a.q_start);
+      const int64_t hi = min((int64_t)a.cu[b1 + 1], q_end);      // exclusive
+      if (hi > lo) {
+        lo_t = (int)((lo - a.q_start) / a.gran);
+        hi_t = (int)((hi - 1 - a.q_start) / a.gran);
+      }
     }
     a.tiles[i] = make_int2(lo_t, hi_t);
     const int cost = hi_t - lo_t + 1;
@@ -188,13 +193,13 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   // query tiles of 128 rows listing 128-key tiles (validates cu_seqlens)
   SchedArgs a;
   a.cu = p.cu; a.ndoc = p.ndoc;
-  a.q_start = 0; a.q_len = p.q_len; a.kv_start = 0; a.kv_len = p.kv_len;
+  a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
   a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub;
   a.tiles = reinterpret_cast<int2*>(ws + L.qtiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.qorder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.qhist);
   a.n_tiles = (int32_t)L.n_qtiles;
-  a.n_buckets = (int32_t)L.n_sub + 2;
+  a.n_buckets = (int32_t)L.n_ktiles + 2;
   a.hdr = p.hdr; a.second = 0;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   cudaError_t e = cudaGetLastError();
@@ -205,7 +210,7 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.order = reinterpret_cast<int32_t*>(ws + L.korder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.khist);
   a.n_tiles = (int32_t)L.n_ktiles;
-  a.n_buckets = (int32_t)L.n_sub + 2;
+  a.n_buckets = (int32_t)L.n_qtiles + 2;
   a.hdr = p.hdr; a.second = 1;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   return cudaGetLastError();

@@ -45,6 +45,10 @@ _SIGNATURES = {
                             _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_bwd_validate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                      _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz]),
+    "nsp_attn_bwd_accumulate_workspace_size": (_sz, [_i64, _i64, _i32, _i32, _i32, _i32]),
+    "nsp_attn_bwd_accumulate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64,
+                                       _i64, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp,
+                                       _vp, _sz, _vp]),
     "nsp_lse_merge": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp, _vp]),
     "nsp_lse_merge_validate": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp]),
     "nsp_seq2head_permute": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
@@ -173,6 +177,24 @@ def nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d, scale
     return _check("nsp_attn_bwd", st)
 
 
+def nsp_attn_bwd_accumulate_workspace_size(q_len: int, kv_len: int, Hq: int, Hkv: int, d: int,
+                                           io_dtype: int = NSP_BF16) -> int:
+    return int(load().nsp_attn_bwd_accumulate_workspace_size(q_len, kv_len, Hq, Hkv, d,
+                                                             int(io_dtype)))
+
+
+def nsp_attn_bwd_accumulate(q, k, v, out, dout, lse, cu_seqlens, ndoc, q_start, q_len, kv_start,
+                            kv_len, Hq, Hkv, d, scale, causal, dq_acc, dk_acc, dv_acc, workspace,
+                            stream=None) -> int:
+    st = load().nsp_attn_bwd_accumulate(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(cu_seqlens),
+        int(ndoc), int(q_start), int(q_len), int(kv_start), int(kv_len), int(Hq), int(Hkv),
+        int(d), float(scale), int(bool(causal)), _dtype(q), _ptr(dq_acc), _ptr(dk_acc),
+        _ptr(dv_acc), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    return _check("nsp_attn_bwd_accumulate", st)
+
+
 def nsp_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], out, lse,
                   stream=None) -> int:
     n = len(outs)
@@ -262,6 +284,23 @@ def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, works
     nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, d,
                  scale, causal, dq, dk, dv, workspace, stream)
     return dq, dk, dv
+
+
+def attn_bwd_accumulate(q, k, v, out, dout, lse, cu_seqlens, dq_acc, dk_acc, dv_acc, scale=None,
+                        causal=True, q_start=0, kv_start=0, workspace=None, stream=None):
+    """Add the block (q rows from q_start) x (keys from kv_start) into the
+    float32 gradient accumulators in place."""
+    q_len, Hq, d = q.shape
+    kv_len, Hkv, _ = k.shape
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_bwd_accumulate_workspace_size(q_len, kv_len, Hq, Hkv, d,
+                                                                       _dtype(q)),
+                                dtype=torch.uint8, device=q.device)
+    nsp_attn_bwd_accumulate(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, q_start,
+                            q_len, kv_start, kv_len, Hq, Hkv, d, scale, causal, dq_acc, dk_acc,
+                            dv_acc, workspace, stream)
+    return dq_acc, dk_acc, dv_acc
 
 
 def lse_merge(outs, lses, out_dtype=torch.float32, stream=None):
