@@ -313,6 +313,34 @@ class Problem:
                 self.nsp.nsp_attn_fwd(*args)
                 started.add(qs)
 
+    def ring_bwd(self, stream):
+        """The ring backward: every causal (q-shard, kv-shard) block's dq/dk/dv
+        added into float32 accumulators (zeroed first) by nsp_attn_bwd_accumulate,
+        with the forward's out and lse of the query shard."""
+        n = self.T // RING_SHARDS
+        if not hasattr(self, "_rb"):
+            dev = self.q.device
+            self._rb = {
+                "dq": torch.zeros((self.T, self.Hq, self.d), dtype=torch.float32, device=dev),
+                "dk": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
+                "dv": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
+                "lse": [torch.empty((self.Hq, n), dtype=torch.float32, device=dev)
+                        for _ in range(RING_SHARDS)],
+                "ws": torch.empty(self.nsp.nsp_attn_bwd_accumulate_workspace_size(
+                    n, n, self.Hq, self.Hkv, self.d), dtype=torch.uint8, device=dev)}
+            for qs, (qa, qb) in enumerate(self.bounds):
+                self._rb["lse"][qs].copy_(self.lse[:, qa:qb])
+        rb = self._rb
+        for t in (rb["dq"], rb["dk"], rb["dv"]):
+            t.zero_()
+        for qs, ks, _ in self.ring_pairs:
+            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
+            self.nsp.nsp_attn_bwd_accumulate(
+                self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n], self.out[qa:qa + n],
+                self.dout[qa:qa + n], rb["lse"][qs], self.cu, len(self.w.lengths), qa, n, ka, n,
+                self.Hq, self.Hkv, self.d, self.scale, True, rb["dq"][qa:qa + n],
+                rb["dk"][ka:ka + n], rb["dv"][ka:ka + n], rb["ws"], stream)
+
     def merged_l_view(self, qs):
         # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
         if not hasattr(self, "_ml"):
@@ -503,20 +531,16 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def time_extra_legs(prob, stream, flush, K, peaks):
-    """Entry points outside the step, timed alone the same way (graph replay,
-    L2 flushed before each timed call, CUDA events on the stream):
-    ring_accumulate, the ring legs with the merge fused into attention."""
+def _time_leg(fn, stream, flush, reps):
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(stream.device)
-    prob.ring_accumulate(stream)            # warm
+    fn(stream)                              # warm (lazy buffers)
     torch.cuda.synchronize()
     side.wait_stream(stream)
     with torch.cuda.graph(g, stream=side):
-        prob.ring_accumulate(side)
+        fn(side)
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    reps = max(3, min(K, 50))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for i in range(reps):
@@ -525,11 +549,30 @@ def time_extra_legs(prob, stream, flush, K, peaks):
         g.replay()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    return statistics.mean(s.elapsed_time(e) for s, e in ev)
+
+
+def time_extra_legs(prob, stream, flush, K, peaks):
+    """Entry points outside the step, timed alone the same way (graph replay,
+    L2 flushed before each timed call, CUDA events on the stream):
+    ring_accumulate, the ring legs with the merge fused into attention, and
+    ring_bwd, the ring backward (its three float32 accumulators are zeroed
+    inside the timed region, by PyTorch)."""
+    reps = max(3, min(K, 50))
+    extra = {}
+    ms = _time_leg(prob.ring_accumulate, stream, flush, reps)
     tf = prob.ring_flop / ms / 1e9
-    return {"ring_accumulate": {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+    extra["ring_accumulate"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
                                 "blocks": len(prob.ring_pairs),
-                                "out": "float32 out + lse per shard"}}
+                                "out": "float32 out + lse per shard"}
+    if prob.dout is not None:
+        ms = _time_leg(prob.ring_bwd, stream, flush, reps)
+        flop = prob.ring_flop * 10.0 / 4.0
+        tf = flop / ms / 1e9
+        extra["ring_bwd"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+                             "blocks": len(prob.ring_pairs),
+                             "out": "float32 dq, dk, dv accumulated over the blocks"}
+    return extra
 
 
 def run_e2e(args, prob, nsp, w, device, stream, world):

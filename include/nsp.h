@@ -318,6 +318,35 @@ int32_t nsp_status_query(const void* workspace, nsp_stream_t stream);
 int32_t nsp_attn_pairs(const int32_t* cu_seqlens_host, int32_t ndoc, int32_t causal,
                        double* pairs);
 
+/* ------------------------------------------------------------------------
+ * Cost of one attention call, from a HOST copy of cu_seqlens: the hook a
+ * planner that balances attention work over ranks or pipelines needs (NSP
+ * Sec. 4.1: the backend reports the attention FLOPs of the inputs routed to
+ * it; HSAP Sec. 3.2 balances ranks by attention block counts).  For the
+ * query rows [q_start, q_start + q_len) against the keys
+ * [kv_start, kv_start + kv_len) (the whole stream: 0, T, 0, T):
+ *   pairs      allowed (query, key) pairs per query head;
+ *   fwd_flop   4 d Hq pairs (Q K^T and P V);
+ *   bwd_flop   10 d Hq pairs (the recomputed Q K^T, dOut V^T, P^T dOut,
+ *              dS^T Q, dS K);
+ *   tiles      (128-row query tile, 128-key tile) pairs holding at least one
+ *              allowed pair: the tiles the kernels schedule, per query head
+ *              (executed tensor-core work is 4 d Hq 128^2 tiles forward);
+ *   fwd_bytes  compulsory HBM bytes of nsp_attn_fwd: q, k, v read, out
+ *              written in io_dtype, lse written (float32);
+ *   bwd_bytes  compulsory HBM bytes of nsp_attn_bwd: q, k, v, out, dout and
+ *              lse read, dq, dk, dv written.
+ * Returns NSP_ERR_INVALID for a malformed cu_seqlens, ranges outside it or
+ * bad head counts; *cost is written only on NSP_OK.  No device work.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  double pairs, fwd_flop, bwd_flop, tiles, fwd_bytes, bwd_bytes;
+} nsp_attn_cost_t;
+
+int32_t nsp_attn_cost(const int32_t* cu_seqlens_host, int32_t ndoc, int64_t q_start,
+                      int64_t q_len, int64_t kv_start, int64_t kv_len, int32_t Hq, int32_t Hkv,
+                      int32_t d, int32_t causal, int32_t io_dtype, nsp_attn_cost_t* cost);
+
 #ifdef __cplusplus
 }
 #endif

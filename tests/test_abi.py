@@ -131,3 +131,42 @@ def test_accumulate_rejects_on_host(lib):
     assert call(A + (1 << 16) + 4) == nsp.NSP_ERR_ALIGN
     assert call(A + (1 << 16), scale=0.0) == nsp.NSP_ERR_INVALID
     assert call(A + (1 << 16), acc=A + 16388) == nsp.NSP_ERR_ALIGN
+
+
+def _brute_cost(cu, qa, qb, ka, kb, causal):
+    """Allowed pairs and 128 x 128 tiles holding one, by enumeration."""
+    cu = np.asarray(cu, np.int64)
+    doc = np.searchsorted(cu, np.arange(cu[-1]), side="right") - 1
+    pairs, tiles = 0, set()
+    for t in range(qa, qb):
+        for j in range(ka, kb):
+            if doc[t] == doc[j] and (not causal or j <= t):
+                pairs += 1
+                tiles.add(((t - qa) // 128, (j - ka) // 128))
+    return pairs, len(tiles)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attn_cost_matches_enumeration(lib, causal):
+    r = np.random.default_rng(3)
+    lens = [1, 300, 0, 45, 129, 7, 260, 2]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    ranges = [(0, T, 0, T), (100, 500, 0, 300), (300, 700, 350, T), (0, 128, 500, T)]
+    for _ in range(4):
+        a, b = sorted(r.integers(0, T + 1, 2))
+        c, e = sorted(r.integers(0, T + 1, 2))
+        ranges.append((int(a), int(b), int(c), int(e)))
+    for qa, qb, ka, kb in ranges:
+        c = nsp.nsp_attn_cost(cu, 32, 4, 128, causal, nsp.NSP_BF16, qa, qb - qa, ka, kb - ka)
+        pairs, tiles = _brute_cost(cu, qa, qb, ka, kb, causal)
+        assert c["pairs"] == pairs and c["tiles"] == tiles, (qa, qb, ka, kb)
+        assert c["fwd_flop"] == 4 * 128 * 32 * pairs and c["bwd_flop"] == 10 * 128 * 32 * pairs
+    whole = nsp.nsp_attn_cost(cu, 32, 4, 128, causal)
+    assert whole["pairs"] == nsp.nsp_attn_pairs(cu, causal)
+    # compulsory bytes of the whole stream, bf16: q/out/dout/dq 32 heads, k/v/dk/dv 4 heads
+    row_q, row_kv, lse = T * 32 * 128 * 2, T * 4 * 128 * 2, T * 32 * 4
+    assert whole["fwd_bytes"] == 2 * row_q + 2 * row_kv + lse
+    assert whole["bwd_bytes"] == 4 * row_q + 4 * row_kv + lse
+    with pytest.raises(nsp.NspError):
+        nsp.nsp_attn_cost(cu, 32, 4, 128, causal, nsp.NSP_BF16, 10, T)   # past the stream

@@ -1,7 +1,8 @@
 // C ABI entry points: host-side validation, workspace carving and dispatch.
 // Nothing here allocates memory or synchronises (except nsp_status_query).
-#include <cstdio>
+#include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstring>
 
 #include "nsp_internal.cuh"
@@ -335,6 +336,62 @@ int32_t nsp_attn_pairs(const int32_t* cu_seqlens_host, int32_t ndoc, int32_t cau
     acc += causal ? 0.5 * (double)L * (double)(L + 1) : (double)L * (double)L;
   }
   *pairs = acc;
+  return NSP_OK;
+}
+
+int32_t nsp_attn_cost(const int32_t* cu, int32_t ndoc, int64_t q_start, int64_t q_len,
+                      int64_t kv_start, int64_t kv_len, int32_t Hq, int32_t Hkv, int32_t d,
+                      int32_t causal, int32_t io_dtype, nsp_attn_cost_t* cost) {
+  if (!cu || !cost || ndoc < 1 || cu[0] != 0) return NSP_ERR_INVALID;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || !dtype_ok(io_dtype)) return NSP_ERR_INVALID;
+  if ((causal != 0 && causal != 1) || q_start < 0 || q_len < 0 || kv_start < 0 || kv_len < 0)
+    return NSP_ERR_INVALID;
+  for (int32_t i = 0; i < ndoc; ++i)
+    if (cu[i + 1] < cu[i]) return NSP_ERR_INVALID;
+  const int64_t T = cu[ndoc];
+  if (q_start + q_len > T || kv_start + kv_len > T) return NSP_ERR_INVALID;
+  const int64_t qa = q_start, qb = q_start + q_len, ka = kv_start, kb = kv_start + kv_len;
+  // allowed pairs, per document: rows t in [t0, t1) see keys [lo, hi(t))
+  double pairs = 0.0;
+  for (int32_t b = 0; b < ndoc; ++b) {
+    const int64_t s = cu[b], e = cu[b + 1];
+    const int64_t t0 = std::max(s, qa), t1 = std::min(e, qb);
+    const int64_t lo = std::max(s, ka);
+    if (t1 <= t0) continue;
+    if (!causal) {
+      const int64_t w = std::min(e, kb) - lo;
+      if (w > 0) pairs += (double)w * (double)(t1 - t0);
+      continue;
+    }
+    // rows with t + 1 <= kb see t + 1 - lo keys (when positive), the rest kb - lo
+    const int64_t a0 = std::max(t0, lo), a1 = std::min(t1, kb);
+    if (a1 > a0)      // sum over t in [a0, a1) of (t + 1 - lo)
+      pairs += 0.5 * (double)(a1 - a0) * (double)((a0 + 1 - lo) + (a1 - lo));
+    const int64_t b0 = std::max(t0, kb);
+    if (t1 > b0 && kb > lo) pairs += (double)(t1 - b0) * (double)(kb - lo);
+  }
+  // scheduled tiles: per 128-row query tile, the contiguous 128-key tiles
+  // from its first row's document start to its last row's last visible key
+  double tiles = 0.0;
+  for (int64_t r0 = qa; r0 < qb; r0 += kTileM) {
+    const int64_t r1 = std::min(r0 + kTileM, qb) - 1;
+    const int32_t* it0 = std::upper_bound(cu, cu + ndoc + 1, (int32_t)r0);
+    const int32_t* it1 = std::upper_bound(cu, cu + ndoc + 1, (int32_t)r1);
+    const int64_t b0 = (it0 - cu) - 1, b1 = (it1 - cu) - 1;
+    const int64_t lo = std::max((int64_t)cu[b0], ka);
+    const int64_t hi = std::min(causal ? r1 + 1 : (int64_t)cu[b1 + 1], kb);
+    if (hi > lo) tiles += (double)((hi - 1 - ka) / kTileN - (lo - ka) / kTileN + 1);
+  }
+  const double e = io_dtype == NSP_BF16 ? 2.0 : 4.0;
+  const double qo = (double)q_len * Hq * d * e;        // one [q_len, Hq, d] tensor
+  const double kv = (double)kv_len * Hkv * d * e;      // one [kv_len, Hkv, d] tensor
+  const double ls = 4.0 * (double)Hq * (double)q_len;  // lse
+  cost->pairs = pairs;
+  cost->fwd_flop = 4.0 * d * Hq * pairs;
+  cost->bwd_flop = 10.0 * d * Hq * pairs;
+  cost->tiles = tiles;
+  cost->fwd_bytes = 2.0 * qo + 2.0 * kv + ls;                // q, k, v in; out, lse out
+  cost->bwd_bytes = 3.0 * qo + 2.0 * kv + ls + qo + 2.0 * kv;  // q, out, dout, k, v, lse; dq, dk, dv
   return NSP_OK;
 }
 

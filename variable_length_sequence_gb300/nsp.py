@@ -55,7 +55,15 @@ _SIGNATURES = {
     "nsp_seq2head_permute_validate": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32]),
     "nsp_status_query": (_i32, [_vp, _vp]),
     "nsp_attn_pairs": (_i32, [_vp, _i32, _i32, C.POINTER(C.c_double)]),
+    "nsp_attn_cost": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
+                             _vp]),
 }
+
+
+class AttnCost(C.Structure):
+    """nsp_attn_cost_t."""
+    _fields_ = [(n, C.c_double) for n in ("pairs", "fwd_flop", "bwd_flop", "tiles",
+                                           "fwd_bytes", "bwd_bytes")]
 
 
 class NspError(RuntimeError):
@@ -227,6 +235,22 @@ def nsp_attn_pairs(cu_seqlens_host, causal=True) -> float:
     st = load().nsp_attn_pairs(cu.ctypes.data, len(cu) - 1, int(bool(causal)), C.byref(out))
     _check("nsp_attn_pairs", st)
     return out.value
+
+
+def nsp_attn_cost(cu_seqlens_host, Hq, Hkv, d, causal=True, io_dtype=NSP_BF16, q_start=0,
+                  q_len=None, kv_start=0, kv_len=None) -> dict:
+    """Cost of one attention call (whole stream by default) as a dict."""
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    T = int(cu[-1])
+    q_len = T - q_start if q_len is None else q_len
+    kv_len = T - kv_start if kv_len is None else kv_len
+    c = AttnCost()
+    st = load().nsp_attn_cost(cu.ctypes.data, len(cu) - 1, int(q_start), int(q_len),
+                              int(kv_start), int(kv_len), int(Hq), int(Hkv), int(d),
+                              int(bool(causal)), int(io_dtype), C.cast(C.pointer(c), C.c_void_p))
+    _check("nsp_attn_cost", st)
+    return {n: getattr(c, n) for n, _ in AttnCost._fields_}
 
 
 # ----------------------------------------------------------------------------- conveniences
