@@ -297,12 +297,15 @@ class Problem:
 
     def ring_accumulate(self, stream):
         """The ring legs with the merge fused into the attention epilogue: per
-        query shard the first block is a plain float32 partial (it writes the
-        running result), every later block is merged into it in place by
+        query shard the diagonal block is a plain float32 partial (it writes the
+        running result), every other block is merged into it in place by
         nsp_attn_fwd_accumulate.  Result: float32 out and lse per shard."""
         n = self.T // RING_SHARDS
         started = set()
-        for qs, ks, _ in self.ring_pairs:
+        # a ring meets its own (diagonal) block first: that one writes the
+        # running result; the blocks received after it are merged into it
+        order = sorted(self.ring_pairs, key=lambda e: (e[0], e[1] != e[0], e[1]))
+        for qs, ks, _ in order:
             qa, ka = self.bounds[qs][0], self.bounds[ks][0]
             args = (self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n], self.cu,
                     len(self.w.lengths), qa, n, ka, n, self.Hq, self.Hkv, self.d, self.scale,
@@ -491,12 +494,12 @@ def run_ours(args, world, rank, local):
     roof["peak_source"] = peaks["source"] + " (burst)"
 
     extra = None
-    if prob.ring_pairs:
+    if prob.ring_pairs and not args.no_extra:
         extra = time_extra_legs(prob, stream, flush, K, peaks)
         extra["ring_accumulate"]["partials_plus_merge_ms"] = legs["ring_partials"] + legs["merge"]
 
     e2e = None
-    if "bwd" in legs:
+    if "bwd" in legs and not args.no_e2e:
         e2e = run_e2e(args, prob, nsp, w, device, stream, world)
 
     cpu = None
@@ -708,6 +711,10 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the legs timed outside the step (ring accumulate / backward)")
     ap.add_argument("--config", type=int, choices=sorted(CONFIG_LEGS), default=CONFIG_ID,
                     help="workload (default: config 2, the bench workload)")
     args = ap.parse_args()

@@ -136,6 +136,17 @@ __device__ __forceinline__ void add_row32_f32(float* dst, const uint32_t (&v)[32
   }
 }
 
+// dst[0..31] += scale * v as float4 atomic reductions (rows shared by items).
+__device__ __forceinline__ void red_row32_f32(float* dst, const uint32_t (&v)[32], float scale) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    atomicAdd(d4 + i, make_float4(__uint_as_float(v[4 * i]) * scale,
+                                  __uint_as_float(v[4 * i + 1]) * scale,
+                                  __uint_as_float(v[4 * i + 2]) * scale,
+                                  __uint_as_float(v[4 * i + 3]) * scale));
+}
+
 // 1024-aligned view of dynamic shared memory, or nullptr (error recorded)
 // when the aligned structure would not fit in the launch's allocation.
 template <typename S>
@@ -161,6 +172,8 @@ struct BwdArgs {
   const float* nlse2;     // [Hq, Tp] -lse * log2(e)
   const float* delta;     // [Hq, Tp]
   int64_t Tp;
+  int hsplit;             // dK/dV items per (key tile, KV head): each takes G / hsplit
+                          // query heads (> 1 only when accumulating with atomics)
   __nv_bfloat16* dq;      // [q_len, Hq, d]
   __nv_bfloat16* dk;      // [kv_len, Hkv, d]
   __nv_bfloat16* dv;
@@ -176,7 +189,7 @@ struct BwdArgs {
 // ================================================================ dK / dV
 
 struct KvItem {
-  int ktile, g, i_lo, n_q, steps, pad[3];   // steps = G * n_q; -1 stops
+  int ktile, g, h0, i_lo, n_q, steps, pad[2];   // heads h0 .., steps = heads * n_q; -1 stops
 };
 
 struct __align__(1024) SmemKV {
@@ -261,7 +274,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   volatile int* abort_flag = &sm.abort_flag;
   const int G = p.Hq / p.Hkv;
   const int64_t n_keys = p.kv_len;           // keys of the range (row index of K, V, dK, dV)
-  const int n_items = hdr->n_items2 * p.Hkv;
+  const int n_per_tile = p.Hkv * a.hsplit;   // items per key tile
+  const int n_items = hdr->n_items2 * n_per_tile;
+  const int heads_per_item = G / a.hsplit;
 
   if (warp >= 16) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kKvRegsControl));
@@ -270,18 +285,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) {
         uint32_t it_count = 0, kv_count = 0, q_count = 0, loads = 0;
         bool ok = true;
+        // the next item's index is fetched one item ahead: the atomic's round
+        // trip overlaps this item's loads
+        int idx_next = atomicAdd(&hdr->counter2, 1);
         while (ok) {
-          const int idx = atomicAdd(&hdr->counter2, 1);
+          const int idx = idx_next;
+          if (idx < n_items) idx_next = atomicAdd(&hdr->counter2, 1);
           KvItem it;
-          it.ktile = 0; it.g = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
+          it.ktile = 0; it.g = 0; it.h0 = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
           if (idx < n_items) {
-            const int kt = a.korder[idx / p.Hkv];
+            const int kt = a.korder[idx / n_per_tile];
             const int2 tr = a.ktiles[kt];
+            const int rem = idx - (idx / n_per_tile) * n_per_tile;
             it.ktile = kt;
-            it.g = idx - (idx / p.Hkv) * p.Hkv;
+            it.g = rem / a.hsplit;
+            it.h0 = it.g * G + (rem - it.g * a.hsplit) * heads_per_item;
             it.i_lo = tr.x;
             it.n_q = tr.y - tr.x + 1;
-            it.steps = G * it.n_q;
+            it.steps = heads_per_item * it.n_q;
           }
           const uint32_t slot = it_count & 1;
           if (it_count >= 2 &&
@@ -307,7 +328,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           ++kv_count;
           for (int n = 0; n < it.steps; ++n) {
             const int hh = n / it.n_q;
-            const int h = it.g * G + hh;
+            const int h = it.h0 + hh;
             const int i = it.i_lo + (n - hh * it.n_q);
             const uint32_t fill = q_count >> 1;             // fill index of both slots
             const uint32_t sq = q_count & 3, sd = (q_count + 2) & 3;
@@ -633,7 +654,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld32(tmem + lane_base + col + c * 32, v);
           tmem_wait_ld();
           if (key >= n_keys) continue;
-          if (p.accumulate)
+          if (p.accumulate && a.hsplit > 1)     // other items add into the same rows
+            red_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
+          else if (p.accumulate)
             add_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
           else
             store_row32_bf16((is_dk ? a.dk : a.dv) + off + c * 32, v, scale);
@@ -768,8 +791,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it_count = 0, q_count = 0, k_count = 0, v_count = 0;
       bool ok = true;
+      int idx_next = atomicAdd(&hdr->counter, 1);      // fetched one item ahead
       while (ok) {
-        const int idx = atomicAdd(&hdr->counter, 1);
+        const int idx = idx_next;
+        if (idx < n_items) idx_next = atomicAdd(&hdr->counter, 1);
         QItem it;
         it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
         if (idx < n_items) {
@@ -1109,6 +1134,16 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);
   a.korder = reinterpret_cast<const int*>(ws + L.korder);
   const int grid = num_sms();
+  // A ring block has few key tiles: split each (key tile, KV head) item over
+  // query-head subsets until there are two items per SM (the subsets add
+  // into the float32 accumulators with atomics).  The whole-stream backward
+  // writes each dK/dV row once (hsplit = 1).
+  const int G = p.Hq / p.Hkv;
+  a.hsplit = 1;
+  if (p.accumulate)
+    while (a.hsplit < G && G % (2 * a.hsplit) == 0 &&
+           L.n_ktiles * p.Hkv * a.hsplit < 2 * (int64_t)grid)
+      a.hsplit *= 2;
   constexpr size_t kv_bytes = smem_bytes<SmemKV>();
   constexpr size_t q_bytes = smem_bytes<SmemQ>();
   e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
