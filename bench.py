@@ -344,6 +344,18 @@ class Problem:
                 self.Hq, self.Hkv, self.d, self.scale, True, rb["dq"][qa:qa + n],
                 rb["dk"][ka:ka + n], rb["dv"][ka:ka + n], rb["ws"], stream)
 
+    def fwd_headgroups(self, stream):
+        """The forward on q in the all-to-all's receive layout [P][T][Hq/P][d]
+        (the permute leg's output), out in the same layout: the permutations
+        around an Ulysses attention folded into the attention kernel."""
+        if not hasattr(self, "_hg_out"):
+            self._hg_out = torch.empty_like(self.perm)
+            self._hg_lse = torch.empty_like(self.lse)
+        self.nsp.nsp_attn_fwd_headgroups(self.perm, self.k, self.v, self.cu, len(self.w.lengths),
+                                         self.T, self.Hq, self.Hkv, self.d, PERMUTE_GROUPS,
+                                         self.scale, True, self._hg_out, self._hg_lse, self.ws_f,
+                                         stream)
+
     def merged_l_view(self, qs):
         # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
         if not hasattr(self, "_ml"):
@@ -558,11 +570,17 @@ def _time_leg(fn, stream, flush, reps):
 def time_extra_legs(prob, stream, flush, K, peaks):
     """Entry points outside the step, timed alone the same way (graph replay,
     L2 flushed before each timed call, CUDA events on the stream):
+    fwd_headgroups, the forward on the all-to-all's receive layout;
     ring_accumulate, the ring legs with the merge fused into attention, and
     ring_bwd, the ring backward (its three float32 accumulators are zeroed
     inside the timed region, by PyTorch)."""
     reps = max(3, min(K, 50))
     extra = {}
+    if prob.perm is not None and prob.fwd_flop > 0:
+        ms = _time_leg(prob.fwd_headgroups, stream, flush, reps)
+        tf = prob.fwd_flop / ms / 1e9
+        extra["fwd_headgroups"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+                                   "layout": f"q, out [{PERMUTE_GROUPS}][T][Hq/{PERMUTE_GROUPS}][d]"}
     ms = _time_leg(prob.ring_accumulate, stream, flush, reps)
     tf = prob.ring_flop / ms / 1e9
     extra["ring_accumulate"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],

@@ -157,6 +157,32 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
                                 size_t workspace_bytes, nsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Whole-stream forward with q and out in the head-group-major layout an
+ * Ulysses-style all-to-all delivers ([HSAP] Sec. 2.2.2: IntraSP moves
+ * R^{n x H x d} per rank to R^{N x h x d}, h = H / P; [BASP] Sec. II-C):
+ *   q, out: device [P][T][Hq / P][d] (group g holds query heads
+ *     g Hq/P .. (g + 1) Hq/P - 1 of every token, i.e.
+ *     nsp_seq2head_permute's output);
+ *   k, v: device [T][Hkv][d] (the packed layout, not permuted: a group's
+ *     query heads find their key/value head as h / (Hq / Hkv));
+ *   lse: device float32 [Hq, T] or NULL.
+ * The result equals nsp_attn_fwd on the packed layout followed by
+ * nsp_seq2head_permute of out, bit for bit (same kernels, same order of
+ * arithmetic), without either permutation pass: the kernels address the
+ * grouped rows directly (TMA coordinates of a [P T, (Hq/P) d] map).
+ * P must divide Hq; P T must fit in int32.  Kernel choice as nsp_attn_fwd
+ * (tensor cores for bf16, d = 128, even Hq / Hkv; CUDA cores otherwise).
+ * Other arguments and errors: as nsp_attn_fwd
+ * with q_start = kv_start = 0, q_len = kv_len = T (workspace sized by
+ * nsp_attn_fwd_workspace_size(T, T, ...)); a bad P is NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_attn_fwd_headgroups(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t Hq,
+                                int32_t Hkv, int32_t d, int32_t P, float scale, int32_t causal,
+                                int32_t io_dtype, void* out, int32_t out_dtype, float* lse,
+                                void* workspace, size_t workspace_bytes, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * nsp_attn_fwd without a workspace argument.  No page has a counterpart of
  * this entry point: it exists for callers that cannot allocate device
  * memory where they run attention (code inside a custom allocator or

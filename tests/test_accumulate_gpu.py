@@ -107,7 +107,10 @@ def test_config3_ring_accumulate(nsp):
             torch.cuda.synchronize()
             eo, el = max_abs(f64(acc), f64(mo)), max_abs(f64(lse), f64(ml))
             print(f"[C3 shard {qs}: accumulate vs partials+merge] out {eo:.3e} lse {el:.3e}")
-            assert eo <= 1e-4 and el <= 1e-5
+            # both round P to bf16, against different reference maxima (a
+            # partial's own maximum; the running maximum in place): they
+            # agree far inside the 2e-2 bar, not to float32 rounding
+            assert eo <= 1e-3 and el <= 1e-5
     eo = max_abs(f64(acc_all), f64(whole_o))
     el = max_abs(f64(lse_all), f64(whole_l))
     print(f"[C3 accumulate vs unchunked] out {eo:.3e} lse {el:.3e}")

@@ -2,6 +2,7 @@
 // Nothing here allocates memory or synchronises (except nsp_status_query).
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstdio>
 #include <cstring>
 
@@ -123,6 +124,36 @@ int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t*
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   if (launch_fwd_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
   if (q_len == 0) return NSP_OK;
+  bool launched = false;
+  if (launch_attn_fwd_tc(p, L, ws, s, &launched) != cudaSuccess) return NSP_ERR_CUDA;
+  if (!launched && launch_attn_fwd_simt(p, s) != cudaSuccess) return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+int32_t nsp_attn_fwd_headgroups(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t Hq,
+                                int32_t Hkv, int32_t d, int32_t P, float scale, int32_t causal,
+                                int32_t io_dtype, void* out, int32_t out_dtype, float* lse,
+                                void* workspace, size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = nsp_attn_fwd_validate(q, k, v, cu_seqlens, ndoc, 0, T, 0, T, Hq, Hkv, d, causal,
+                                     io_dtype, out, out_dtype, workspace, workspace_bytes);
+  if (st != NSP_OK) return st;
+  if (P < 1 || Hq % P != 0) return NSP_ERR_INVALID;
+  if ((int64_t)P * T > (int64_t)INT32_MAX) return NSP_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
+  if (lse && !aligned16(lse)) return NSP_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  const FwdWsLayout L = fwd_ws_layout(T, T);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = out_dtype; p.out = out; p.lse = lse;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.q_groups = P;
+  if (launch_fwd_schedule(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (T == 0) return NSP_OK;
   bool launched = false;
   if (launch_attn_fwd_tc(p, L, ws, s, &launched) != cudaSuccess) return NSP_ERR_CUDA;
   if (!launched && launch_attn_fwd_simt(p, s) != cudaSuccess) return NSP_ERR_CUDA;

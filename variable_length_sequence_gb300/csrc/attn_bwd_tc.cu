@@ -121,19 +121,32 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
                  w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
 }
 
-// dst[0..31] += scale * v (raw float32 bits), float32 accumulator row chunk
-// (16-byte aligned: rows are 512 bytes, chunks 128).
-__device__ __forceinline__ void add_row32_f32(float* dst, const uint32_t (&v)[32], float scale) {
+// dst[0..31] = scale * v (raw float32 bits), a float32 row chunk (16-byte
+// aligned: rows are 512 bytes, chunks 128).
+__device__ __forceinline__ void store_row32_f32(float* dst, const uint32_t (&v)[32], float scale) {
   float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d4[i] = make_float4(__uint_as_float(v[4 * i]) * scale, __uint_as_float(v[4 * i + 1]) * scale,
+                        __uint_as_float(v[4 * i + 2]) * scale,
+                        __uint_as_float(v[4 * i + 3]) * scale);
+}
+
+// Ring block: a TMEM accumulator's 32 columns of this thread's lane start as
+// src[0..31] * mul (zero when src is null), so the block's products add onto
+// the running float32 gradient and the epilogue writes it back whole.
+__device__ __forceinline__ void preload_row32(uint32_t taddr, const float* src, float mul) {
+  uint32_t v[32];
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float4 o = d4[i];
-    o.x = fmaf(__uint_as_float(v[4 * i]), scale, o.x);
-    o.y = fmaf(__uint_as_float(v[4 * i + 1]), scale, o.y);
-    o.z = fmaf(__uint_as_float(v[4 * i + 2]), scale, o.z);
-    o.w = fmaf(__uint_as_float(v[4 * i + 3]), scale, o.w);
-    d4[i] = o;
+    const float4 x = src != nullptr ? __ldcg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[4 * i] = __float_as_uint(x.x * mul);
+    v[4 * i + 1] = __float_as_uint(x.y * mul);
+    v[4 * i + 2] = __float_as_uint(x.z * mul);
+    v[4 * i + 3] = __float_as_uint(x.w * mul);
   }
+  tmem_st32(taddr, v);
 }
 
 // dst[0..31] += scale * v as float4 atomic reductions (rows shared by items).
@@ -437,7 +450,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
             tc_fence_after();
-            const bool acc = n > 0;
+            // a ring block with one item per (key tile, KV head) adds onto the
+            // preloaded running dK / dV
+            const bool acc = n > 0 || (p.accumulate && a.hsplit == 1);
             mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
             mma_commit(&sm.dv_done[rb]);
             mma_commit(&sm.slot_empty[sd]);
@@ -524,6 +539,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           qlo[i] = (int)min(max(glo - p.q_start, (int64_t)0), p.q_len);
           qhi[i] = (int)min(max(ghi - p.q_start, (int64_t)0), p.q_len);
         }
+      }
+      if (p.accumulate && a.hsplit == 1) {
+        // ring block, one item per (key tile, KV head): dV and dK start as the
+        // running accumulators (dK / scale), TMEM lane = key row
+        const int64_t key = (int64_t)it.ktile * 128 + r;
+        const bool is_dk = cg >= 2;
+        const float* src = key < n_keys ? (is_dk ? a.dk_acc : a.dv_acc) +
+                                              (key * p.Hkv + it.g) * HD + (cg & 1) * 64
+                                        : nullptr;
+        const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
+        const float mul = is_dk ? 1.f / p.scale : 1.f;
+        preload_row32(tmem + lane_base + col, src, mul);
+        preload_row32(tmem + lane_base + col + 32, src ? src + 32 : nullptr, mul);
+        tmem_wait_st();
       }
       for (int n = 0; n < it.steps; ++n) {
         const int hh = n / it.n_q;
@@ -656,8 +685,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (key >= n_keys) continue;
           if (p.accumulate && a.hsplit > 1)     // other items add into the same rows
             red_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
-          else if (p.accumulate)
-            add_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
+          else if (p.accumulate)                // the running value was preloaded
+            store_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
           else
             store_row32_bf16((is_dk ? a.dk : a.dv) + off + c * 32, v, scale);
         }
@@ -931,7 +960,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_t_split<64>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]), jj > 0);   // dQ += dS K
+          // (a ring block adds onto the preloaded running dQ)
+          mma_t_split<64>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]),
+                          jj > 0 || p.accumulate);                             // dQ += dS K
           mma_commit(&sm.dq_done[b]);
           mma_commit(&sm.k_empty[st]);
           ++jc;
@@ -975,6 +1006,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
         nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + row);
         deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
+      }
+      if (p.accumulate && it.n_kv > 0) {
+        // ring block: dQ's TMEM accumulator starts as the running dq / scale
+        const float* src = valid ? a.dq_acc + (row * p.Hq + h) * HD + wg * 64 : nullptr;
+        const uint32_t col = tmem + lane_base + 384 + wg * 64;
+        preload_row32(col, src, 1.f / p.scale);
+        preload_row32(col + 32, src ? src + 32 : nullptr, 1.f / p.scale);
+        tmem_wait_st();
       }
       for (int jj = 0; jj < it.n_kv; ++jj) {
         const uint32_t b = jc & 1;
@@ -1041,8 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + 384 + wg * 64 + c * 32, v);
           tmem_wait_ld();
           if (!valid) continue;
-          if (p.accumulate)
-            add_row32_f32(a.dq_acc + (row * p.Hq + h) * HD + wg * 64 + c * 32, v, p.scale);
+          if (p.accumulate)           // the running value was preloaded
+            store_row32_f32(a.dq_acc + (row * p.Hq + h) * HD + wg * 64 + c * 32, v, p.scale);
           else
             store_row32_bf16(dst + c * 32, v, p.scale);
         }

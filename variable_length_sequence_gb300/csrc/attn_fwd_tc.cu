@@ -251,13 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
-        const int row0 = it.qtile * BM;
+        // packed layout: map [q_len, Hq d]; head groups: map [P q_len, (Hq/P) d],
+        // head h at column block h % (Hq/P) of rows (h / (Hq/P)) q_len + row
+        const int hpg = p.Hq / p.q_groups;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < 2; ++t) {
+          const int grp = (it.h0 + t) / hpg;
+          const int row0 = (int)(grp * p.q_len) + it.qtile * BM;
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full, (it.h0 + t) * HD + cb * 64,
-                        row0);
+            tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full,
+                        (it.h0 + t - grp * hpg) * HD + cb * 64, row0);
+        }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
@@ -336,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(&sm.p_full[t], p_count[t] & 1, abort_flag, hdr)) { ok = false; continue; }
             ++p_count[t];
             tc_fence_after();
-            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0);
+            // a ring accumulation's O starts as the preloaded running output
+            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0 || p.accumulate);
             if (t == 1) mma_commit(&sm.v_empty[st]);
             if (!has_next) {
               mma_commit(&sm.o_full[t]);
@@ -392,16 +398,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         lo = (int)(glo - p.kv_start);
         hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
       }
-      // ring accumulation: the running lse is read now and the running
-      // output row is brought into L2, so the epilogue does not wait on DRAM
-      float la_row = -INFINITY;
-      if (p.accumulate && valid && hi > lo) {
-        la_row = p.lse[(int64_t)h * p.q_len + row];
-        const float* arow = reinterpret_cast<const float*>(p.out) + (row * p.Hq + h) * HD;
-#pragma unroll
-        for (int c = 0; c < HD * 4 / 128; ++c) prefetch_l2(arow + c * 32);
-      }
       float m = -INFINITY, l = 0.f;
+      // Ring accumulation: a row that sees a key of this block (acc_row)
+      // enters the online softmax with its running result as one more
+      // weighted term: O starts as the running output acc, with weight 1 at
+      // the reference maximum m = lse_acc (log2 units), so at the end O / l
+      // and m + log2 l are the merged output and lse (the rescaling of O and
+      // l as the maximum grows covers acc too).  The preload runs while the
+      // item's first S is computed; the block's first P V then accumulates
+      // onto it.  Every other row starts from O = 0 and is not written.
+      const bool acc_row = p.accumulate && valid && hi > lo;
+      if constexpr (sizeof(TO) == 4) {
+        if (p.accumulate && it.n_kv > 0) {
+          float la2 = -INFINITY;
+          if (acc_row) la2 = p.lse[(int64_t)h * p.q_len + row] * kLog2e;
+          const float4* arow = reinterpret_cast<const float4*>(out + qo_offset(p, row, h));
+          {
+            // the whole 512-byte row in flight at once (one DRAM round trip;
+            // S's registers are not live yet)
+            uint32_t v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 x = la2 != -INFINITY ? __ldcg(arow + c * 8 + i)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[c][4 * i] = __float_as_uint(x.x);
+                v[c][4 * i + 1] = __float_as_uint(x.y);
+                v[c][4 * i + 2] = __float_as_uint(x.z);
+                v[c][4 * i + 3] = __float_as_uint(x.w);
+              }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st32(o_tm + c * 32, v[c]);
+          }
+          tmem_wait_st();              // before a first-tile rescale reads O back
+          if (la2 != -INFINITY) {
+            m = la2;
+            l = 1.f;
+          }
+        }
+      }
       bool ok = true;
       for (int jj = 0; jj < it.n_kv; ++jj) {
         if (!mbar_wait(&sm.s_full[t], s_count & 1, abort_flag, hdr)) { ok = false; break; }
@@ -480,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      TO* dst = out + (row * p.Hq + h) * HD;
+      TO* dst = out + qo_offset(p, row, h);
       if (it.n_kv > 0) {
         if (!mbar_wait(&sm.o_full[t], o_count & 1, abort_flag, hdr)) break;
         ++o_count;
@@ -490,33 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // of a row write 32 contiguous bytes and consecutive stores of a
           // warp continue the same 8 rows; thread t holds rows 8 i + t/4 of
           // the warp's 32 (i = 0..3)
-          //
-          // Ring accumulation (acc, lse_acc updated in place): with this
-          // block's lse_p = m + log2 l (log2 units) and the running lse_a,
-          // lse' = log2(2^lse_a + 2^lse_p), acc' = 2^(lse_a - lse') acc +
-          // 2^(m - lse') O, since O / l weighted by 2^(lse_p - lse') is
-          // O 2^(m - lse').  A row seeing no key keeps (acc, lse_a); a row
-          // whose lse_a is -inf is written without reading acc.
-          float wa = 0.f, wp = inv;
-          if (p.accumulate) {
-            wp = 0.f;
-            if (valid && l > 0.f) {
-              float* lse_a = p.lse + (int64_t)h * p.q_len + row;
-              const float lp2 = m + __log2f(l);
-              const float la2 = la_row * kLog2e;
-              const float mx = fmaxf(la2, lp2);
-              const float l2 = mx + __log2f(ex2(la2 - mx) + ex2(lp2 - mx));
-              wa = ex2(la2 - l2);
-              wp = ex2(m - l2);
-              *lse_a = l2 * kLn2;
-            }
-          }
-          float war[4], wpr[4];
+          // (ring accumulation: rows that saw no key of the block keep their
+          // running output, so they are skipped)
+          const float wp = (p.accumulate && !acc_row) ? 0.f : inv;
+          float wpr[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            war[i] = __shfl_sync(0xffffffffu, wa, 8 * i + (lane >> 2));
-            wpr[i] = __shfl_sync(0xffffffffu, wp, 8 * i + (lane >> 2));
-          }
+          for (int i = 0; i < 4; ++i) wpr[i] = __shfl_sync(0xffffffffu, wp, 8 * i + (lane >> 2));
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t x[32];
@@ -527,18 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
               const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + 8 * i + (lane >> 2);
-              if (grow < p.q_len && !(p.accumulate && wpr[i] == 0.f)) {
-                float2* d = reinterpret_cast<float2*>(
-                    out + (grow * p.Hq + h) * HD + c * 32 + 8 * ((k >> 1) & 3) + 2 * (lane & 3));
-                float2 y = make_float2(__uint_as_float(x[2 * k]) * wpr[i],
-                                       __uint_as_float(x[2 * k + 1]) * wpr[i]);
-                if (war[i] != 0.f) {
-                  const float2 a = *d;
-                  y.x = fmaf(war[i], a.x, y.x);
-                  y.y = fmaf(war[i], a.y, y.y);
-                }
-                *d = y;
-              }
+              if (grow < p.q_len && (!p.accumulate || wpr[i] != 0.f))
+                *reinterpret_cast<float2*>(out + qo_offset(p, grow, h) + c * 32 +
+                                           8 * ((k >> 1) & 3) + 2 * (lane & 3)) =
+                    make_float2(__uint_as_float(x[2 * k]) * wpr[i],
+                                __uint_as_float(x[2 * k + 1]) * wpr[i]);
             }
           }
         } else {
@@ -560,10 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + rr + sub;
           if (grow < p.q_len)
-            reinterpret_cast<uint4*>(out + (grow * p.Hq + h) * HD)[part] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(out + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
         }
       }
-      if (valid && p.lse != nullptr && !p.accumulate)
+      if (valid && p.lse != nullptr && (!p.accumulate || acc_row))
         p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
@@ -629,7 +637,7 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
   if (p.io_dtype != NSP_BF16 || p.d != HD || (p.Hq / p.Hkv) % 2 != 0) return cudaSuccess;
   if (p.q_len <= 0 || p.kv_len <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.q_len, (int64_t)p.Hq * HD) ||
+  if (!make_map(&mq, p.q, p.q_len * p.q_groups, (int64_t)(p.Hq / p.q_groups) * HD) ||
       !make_map(&mk, p.k, p.kv_len, (int64_t)p.Hkv * HD) ||
       !make_map(&mv, p.v, p.kv_len, (int64_t)p.Hkv * HD))
     return cudaSuccess;                       // no tensor-map support: CUDA-core path

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kFwdThreads) attn_fwd_simt_kernel(AttnProblem 
   const float sl2 = p.scale * kLog2e;
 #pragma unroll
   for (int c = 0; c < DH; ++c)
-    qr[c] = valid ? ld_in(Q + (row * p.Hq + h) * D + half * DH + c) * sl2 : 0.f;
+    qr[c] = valid ? ld_in(Q + qo_offset(p, row, h) + half * DH + c) * sl2 : 0.f;
 
   float o[DH];
 #pragma unroll
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kFwdThreads) attn_fwd_simt_kernel(AttnProblem 
     const float mx = fmaxf(la, lp);
     const float L = mx + logf(expf(la - mx) + expf(lp - mx));
     const float wa = expf(la - L), wp = expf(lp - L) * inv;
-    float* A = reinterpret_cast<float*>(p.out) + (row * p.Hq + h) * D + half * DH;
+    float* A = reinterpret_cast<float*>(p.out) + qo_offset(p, row, h) + half * DH;
 #pragma unroll
     for (int c = 0; c < DH; ++c) A[c] = fmaf(wa, A[c], wp * o[c]);
     if (half == 0) p.lse[(int64_t)h * p.q_len + row] = L;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kFwdThreads) attn_fwd_simt_kernel(AttnProblem 
   if (!valid) return;
   TO* O = reinterpret_cast<TO*>(p.out);
 #pragma unroll
-  for (int c = 0; c < DH; ++c) st_out(O + (row * p.Hq + h) * D + half * DH + c, o[c] * inv);
+  for (int c = 0; c < DH; ++c) st_out(O + qo_offset(p, row, h) + half * DH + c, o[c] * inv);
   if (half == 0 && p.lse != nullptr)
     p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }

@@ -106,6 +106,9 @@ struct AttnProblem {
   // unchanged).  Backward: add the block's dq/dk/dv into float32
   // accumulators instead of writing io-typed gradients.
   int32_t accumulate = 0;
+  // Query / output layout: 1 = [q_len, Hq, d]; P > 1 = the head-group-major
+  // [P][q_len][Hq / P][d] layout an all-to-all delivers (forward only).
+  int32_t q_groups = 1;
 };
 
 // ---- launchers implemented in the .cu files (return cudaError_t) ----
@@ -163,6 +166,16 @@ __device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int ndoc, 
     if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Element offset of (range-relative row, query head h) in q / out: the
+// packed [rows, Hq, d] layout, or the head-group-major [P][rows][Hq/P][d]
+// layout when p.q_groups = P > 1.
+__device__ __forceinline__ int64_t qo_offset(const AttnProblem& p, int64_t row, int h) {
+  if (p.q_groups <= 1) return (row * p.Hq + h) * p.d;
+  const int hpg = p.Hq / p.q_groups;
+  const int g = h / hpg;
+  return (((int64_t)g * p.q_len + row) * hpg + (h - g * hpg)) * p.d;
 }
 
 __device__ __forceinline__ bool status_bad(const WsHeader* hdr) {

@@ -36,6 +36,8 @@ _SIGNATURES = {
                             _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_accumulate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                        _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "nsp_attn_fwd_headgroups": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                       _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
     "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
@@ -163,6 +165,17 @@ def nsp_attn_fwd_accumulate(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start,
     return _check("nsp_attn_fwd_accumulate", st)
 
 
+def nsp_attn_fwd_headgroups(q, k, v, cu_seqlens, ndoc, T, Hq, Hkv, d, P, scale, causal, out, lse,
+                            workspace, stream=None) -> int:
+    st = load().nsp_attn_fwd_headgroups(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(ndoc),
+                                        int(T), int(Hq), int(Hkv), int(d), int(P), float(scale),
+                                        int(bool(causal)), _dtype(q), _ptr(out), _dtype(out),
+                                        _ptr(lse), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
+    return _check("nsp_attn_fwd_headgroups", st)
+
+
 def nsp_attn_fwd_noalloc(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len, Hq, Hkv,
                          d, scale, causal, out, lse, device_status=None, stream=None) -> int:
     """nsp_attn_fwd for callers that cannot allocate: no workspace argument
@@ -271,6 +284,23 @@ def attn_fwd(q, k, v, cu_seqlens, scale=None, causal=True, out_dtype=None, q_sta
                                 dtype=torch.uint8, device=q.device)
     nsp_attn_fwd(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, q_start, q_len, kv_start, kv_len,
                  Hq, Hkv, d, scale, causal, out, lse, workspace, stream)
+    return out, lse
+
+
+def attn_fwd_headgroups(qg, k, v, cu_seqlens, scale=None, causal=True, out_dtype=None,
+                        workspace=None, stream=None):
+    """Forward on q in the head-group-major layout qg [P, T, Hq/P, d]; returns
+    out in the same layout and lse [Hq, T]."""
+    P, T, hpg, d = qg.shape
+    Hq, Hkv = P * hpg, k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    out = torch.empty(qg.shape, dtype=out_dtype or qg.dtype, device=qg.device)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=qg.device)
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d), dtype=torch.uint8,
+                                device=qg.device)
+    nsp_attn_fwd_headgroups(qg, k, v, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, d, P, scale,
+                            causal, out, lse, workspace, stream)
     return out, lse
 
 
