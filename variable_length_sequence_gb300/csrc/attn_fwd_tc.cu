@@ -37,6 +37,13 @@
 // document's start up to itself, clipped to the key range), so a KV tile
 // is either fully visible to a row or masked per column by two compares;
 // tiles no row can see are never scheduled.
+//
+// Ring accumulation (p.accumulate, float32 out): the row's running output
+// and lse enter the online softmax as one more term (O preloaded at the
+// item's start, m = running lse, l = 1), so the plain epilogue writes the
+// merged result.  Head groups (p.q_groups = P > 1): q and out are
+// [P][q_len][Hq/P][d]; the Q map is [P q_len, (Hq/P) d] and a head's tile
+// sits at row block (h / (Hq/P)) q_len, column block h % (Hq/P).
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
