@@ -356,6 +356,22 @@ class Problem:
                                          self.scale, True, self._hg_out, self._hg_lse, self.ws_f,
                                          stream)
 
+    def bwd_headgroups(self, stream):
+        """The backward in the same receive layout (q, out, dout, dq grouped;
+        k, v, dk, dv packed), on the grouped forward's out and lse."""
+        if not hasattr(self, "_hg_dout"):
+            self._hg_dout = torch.empty_like(self.perm)
+            self.nsp.nsp_seq2head_permute(self.dout, self._hg_dout, self.T, self.Hq, self.d,
+                                          PERMUTE_GROUPS, False, stream)
+            self._hg_dq = torch.empty_like(self.perm)
+            self._hg_dk = torch.empty_like(self.k)
+            self._hg_dv = torch.empty_like(self.v)
+        self.nsp.nsp_attn_bwd_headgroups(self.perm, self.k, self.v, self._hg_out, self._hg_dout,
+                                         self._hg_lse, self.cu, len(self.w.lengths), self.T,
+                                         self.Hq, self.Hkv, self.d, PERMUTE_GROUPS, self.scale,
+                                         True, self._hg_dq, self._hg_dk, self._hg_dv, self.ws_b,
+                                         stream)
+
     def merged_l_view(self, qs):
         # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
         if not hasattr(self, "_ml"):
@@ -570,7 +586,8 @@ def _time_leg(fn, stream, flush, reps):
 def time_extra_legs(prob, stream, flush, K, peaks):
     """Entry points outside the step, timed alone the same way (graph replay,
     L2 flushed before each timed call, CUDA events on the stream):
-    fwd_headgroups, the forward on the all-to-all's receive layout;
+    fwd_headgroups / bwd_headgroups, forward and backward on the all-to-all's
+    receive layout;
     ring_accumulate, the ring legs with the merge fused into attention, and
     ring_bwd, the ring backward (its three float32 accumulators are zeroed
     inside the timed region, by PyTorch)."""
@@ -581,6 +598,12 @@ def time_extra_legs(prob, stream, flush, K, peaks):
         tf = prob.fwd_flop / ms / 1e9
         extra["fwd_headgroups"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
                                    "layout": f"q, out [{PERMUTE_GROUPS}][T][Hq/{PERMUTE_GROUPS}][d]"}
+        if prob.bwd_flop > 0:
+            ms = _time_leg(prob.bwd_headgroups, stream, flush, reps)
+            tf = prob.bwd_flop / ms / 1e9
+            extra["bwd_headgroups"] = {"ms": ms, "tflops": tf,
+                                       "frac_bf16": tf / peaks["bf16_tflops"],
+                                       "layout": "q, out, dout, dq grouped; k, v, dk, dv packed"}
     ms = _time_leg(prob.ring_accumulate, stream, flush, reps)
     tf = prob.ring_flop / ms / 1e9
     extra["ring_accumulate"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],

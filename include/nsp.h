@@ -251,6 +251,25 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
                               size_t workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * Whole-stream backward in the Ulysses receive layout, the backward of
+ * nsp_attn_fwd_headgroups ([HSAP] Sec. 2.2.2; [BASP] Sec. II-C):
+ *   q, out, dout, dq: device [P][T][Hq / P][d] (head-group-major);
+ *   k, v, dk, dv: device [T][Hkv][d] (packed);
+ *   lse: device float32 [Hq, T].
+ * The gradients equal nsp_attn_bwd on the packed layout with dq moved by
+ * nsp_seq2head_permute, bit for bit, without the permutation passes.
+ * P must divide Hq; P T must fit in int32.  Other arguments, workspace
+ * (nsp_attn_bwd_workspace_size(T, ...)) and errors: as nsp_attn_bwd; a bad P
+ * is NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_attn_bwd_headgroups(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t Hq,
+                                int32_t Hkv, int32_t d, int32_t P, float scale, int32_t causal,
+                                int32_t io_dtype, void* dq, void* dk, void* dv, void* workspace,
+                                size_t workspace_bytes, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Ring-block backward: one (query range, key range) block's share of the
  * gradients, added into float32 accumulators.  In ring-style InterSP
  * ([HSAP] Sec. 2.2.1) each rank keeps its query shard and the key/value

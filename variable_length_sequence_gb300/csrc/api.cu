@@ -246,6 +246,36 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   return e == cudaSuccess ? NSP_OK : NSP_ERR_CUDA;
 }
 
+int32_t nsp_attn_bwd_headgroups(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse,
+                                const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t Hq,
+                                int32_t Hkv, int32_t d, int32_t P, float scale, int32_t causal,
+                                int32_t io_dtype, void* dq, void* dk, void* dv, void* workspace,
+                                size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = nsp_attn_bwd_validate(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d,
+                                     causal, io_dtype, dq, dk, dv, workspace, workspace_bytes);
+  if (st != NSP_OK) return st;
+  if (P < 1 || Hq % P != 0) return NSP_ERR_INVALID;
+  if ((int64_t)P * T > (int64_t)INT32_MAX) return NSP_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  const bool tc = bwd_tc_eligible(io_dtype, d, Hq, Hkv);
+  const BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
+  AttnProblem p;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = io_dtype; p.out = nullptr; p.lse = nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.q_groups = P;
+  if (launch_bwd_schedules(p, L, ws, s) != cudaSuccess) return NSP_ERR_CUDA;
+  if (T == 0) return NSP_OK;
+  const cudaError_t e = tc ? launch_attn_bwd_tc(p, out, dout, lse, dq, dk, dv, L, ws, s)
+                           : launch_attn_bwd_simt(p, out, dout, lse, dq, dk, dv, L, ws, s);
+  return e == cudaSuccess ? NSP_OK : NSP_ERR_CUDA;
+}
+
 size_t nsp_attn_bwd_accumulate_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq,
                                               int32_t Hkv, int32_t d, int32_t io_dtype) {
   (void)Hkv; (void)io_dtype;

@@ -298,12 +298,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) {
         uint32_t it_count = 0, kv_count = 0, q_count = 0, loads = 0;
         bool ok = true;
-        // the next item's index is fetched one item ahead: the atomic's round
-        // trip overlaps this item's loads
-        int idx_next = atomicAdd(&hdr->counter2, 1);
         while (ok) {
-          const int idx = idx_next;
-          if (idx < n_items) idx_next = atomicAdd(&hdr->counter2, 1);
+          const int idx = atomicAdd(&hdr->counter2, 1);
           KvItem it;
           it.ktile = 0; it.g = 0; it.h0 = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
           if (idx < n_items) {
@@ -351,10 +347,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&sm.slot_full[sq], kTile + 128 * sizeof(float));
+            // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
+            const int hpg = p.Hq / p.q_groups, grp = h / hpg;
+            const int qx = (h - grp * hpg) * HD, qy = (int)(grp * p.q_len) + i * 128;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], h * HD + cb * 64,
-                          i * 128);
+              tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], qx + cb * 64, qy);
             const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
             bulk_load(sm.vec[sq], a.nlse2 + row, 128 * sizeof(float), &sm.slot_full[sq]);
             ++loads;
@@ -366,8 +364,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mbar_arrive_expect_tx(&sm.slot_full[sd], kTile + 128 * sizeof(float));
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.qd[sd] + cb * kBlk, &tm_do, &sm.slot_full[sd], h * HD + cb * 64,
-                          i * 128);
+              tma_load_2d(sm.qd[sd] + cb * kBlk, &tm_do, &sm.slot_full[sd], qx + cb * 64, qy);
             bulk_load(sm.vec[sd], a.delta + row, 128 * sizeof(float), &sm.slot_full[sd]);
             ++loads;
             ++q_count;
@@ -820,10 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it_count = 0, q_count = 0, k_count = 0, v_count = 0;
       bool ok = true;
-      int idx_next = atomicAdd(&hdr->counter, 1);      // fetched one item ahead
       while (ok) {
-        const int idx = idx_next;
-        if (idx < n_items) idx_next = atomicAdd(&hdr->counter, 1);
+        const int idx = atomicAdd(&hdr->counter, 1);
         QItem it;
         it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
         if (idx < n_items) {
@@ -853,11 +848,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTile);
+        {
+          // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
+          const int hpg = p.Hq / p.q_groups, grp = it.h / hpg;
+          const int qx = (it.h - grp * hpg) * HD, qy = (int)(grp * p.q_len) + it.qtile * 128;
 #pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-          tma_load_2d(sm.q + cb * kBlk, &tm_q, &sm.q_full, it.h * HD + cb * 64, it.qtile * 128);
-          tma_load_2d(sm.dout + cb * kBlk, &tm_do, &sm.q_full, it.h * HD + cb * 64,
-                      it.qtile * 128);
+          for (int cb = 0; cb < 2; ++cb) {
+            tma_load_2d(sm.q + cb * kBlk, &tm_q, &sm.q_full, qx + cb * 64, qy);
+            tma_load_2d(sm.dout + cb * kBlk, &tm_do, &sm.q_full, qx + cb * 64, qy);
+          }
         }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
@@ -1009,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (p.accumulate && it.n_kv > 0) {
         // ring block: dQ's TMEM accumulator starts as the running dq / scale
-        const float* src = valid ? a.dq_acc + (row * p.Hq + h) * HD + wg * 64 : nullptr;
+        const float* src = valid ? a.dq_acc + qo_offset(p, row, h) + wg * 64 : nullptr;
         const uint32_t col = tmem + lane_base + 384 + wg * 64;
         preload_row32(col, src, 1.f / p.scale);
         preload_row32(col + 32, src ? src + 32 : nullptr, 1.f / p.scale);
@@ -1070,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: dQ = scale * accumulated dS K, written once in bf16 (my half of d)
-      __nv_bfloat16* dst = a.dq + (row * p.Hq + h) * HD + wg * 64;
+      __nv_bfloat16* dst = a.dq + qo_offset(p, row, h) + wg * 64;
       if (it.n_kv > 0) {
         if (!mbar_wait(&sm.o_full, items_done & 1, abort_flag, hdr)) break;
         tc_fence_after();
@@ -1081,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (!valid) continue;
           if (p.accumulate)           // the running value was preloaded
-            store_row32_f32(a.dq_acc + (row * p.Hq + h) * HD + wg * 64 + c * 32, v, p.scale);
+            store_row32_f32(a.dq_acc + qo_offset(p, row, h) + wg * 64 + c * 32, v, p.scale);
           else
             store_row32_bf16(dst + c * 32, v, p.scale);
         }
@@ -1149,13 +1148,14 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   const int64_t T = p.q_len;
   CUtensorMap mq, mdo, mk, mv;
   const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
-  if (!make_map(&mq, p.q, T, qc) || !make_map(&mdo, dout, T, qc) ||
+  const int64_t qrows = T * p.q_groups, qcols = qc / p.q_groups;   // grouped: [P T, (Hq/P) d]
+  if (!make_map(&mq, p.q, qrows, qcols) || !make_map(&mdo, dout, qrows, qcols) ||
       !make_map(&mk, p.k, p.kv_len, kc) || !make_map(&mv, p.v, p.kv_len, kc))
     return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
   cudaError_t e = launch_bwd_delta(out, dout, lse, delta, nlse2, T, L.Tp, p.Hq, HD, p.io_dtype,
-                                   p.hdr, s);
+                                   p.q_groups, p.hdr, s);
   if (e != cudaSuccess) return e;
   BwdArgs a;
   a.p = p;

@@ -222,12 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it_count = 0, q_count = 0, kv_count = 0;
       bool ok = true;
-      // the next item's index is fetched one item ahead: the atomic's round
-      // trip overlaps this item's loads
-      int idx_next = atomicAdd(&hdr->counter, 1);
       while (ok) {
-        const int idx = idx_next;
-        if (idx < n_items) idx_next = atomicAdd(&hdr->counter, 1);
+        const int idx = atomicAdd(&hdr->counter, 1);
         Item it;
         it.qtile = -1; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
         if (idx < n_items) {

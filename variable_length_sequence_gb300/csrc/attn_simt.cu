@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
         const int rr = e / D, c = e % D;
         const int64_t t = t0 + rr;
         const bool ok = t < r_hi;
-        sm.q[rr][c] = ok ? ld_in(Q + (t * p.Hq + h) * D + c) : 0.f;
-        sm.dO[rr][c] = ok ? ld_in(dout + (t * p.Hq + h) * D + c) : 0.f;
+        sm.q[rr][c] = ok ? ld_in(Q + qo_offset(p, t, h) + c) : 0.f;
+        sm.dO[rr][c] = ok ? ld_in(dout + qo_offset(p, t, h) + c) : 0.f;
       }
       if (tid < kBwdBM) {
         const int64_t t = t0 + tid;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kBwdThreads) attn_bwd_dkdv_simt_kernel(
         float acc = 0.f;
 #pragma unroll 8
         for (int jj = 0; jj < kBwdBK; ++jj) acc = fmaf(sm.ds[rr][jj], sm.k[jj][c], acc);
-        if (acc != 0.f) atomicAdd(dq_acc + (t * p.Hq + h) * D + c, acc * p.scale);
+        if (acc != 0.f) atomicAdd(dq_acc + qo_offset(p, t, h) + c, acc * p.scale);
       }
     }
   }
@@ -327,7 +327,7 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
   if (!p.accumulate) e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)T * p.Hq * D, s);
   if (e != cudaSuccess) return e;
   e = launch_bwd_delta(out, dout, lse, delta, reinterpret_cast<float*>(ws + L.nlse2), T, L.Tp,
-                       p.Hq, D, p.io_dtype, p.hdr, s);
+                       p.Hq, D, p.io_dtype, p.q_groups, p.hdr, s);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(BwdSmem<D>);
   e = cudaFuncSetAttribute(attn_bwd_dkdv_simt_kernel<TI, D>,

@@ -29,14 +29,16 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&x)[4]) {
 
 // delta[h, t] = <dout[t, h, :], out[t, h, :]> and nlse2[h, t] = -lse[h, t] log2(e),
 // both with row stride Tp (rows padded to whole tiles, padding set to 0);
-// TPR threads share one (t, h) row.
+// TPR threads share one (t, h) row.  Rows are walked in memory order: the
+// packed [T, Hq, d] layout (P = 1) or the head-group-major [P][T][Hq/P][d].
 template <typename TI, int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ out,
                                                         const TI* __restrict__ dout,
                                                         const float* __restrict__ lse,
                                                         float* __restrict__ delta,
                                                         float* __restrict__ nlse2, int64_t T,
-                                                        int64_t Tp, int Hq, const WsHeader* hdr) {
+                                                        int64_t Tp, int Hq, int P,
+                                                        const WsHeader* hdr) {
   constexpr int VEC = 16 / sizeof(TI);
   constexpr int TPR = D / VEC;                  // 16 (bf16, d=128) ... 32 (f32, d=128)
   constexpr int RPW = 32 / TPR;                 // rows per warp step
@@ -61,8 +63,18 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (rr < rows && part == 0) {
-      const int64_t t = rr / Hq;
-      const int h = (int)(rr - t * Hq);
+      int64_t t;
+      int h;
+      if (P <= 1) {
+        t = rr / Hq;
+        h = (int)(rr - t * Hq);
+      } else {                              // rr = (g T + t) (Hq/P) + j, h = g (Hq/P) + j
+        const int hpg = Hq / P;
+        const int64_t gt = rr / hpg;
+        const int64_t g = gt / T;
+        t = gt - g * T;
+        h = (int)(g * hpg + (rr - gt * hpg));
+      }
       delta[(int64_t)h * Tp + t] = acc;
       nlse2[(int64_t)h * Tp + t] = lse[(int64_t)h * T + t] * -1.4426950408889634f;
     }
@@ -103,26 +115,26 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
                              float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
-                             WsHeader* hdr, cudaStream_t s) {
+                             int P, WsHeader* hdr, cudaStream_t s) {
   const int blocks = num_sms() * 8;
   if (io_dtype == NSP_BF16) {
     if (d == 128)
       bwd_delta_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, s>>>(
           reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, nlse2, T, Tp, Hq, hdr);
+          lse, delta, nlse2, T, Tp, Hq, P, hdr);
     else
       bwd_delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(
           reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, nlse2, T, Tp, Hq, hdr);
+          lse, delta, nlse2, T, Tp, Hq, P, hdr);
   } else {
     if (d == 128)
       bwd_delta_kernel<float, 128><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
                                                          reinterpret_cast<const float*>(dout),
-                                                         lse, delta, nlse2, T, Tp, Hq, hdr);
+                                                         lse, delta, nlse2, T, Tp, Hq, P, hdr);
     else
       bwd_delta_kernel<float, 64><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
                                                         reinterpret_cast<const float*>(dout),
-                                                        lse, delta, nlse2, T, Tp, Hq, hdr);
+                                                        lse, delta, nlse2, T, Tp, Hq, P, hdr);
   }
   count_launches(1);
   return cudaGetLastError();

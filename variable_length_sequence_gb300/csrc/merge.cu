@@ -49,7 +49,7 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
 }
 
 template <typename TO>
-__global__ void __launch_bounds__(kMergeThreads, 2) lse_merge_kernel(MergePtrs ptrs, int n,
+__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(MergePtrs ptrs, int n,
                                                                   int64_t T, int H, int d,
                                                                   TO* __restrict__ out,
                                                                   float* __restrict__ lse_out) {

@@ -106,8 +106,8 @@ struct AttnProblem {
   // unchanged).  Backward: add the block's dq/dk/dv into float32
   // accumulators instead of writing io-typed gradients.
   int32_t accumulate = 0;
-  // Query / output layout: 1 = [q_len, Hq, d]; P > 1 = the head-group-major
-  // [P][q_len][Hq / P][d] layout an all-to-all delivers (forward only).
+  // Query-side layout (q, out, dout, dq): 1 = [q_len, Hq, d]; P > 1 = the
+  // head-group-major [P][q_len][Hq / P][d] layout an all-to-all delivers.
   int32_t q_groups = 1;
 };
 
@@ -130,7 +130,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
                                const BwdWsLayout& L, char* ws, cudaStream_t s);
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
                              float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
-                             WsHeader* hdr, cudaStream_t s);
+                             int P, WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n, int io_dtype,
                               WsHeader* hdr, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,

@@ -47,6 +47,9 @@ _SIGNATURES = {
                             _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_bwd_validate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
                                      _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz]),
+    "nsp_attn_bwd_headgroups": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                       _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
+                                       _vp]),
     "nsp_attn_bwd_accumulate_workspace_size": (_sz, [_i64, _i64, _i32, _i32, _i32, _i32]),
     "nsp_attn_bwd_accumulate": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64,
                                        _i64, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp,
@@ -198,6 +201,18 @@ def nsp_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d, scale
     return _check("nsp_attn_bwd", st)
 
 
+def nsp_attn_bwd_headgroups(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, Hq, Hkv, d, P, scale,
+                            causal, dq, dk, dv, workspace, stream=None) -> int:
+    st = load().nsp_attn_bwd_headgroups(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                        _ptr(lse), _ptr(cu_seqlens), int(ndoc), int(T), int(Hq),
+                                        int(Hkv), int(d), int(P), float(scale),
+                                        int(bool(causal)), _dtype(q), _ptr(dq), _ptr(dk),
+                                        _ptr(dv), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream))
+    return _check("nsp_attn_bwd_headgroups", st)
+
+
 def nsp_attn_bwd_accumulate_workspace_size(q_len: int, kv_len: int, Hq: int, Hkv: int, d: int,
                                            io_dtype: int = NSP_BF16) -> int:
     return int(load().nsp_attn_bwd_accumulate_workspace_size(q_len, kv_len, Hq, Hkv, d,
@@ -302,6 +317,21 @@ def attn_fwd_headgroups(qg, k, v, cu_seqlens, scale=None, causal=True, out_dtype
     nsp_attn_fwd_headgroups(qg, k, v, cu_seqlens, cu_seqlens.numel() - 1, T, Hq, Hkv, d, P, scale,
                             causal, out, lse, workspace, stream)
     return out, lse
+
+
+def attn_bwd_headgroups(qg, k, v, outg, doutg, lse, cu_seqlens, scale=None, causal=True,
+                        workspace=None, stream=None):
+    """Backward with q, out, dout (and the returned dq) in [P, T, Hq/P, d]."""
+    P, T, hpg, d = qg.shape
+    Hq, Hkv = P * hpg, k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(qg), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, _dtype(qg)),
+                                dtype=torch.uint8, device=qg.device)
+    nsp_attn_bwd_headgroups(qg, k, v, outg, doutg, lse, cu_seqlens, cu_seqlens.numel() - 1, T,
+                            Hq, Hkv, d, P, scale, causal, dq, dk, dv, workspace, stream)
+    return dq, dk, dv
 
 
 def ring_accumulate_init(q_len, Hq, d, device):
