@@ -60,8 +60,8 @@ RING_SHARDS = 8
 PERMUTE_GROUPS = 8
 L2_FLUSH_BYTES = 256 << 20
 # ncu DRAM read + write bytes of one main-forward launch of this workload
-# (378.1 MB + 234.9 MB), taken on the current forward kernel.
-FWD_LAUNCH_DRAM_BYTES = 613.0e6
+# (374.2 MB + 234.4 MB), taken on the current forward kernel.
+FWD_LAUNCH_DRAM_BYTES = 608.6e6
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -287,13 +287,16 @@ class Problem:
                                   self.part_l[(qs, ks)], self.ws_r, stream)
 
     def merge(self, stream):
+        """Every shard's partials merged in one launch (nsp_lse_merge_batch)."""
         n = self.T // RING_SHARDS
+        segments, outs, lses = [], [], []
         for qs in range(RING_SHARDS):
             keys = [(a, b) for a, b, _ in self.ring_pairs if a == qs]
             qa = self.bounds[qs][0]
-            self.nsp.nsp_lse_merge([self.part_o[p] for p in keys],
-                                   [self.part_l[p] for p in keys],
-                                   self.merged_o[qa:qa + n], self.merged_l_view(qs), stream)
+            segments.append(([self.part_o[p] for p in keys], [self.part_l[p] for p in keys]))
+            outs.append(self.merged_o[qa:qa + n])
+            lses.append(self.merged_l_view(qs))
+        self.nsp.nsp_lse_merge_batch(segments, outs, lses, stream)
 
     def ring_accumulate(self, stream):
         """The ring legs with the merge fused into the attention epilogue: per

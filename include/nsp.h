@@ -331,6 +331,27 @@ int32_t nsp_lse_merge_validate(const float* const* outs, const float* const* lse
                                int32_t out_dtype, const float* lse);
 
 /* ------------------------------------------------------------------------
+ * Several independent LSE merges in one launch: segment g combines its
+ * counts[g] partials into out[g] / lse[g], exactly as nsp_lse_merge would
+ * (same arithmetic, same results).  For a ring on one GPU this merges every
+ * query shard at once ([HSAP] Sec. 2.2.1), so the launch ramps up and
+ * drains once instead of once per shard.
+ *   nseg: 1 .. 16 segments, each of T tokens, H heads, head dim d.
+ *   counts: HOST int32 [nseg], each >= 1, sum <= 64.
+ *   outs, lses: HOST arrays of sum(counts) device pointers, segment after
+ *     segment (layouts as in nsp_lse_merge).
+ *   out: HOST array of nseg device pointers [T, H, d] (out_dtype);
+ *   lse: HOST array of nseg device pointers [H, T] (entries may be NULL),
+ *     or NULL.
+ * Errors: as nsp_lse_merge, per segment; bad nseg / counts are
+ * NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_lse_merge_batch(int32_t nseg, const int32_t* counts, const float* const* outs,
+                            const float* const* lses, int64_t T, int32_t H, int32_t d,
+                            void* const* out, int32_t out_dtype, float* const* lse,
+                            nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Ulysses seq -> head permutation ([HSAP] Sec. 2.2.2: blocks in
  * R^{n x H x d} per group become R^{N x h x d}, h = H / P; [BASP] Sec. II-C).
  * With the P sequence shards stacked on this device as in = [T, H, d]:

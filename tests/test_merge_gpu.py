@@ -63,3 +63,33 @@ def test_merge_edge_rows(nsp):
     assert max_abs(f64(go), o1) <= 1e-6 and max_abs(f64(gl), l1) <= 1e-6
     go, gl = nsp.lse_merge([torch.from_numpy(o2).cuda()] * 3, [torch.from_numpy(l2).cuda()] * 3)
     assert torch.all(go == 0) and torch.all(torch.isneginf(gl))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_merge_batch_equals_single_merges(nsp, out_dtype):
+    """nsp_lse_merge_batch: 5 segments of 1-9 partials in one launch give the
+    same bits as one nsp_lse_merge per segment, and the oracle merge."""
+    r = np.random.default_rng(8)
+    T, H, d = 333, 8, 128
+    segments, refs = [], []
+    for g, n in enumerate((1, 3, 9, 2, 4)):
+        outs = [torch.from_numpy(r.standard_normal((T, H, d)).astype(np.float32)).cuda()
+                for _ in range(n)]
+        lses = []
+        for i in range(n):
+            l = r.standard_normal((H, T)).astype(np.float32) * 3
+            l[:, r.integers(0, T, 20)] = -np.inf                 # rows without keys
+            if g == 3:
+                l[:, :7] = -np.inf                               # rows that saw nothing at all
+            lses.append(torch.from_numpy(l).cuda())
+        segments.append((outs, lses))
+        refs.append(nsp.lse_merge(outs, lses, out_dtype=out_dtype))
+    outs_m = [torch.empty((T, H, d), dtype=out_dtype, device="cuda") for _ in segments]
+    lses_m = [torch.empty((H, T), dtype=torch.float32, device="cuda") for _ in segments]
+    nsp.nsp_lse_merge_batch(segments, outs_m, lses_m)
+    torch.cuda.synchronize()
+    for (ro, rl), go, gl, (outs, lses) in zip(refs, outs_m, lses_m, segments):
+        assert torch.equal(go, ro) and torch.equal(gl, rl)
+        oo, ol = oracle.lse_merge([f64(o) for o in outs], [f64(l) for l in lses])
+        tol = 1e-5 if out_dtype == torch.float32 else 2e-2
+        assert max_abs(f64(go), oo) <= tol and max_abs(f64(gl), ol) <= 1e-5

@@ -350,6 +350,32 @@ int32_t nsp_lse_merge(const float* const* outs, const float* const* lses, int32_
   return NSP_OK;
 }
 
+int32_t nsp_lse_merge_batch(int32_t nseg, const int32_t* counts, const float* const* outs,
+                            const float* const* lses, int64_t T, int32_t H, int32_t d,
+                            void* const* out, int32_t out_dtype, float* const* lse,
+                            nsp_stream_t stream) {
+  if (nseg < 1 || nseg > 16 || !counts || !out) return NSP_ERR_INVALID;
+  int total = 0;
+  for (int g = 0; g < nseg; ++g) {
+    if (counts[g] < 1) return NSP_ERR_INVALID;
+    total += counts[g];
+  }
+  if (total > 64) return NSP_ERR_INVALID;
+  int first = 0;
+  for (int g = 0; g < nseg; ++g) {     // each segment: the checks of nsp_lse_merge
+    const int32_t st = nsp_lse_merge_validate(outs ? outs + first : nullptr,
+                                              lses ? lses + first : nullptr, counts[g], T, H, d,
+                                              out[g], out_dtype, lse ? lse[g] : nullptr);
+    if (st != NSP_OK) return st;
+    first += counts[g];
+  }
+  if (T == 0) return NSP_OK;
+  if (launch_lse_merge_segments(nseg, counts, outs, lses, T, H, d, out, out_dtype, lse,
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
 int32_t nsp_seq2head_permute_validate(const void* in, const void* out, int64_t T, int32_t H,
                                       int32_t d, int32_t P, int32_t elem_bytes) {
   if (T < 0 || H < 1 || d < 1 || P < 1 || H % P != 0) return NSP_ERR_INVALID;

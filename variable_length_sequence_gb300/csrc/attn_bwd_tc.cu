@@ -348,8 +348,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             mbar_arrive_expect_tx(&sm.slot_full[sq], kTile + 128 * sizeof(float));
             // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
-            const int hpg = p.Hq / p.q_groups, grp = h / hpg;
-            const int qx = (h - grp * hpg) * HD, qy = (int)(grp * p.q_len) + i * 128;
+            int qx = h * HD, qy = i * 128;
+            if (p.q_groups > 1) {
+              const int hpg = p.Hq / p.q_groups, grp = h / hpg;
+              qx = (h - grp * hpg) * HD;
+              qy += (int)(grp * p.q_len);
+            }
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
               tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], qx + cb * 64, qy);

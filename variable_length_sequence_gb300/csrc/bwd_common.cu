@@ -31,7 +31,7 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&x)[4]) {
 // both with row stride Tp (rows padded to whole tiles, padding set to 0);
 // TPR threads share one (t, h) row.  Rows are walked in memory order: the
 // packed [T, Hq, d] layout (P = 1) or the head-group-major [P][T][Hq/P][d].
-template <typename TI, int D>
+template <typename TI, int D, bool GROUPED>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ out,
                                                         const TI* __restrict__ dout,
                                                         const float* __restrict__ lse,
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const TI* __restrict__ o
     if (rr < rows && part == 0) {
       int64_t t;
       int h;
-      if (P <= 1) {
+      if constexpr (!GROUPED) {
         t = rr / Hq;
         h = (int)(rr - t * Hq);
       } else {                              // rr = (g T + t) (Hq/P) + j, h = g (Hq/P) + j
@@ -117,25 +117,26 @@ cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse
                              float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
                              int P, WsHeader* hdr, cudaStream_t s) {
   const int blocks = num_sms() * 8;
-  if (io_dtype == NSP_BF16) {
-    if (d == 128)
-      bwd_delta_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, nlse2, T, Tp, Hq, P, hdr);
-    else
-      bwd_delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(
-          reinterpret_cast<const __nv_bfloat16*>(out), reinterpret_cast<const __nv_bfloat16*>(dout),
-          lse, delta, nlse2, T, Tp, Hq, P, hdr);
-  } else {
-    if (d == 128)
-      bwd_delta_kernel<float, 128><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
-                                                         reinterpret_cast<const float*>(dout),
-                                                         lse, delta, nlse2, T, Tp, Hq, P, hdr);
-    else
-      bwd_delta_kernel<float, 64><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(out),
-                                                        reinterpret_cast<const float*>(dout),
-                                                        lse, delta, nlse2, T, Tp, Hq, P, hdr);
-  }
+  const bool g = P > 1;
+  auto go = [&](auto kern, const auto* o, const auto* dq) {
+    kern<<<blocks, 256, 0, s>>>(o, dq, lse, delta, nlse2, T, Tp, Hq, P, hdr);
+  };
+  using bf = __nv_bfloat16;
+  const bf* ob = reinterpret_cast<const bf*>(out);
+  const bf* db = reinterpret_cast<const bf*>(dout);
+  const float* of = reinterpret_cast<const float*>(out);
+  const float* df = reinterpret_cast<const float*>(dout);
+  // the packed layout's instantiation has no head-group arithmetic at all
+  if (io_dtype == NSP_BF16 && d == 128)
+    g ? go(bwd_delta_kernel<bf, 128, true>, ob, db) : go(bwd_delta_kernel<bf, 128, false>, ob, db);
+  else if (io_dtype == NSP_BF16)
+    g ? go(bwd_delta_kernel<bf, 64, true>, ob, db) : go(bwd_delta_kernel<bf, 64, false>, ob, db);
+  else if (d == 128)
+    g ? go(bwd_delta_kernel<float, 128, true>, of, df)
+      : go(bwd_delta_kernel<float, 128, false>, of, df);
+  else
+    g ? go(bwd_delta_kernel<float, 64, true>, of, df)
+      : go(bwd_delta_kernel<float, 64, false>, of, df);
   count_launches(1);
   return cudaGetLastError();
 }

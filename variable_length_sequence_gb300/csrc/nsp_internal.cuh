@@ -136,6 +136,10 @@ cudaError_t launch_dq_convert(const float* acc, void* dq, int64_t n, int io_dtyp
 cudaError_t launch_lse_merge(const float* const* outs, const float* const* lses, int n,
                              int64_t T, int H, int d, void* out, int out_dtype, float* lse,
                              cudaStream_t s);
+cudaError_t launch_lse_merge_segments(int nseg, const int* counts, const float* const* outs,
+                                      const float* const* lses, int64_t T, int H, int d,
+                                      void* const* dst, int out_dtype, float* const* dst_lse,
+                                      cudaStream_t s);
 cudaError_t launch_permute(const void* in, void* out, int64_t T, int H, int d, int P,
                            int elem_bytes, int inverse, cudaStream_t s);
 

@@ -55,6 +55,7 @@ _SIGNATURES = {
                                        _i64, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp,
                                        _vp, _sz, _vp]),
     "nsp_lse_merge": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "nsp_lse_merge_batch": (_i32, [_i32, _vp, _vp, _vp, _i64, _i32, _i32, _vp, _i32, _vp, _vp]),
     "nsp_lse_merge_validate": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp]),
     "nsp_seq2head_permute": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
     "nsp_seq2head_permute_validate": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32]),
@@ -240,6 +241,27 @@ def nsp_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], ou
     st = load().nsp_lse_merge(C.cast(po, C.c_void_p), C.cast(pl, C.c_void_p), n, T, H, d,
                               _ptr(out), _dtype(out), _ptr(lse), _stream(stream))
     return _check("nsp_lse_merge", st)
+
+
+def nsp_lse_merge_batch(segments, outs_merged, lses_merged=None, stream=None) -> int:
+    """segments: list of (outs, lses) partial lists; outs_merged / lses_merged:
+    one tensor per segment (lses_merged entries may be None)."""
+    nseg = len(segments)
+    counts = (C.c_int32 * nseg)(*[len(o) for o, _ in segments])
+    po = [_ptr(o) for os_, _ in segments for o in os_]
+    pl = [_ptr(l) for _, ls in segments for l in ls]
+    T, H, d = segments[0][0][0].shape
+    a_o = (C.c_void_p * len(po))(*po)
+    a_l = (C.c_void_p * len(pl))(*pl)
+    a_d = (C.c_void_p * nseg)(*[_ptr(o) for o in outs_merged])
+    a_dl = None
+    if lses_merged is not None:
+        a_dl = C.cast((C.c_void_p * nseg)(*[_ptr(l) if l is not None else None
+                                             for l in lses_merged]), C.c_void_p)
+    st = load().nsp_lse_merge_batch(nseg, C.cast(counts, C.c_void_p), C.cast(a_o, C.c_void_p),
+                                    C.cast(a_l, C.c_void_p), T, H, d, C.cast(a_d, C.c_void_p),
+                                    _dtype(outs_merged[0]), a_dl, _stream(stream))
+    return _check("nsp_lse_merge_batch", st)
 
 
 def nsp_seq2head_permute(inp, out, T, H, d, P, inverse=False, stream=None) -> int:
