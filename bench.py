@@ -524,14 +524,14 @@ def run_ours(args, world, rank, local):
             "algorithmic_flop": prob.fwd_flop if main_fwd else prob.ring_flop}
     roof["peak_source"] = peaks["source"] + " (burst)"
 
+    e2e = None
+    if "bwd" in legs and not args.no_e2e:
+        e2e = run_e2e(args, prob, nsp, w, device, stream, world)
+
     extra = None
     if prob.ring_pairs and not args.no_extra:
         extra = time_extra_legs(prob, stream, flush, K, peaks)
         extra["ring_accumulate"]["partials_plus_merge_ms"] = legs["ring_partials"] + legs["merge"]
-
-    e2e = None
-    if "bwd" in legs and not args.no_e2e:
-        e2e = run_e2e(args, prob, nsp, w, device, stream, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and cid == CONFIG_ID:
