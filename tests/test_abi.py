@@ -170,3 +170,33 @@ def test_attn_cost_matches_enumeration(lib, causal):
     assert whole["bwd_bytes"] == 4 * row_q + 4 * row_kv + lse
     with pytest.raises(nsp.NspError):
         nsp.nsp_attn_cost(cu, 32, 4, 128, causal, nsp.NSP_BF16, 10, T)   # past the stream
+
+
+def test_batch_merge_and_headgroups_reject_on_host(lib):
+    """nsp_lse_merge_batch, nsp_attn_fwd_headgroups, nsp_attn_bwd_headgroups:
+    bad segment counts, head groups that do not divide Hq and misaligned
+    pointers are refused before any launch."""
+    outs = (C.c_void_p * 3)(A, A + 4096, A + 8192)
+    lses = (C.c_void_p * 3)(A + 12288, A + 16384, A + 20480)
+    dst = (C.c_void_p * 2)(A + 65536, A + 131072)
+
+    def merge(nseg, counts, o=outs):
+        c = (C.c_int32 * len(counts))(*counts)
+        return lib.nsp_lse_merge_batch(nseg, C.cast(c, C.c_void_p), C.cast(o, C.c_void_p),
+                                       C.cast(lses, C.c_void_p), 16, 4, 128,
+                                       C.cast(dst, C.c_void_p), nsp.NSP_BF16, None, None)
+    assert merge(0, [1]) == nsp.NSP_ERR_INVALID
+    assert merge(2, [1, 0]) == nsp.NSP_ERR_INVALID
+    assert merge(17, [1] * 17) == nsp.NSP_ERR_INVALID
+    bad = (C.c_void_p * 3)(A, A + 4100, A + 8192)                # second partial misaligned
+    assert merge(2, [1, 2], bad) == nsp.NSP_ERR_ALIGN
+    a = fwd_args()
+    ws = a["ws_bytes"]
+    for P in (0, 3, 64):
+        assert lib.nsp_attn_fwd_headgroups(a["q"], a["k"], a["v"], a["cu"], 3, 300, 32, 4, 128, P,
+                                           0.088, 1, nsp.NSP_BF16, a["out"], nsp.NSP_BF16, None,
+                                           a["ws"], ws, None) == nsp.NSP_ERR_INVALID
+    wsb = nsp.nsp_attn_bwd_workspace_size(300, 32, 4, 128, nsp.NSP_BF16)
+    ptrs = [A + 4096 * i for i in range(10)]
+    assert lib.nsp_attn_bwd_headgroups(*ptrs[:7], 3, 300, 32, 4, 128, 5, 0.088, 1, nsp.NSP_BF16,
+                                       *ptrs[7:10], A + (1 << 16), wsb, None) == nsp.NSP_ERR_INVALID
