@@ -641,7 +641,7 @@ def run_e2e(args, prob, nsp, w, device, stream, world):
             for n in ("out", "lse", "dq", "dk", "dv")}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_cu.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
-    K = max(2, min(args.steps, 10))
+    K = max(2, min(args.steps, 30))       # the pipeline fills and drains once per run
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event(enable_timing=False)
     in_ready = [ev() for _ in range(K)]
