@@ -814,7 +814,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &sm.abort_flag;
   const int G = p.Hq / p.Hkv;
   const int64_t T = p.q_len;
-  const int n_items = hdr->n_items * p.Hq;
+  // a ring block's query tiles that see no key add nothing: not work items
+  const int n_items = (p.accumulate ? hdr->n_nonempty : hdr->n_items) * p.Hq;
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer

@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &sm.abort_flag;
   const int n_pairs = p.Hq >> 1;
   const int G = p.Hq / p.Hkv;
-  const int n_items = hdr->n_items * n_pairs;
+  // query tiles no key of the range reaches are not work items: the softmax
+  // warps zero-fill them up front (or, accumulating, leave them alone)
+  const int n_items = hdr->n_nonempty * n_pairs;
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -381,6 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t kv_end = p.kv_start + p.kv_len;
     uint32_t it_count = 0, s_count = 0, o_count = 0;
     TO* const out = reinterpret_cast<TO*>(p.out);
+    if (!p.accumulate) {
+      // Query tiles that see no key of the range (listed last by the
+      // schedule): out = 0 and lse = -inf, written by the softmax warps of
+      // every CTA in a grid-stride loop over (tile, head, 32-row group), one
+      // whole row per 16-byte lane group, before the first work item.
+      const int n_empty = hdr->n_items - hdr->n_nonempty;
+      const int64_t units = (int64_t)n_empty * p.Hq * 4;
+      constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
+      constexpr int kRowsPerPass = 32 / kLanesPerRow;
+      const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+      for (int64_t u = (int64_t)blockIdx.x * 8 + warp; u < units; u += (int64_t)gridDim.x * 8) {
+        const int e = (int)(u / (p.Hq * 4));
+        const int rem = (int)(u - (int64_t)e * p.Hq * 4);
+        const int hz = rem >> 2;
+        const int64_t r0 = (int64_t)order[hdr->n_nonempty + e] * BM + (rem & 3) * 32;
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += kRowsPerPass) {
+          const int64_t grow = r0 + rr + sub;
+          if (grow < p.q_len)
+            reinterpret_cast<uint4*>(out + qo_offset(p, grow, hz))[part] = make_uint4(0, 0, 0, 0);
+        }
+        if (p.lse != nullptr && r0 + lane < p.q_len)
+          p.lse[(int64_t)hz * p.q_len + r0 + lane] = -INFINITY;
+      }
+    }
     while (true) {
       const uint32_t slot = it_count & 1;
       if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;

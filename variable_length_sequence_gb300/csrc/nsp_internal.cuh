@@ -17,7 +17,8 @@ struct WsHeader {
   int32_t max_cost;     // largest per-q-tile KV-tile count
   int32_t counter2;     // second work counter (backward dK/dV)
   int32_t n_items2;
-  int32_t pad[58];      // header is 256 bytes
+  int32_t n_nonempty;   // query tiles that see a key (listed first in the order)
+  int32_t pad[57];      // header is 256 bytes
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must stay 256 bytes");
 

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
         a.hdr->status = NSP_ERR_INVALID;
         a.hdr->n_items = 0; a.hdr->counter = 0;
         a.hdr->n_items2 = 0; a.hdr->counter2 = 0;
-        a.hdr->max_cost = 0;
+        a.hdr->max_cost = 0; a.hdr->n_nonempty = 0;
       }
       return;
     }
@@ -153,6 +153,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     run += h;
   }
   __syncthreads();
+  // the empty tiles (cost 0) come last: hist[0] is where they start
+  if (tid == 0 && !a.second) a.hdr->n_nonempty = hist[0];
 
   for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
     const int2 t = a.tiles[i];
