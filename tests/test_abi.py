@@ -2,6 +2,7 @@
 include/nsp.h declares, and rejects bad arguments on the host before any
 CUDA call (only the *_validate entry points and host helpers run here)."""
 import ctypes as C
+import os
 
 import numpy as np
 import pytest
@@ -200,3 +201,37 @@ def test_batch_merge_and_headgroups_reject_on_host(lib):
     ptrs = [A + 4096 * i for i in range(10)]
     assert lib.nsp_attn_bwd_headgroups(*ptrs[:7], 3, 300, 32, 4, 128, 5, 0.088, 1, nsp.NSP_BF16,
                                        *ptrs[7:10], A + (1 << 16), wsb, None) == nsp.NSP_ERR_INVALID
+
+
+def test_plain_c_program_links_and_calls(lib, tmp_path):
+    """The header is plain C and the library links into a C program with no
+    torch or Python: a host-only call (nsp_attn_cost) from C gives the pairs
+    an enumeration gives."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_nsp.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "nsp.h"
+int main(void) {
+  const int32_t cu[4] = {0, 3, 3, 7};          /* lengths 3, 0, 4 */
+  nsp_attn_cost_t c;
+  int32_t st = nsp_attn_cost(cu, 3, 0, 7, 0, 7, 8, 2, 64, 1, NSP_BF16, &c);
+  printf("%d %.0f %.0f %s\n", st, c.pairs, c.tiles, nsp_version());
+  return st;
+}
+''')
+    exe = tmp_path / "use_nsp"
+    libdir = os.path.dirname(nsp.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-I", os.path.dirname(nsp.HEADER), str(src),
+                        "-o", str(exe), f"-L{libdir}", "-l:libnsp.so", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    st, pairs, tiles, version = out.stdout.split(maxsplit=3)
+    assert (int(st), int(pairs), int(tiles)) == (nsp.NSP_OK, 6 + 10, 1)
+    assert "sm_103a" in version
