@@ -125,10 +125,14 @@ int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
 
 /* ------------------------------------------------------------------------
  * Ring partial accumulated in place: the partial block of nsp_attn_fwd
- * merged into a running result by the attention epilogue itself.  This is
- * the ring's online accumulation (HSAP Sec. 2.2.1) with the receive-side
- * rescale fused into the attention computation, as HSAP's Limitations
- * section proposes; nsp_lse_merge is the same combine as a separate pass.
+ * merged into a running result inside the attention kernel itself (the
+ * running result enters the online softmax as one more weighted term).
+ * This is the ring's online accumulation (HSAP Sec. 2.2.1) with the
+ * receive-side rescale fused into the attention computation, as HSAP's
+ * Limitations section proposes; nsp_lse_merge is the same combine as a
+ * separate pass.  Results agree with partials + nsp_lse_merge to well
+ * inside the stated tolerances, not bit for bit (P is rounded to bf16
+ * against a different reference maximum).
  *
  * For the query rows [q_start, q_start + q_len) against the keys
  * [kv_start, kv_start + kv_len) (global token ids, checked against
