@@ -1,0 +1,125 @@
+"""Races and stray writes, without a sanitizer (none is available here).
+
+* Grid independence: the persistent attention kernels take work items
+  dynamically, and each item is computed whole by one CTA, so the results
+  must be bit-identical whatever the number of CTAs.  The grid is shrunk
+  through the NSP_PERSISTENT_CTAS environment variable; a race between CTAs
+  (a shared buffer, a counter, a schedule read before it is written) shows
+  up as a bit difference.
+* Guard zones: every output is a view into a larger buffer whose guard bytes
+  before and after hold a pattern; after the calls the guards must be
+  unchanged, so no kernel writes past the rows, heads or tiles it owns.
+"""
+import os
+
+import pytest
+import torch
+
+from gpu_common import to_dev
+from variable_length_sequence_gb300.workloads import make_custom
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096           # bytes on each side; keeps every view 16-byte aligned
+PATTERN = 0x5A
+
+
+def _run_all(nsp, w, dev):
+    """Forward, backward, a ring partial block and the head-grouped forward."""
+    sc = w.cfg.d ** -0.5
+    out, lse = nsp.attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], scale=sc)
+    dq, dk, dv = nsp.attn_bwd(dev["q"], dev["k"], dev["v"], out, dev["dout"], lse, dev["cu"],
+                              scale=sc)
+    qa, ka = 200, 64
+    po, pl = nsp.attn_fwd(dev["q"][qa:], dev["k"][ka:], dev["v"][ka:], dev["cu"], scale=sc,
+                          out_dtype=torch.float32, q_start=qa, kv_start=ka)
+    og, lg = nsp.attn_fwd_headgroups(nsp.seq2head(dev["q"], 2), dev["k"], dev["v"], dev["cu"],
+                                     scale=sc)
+    torch.cuda.synchronize()
+    return [out, lse, dq, dk, dv, po, pl, og, lg]
+
+
+@pytest.mark.parametrize("lens", [[100, 1, 300, 60, 250, 0, 517], [33] * 40 + [700]],
+                         ids=["mixed", "short_docs"])
+def test_results_do_not_depend_on_the_grid(nsp, lens):
+    w = make_custom(lens, 8, 2, 128, seed=70)
+    dev = to_dev(w)
+    ref = _run_all(nsp, w, dev)
+    old = os.environ.get("NSP_PERSISTENT_CTAS")
+    try:
+        for ctas in ("1", "7", "64"):
+            os.environ["NSP_PERSISTENT_CTAS"] = ctas
+            got = _run_all(nsp, w, dev)
+            for i, (a, b) in enumerate(zip(ref, got)):
+                assert torch.equal(a, b), f"output {i} differs with {ctas} CTAs"
+    finally:
+        if old is None:
+            os.environ.pop("NSP_PERSISTENT_CTAS", None)
+        else:
+            os.environ["NSP_PERSISTENT_CTAS"] = old
+
+
+def _guarded(shape, dtype):
+    n = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((GUARD + n + GUARD,), PATTERN, dtype=torch.uint8, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(dtype).view(shape)
+
+
+def _guards_intact(buf):
+    return bool((buf[:GUARD] == PATTERN).all()) and bool((buf[-GUARD:] == PATTERN).all())
+
+
+def test_outputs_stay_inside_their_buffers(nsp):
+    w = make_custom([100, 1, 300, 60, 250, 0, 129], 8, 2, 128, seed=71)
+    dev = to_dev(w)
+    T, Hq, Hkv, d = w.T, 8, 2, 128
+    sc = d ** -0.5
+    bufs = {}
+
+    def g(name, shape, dtype):
+        b, t = _guarded(shape, dtype)
+        bufs[name] = b
+        return t
+
+    ws_f = g("ws_f", (nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d),), torch.uint8)
+    ws_b = g("ws_b", (nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d),), torch.uint8)
+    out, lse = g("out", (T, Hq, d), torch.bfloat16), g("lse", (Hq, T), torch.float32)
+    nsp.nsp_attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], len(w.lengths), 0, T, 0, T, Hq,
+                     Hkv, d, sc, True, out, lse, ws_f)
+    dq = g("dq", (T, Hq, d), torch.bfloat16)
+    dk, dv = g("dk", (T, Hkv, d), torch.bfloat16), g("dv", (T, Hkv, d), torch.bfloat16)
+    nsp.nsp_attn_bwd(dev["q"], dev["k"], dev["v"], out, dev["dout"], lse, dev["cu"],
+                     len(w.lengths), T, Hq, Hkv, d, sc, True, dq, dk, dv, ws_b)
+    # a ring block: partial, in-place accumulation, block backward
+    qa, ka, n = 256, 0, T - 256
+    po, pl = g("po", (n, Hq, d), torch.float32), g("pl", (Hq, n), torch.float32)
+    ws_r = g("ws_r", (nsp.nsp_attn_fwd_workspace_size(n, n, Hq, Hkv, d),), torch.uint8)
+    nsp.nsp_attn_fwd(dev["q"][qa:], dev["k"][ka:ka + n], dev["v"][ka:ka + n], dev["cu"],
+                     len(w.lengths), qa, n, ka, n, Hq, Hkv, d, sc, True, po, pl, ws_r)
+    nsp.nsp_attn_fwd_accumulate(dev["q"][qa:], dev["k"][ka:ka + n], dev["v"][ka:ka + n],
+                                dev["cu"], len(w.lengths), qa, n, ka, n, Hq, Hkv, d, sc, True,
+                                po, pl, ws_r)
+    gq = g("gq", (n, Hq, d), torch.float32)
+    gk, gv = g("gk", (n, Hkv, d), torch.float32), g("gv", (n, Hkv, d), torch.float32)
+    for t in (gq, gk, gv):
+        t.zero_()
+    ws_ba = g("ws_ba", (nsp.nsp_attn_bwd_accumulate_workspace_size(n, n, Hq, Hkv, d),),
+              torch.uint8)
+    nsp.nsp_attn_bwd_accumulate(dev["q"][qa:], dev["k"][ka:ka + n], dev["v"][ka:ka + n],
+                                out[qa:], dev["dout"][qa:], lse[:, qa:].contiguous(), dev["cu"],
+                                len(w.lengths), qa, n, ka, n, Hq, Hkv, d, sc, True, gq, gk, gv,
+                                ws_ba)
+    # merge (single and batched) and the permutation both ways
+    mo, ml = g("mo", (n, Hq, d), torch.bfloat16), g("ml", (Hq, n), torch.float32)
+    nsp.nsp_lse_merge([po, po], [pl, pl], mo, ml)
+    mb, mbl = g("mb", (n, Hq, d), torch.float32), g("mbl", (Hq, n), torch.float32)
+    mb2 = g("mb2", (n, Hq, d), torch.float32)
+    nsp.nsp_lse_merge_batch([([po], [pl]), ([po, po], [pl, pl])], [mb, mb2], [mbl, None])
+    perm = g("perm", (4, T, Hq // 4, d), torch.bfloat16)
+    back = g("back", (T, Hq, d), torch.bfloat16)
+    nsp.nsp_seq2head_permute(dev["q"], perm, T, Hq, d, 4, False)
+    nsp.nsp_seq2head_permute(perm, back, T, Hq, d, 4, True)
+    torch.cuda.synchronize()
+    bad = [name for name, b in bufs.items() if not _guards_intact(b)]
+    assert not bad, f"guard bytes overwritten around: {bad}"
+    assert torch.equal(back, dev["q"])

@@ -4,6 +4,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "nsp_internal.cuh"
@@ -23,6 +24,22 @@ int num_sms() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     n = 148;
   if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// CTAs of the persistent attention kernels: one per SM, or the positive
+// integer in the environment variable NSP_PERSISTENT_CTAS (read at every
+// launch, capped at the SM count).  Each work item is computed whole by one
+// CTA, so results do not depend on the grid: tests run several grids and
+// compare bits to expose scheduling races.
+int persistent_grid() {
+  const int n = num_sms();
+  const char* e = std::getenv("NSP_PERSISTENT_CTAS");
+  if (e != nullptr && *e != 0) {
+    char* end = nullptr;
+    const long v = std::strtol(e, &end, 10);
+    if (end != nullptr && *end == 0 && v > 0) return (int)std::min<long>(v, n);
+  }
   return n;
 }
 

@@ -1177,7 +1177,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   a.qorder = reinterpret_cast<const int*>(ws + L.qorder);
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);
   a.korder = reinterpret_cast<const int*>(ws + L.korder);
-  const int grid = num_sms();
+  const int grid = persistent_grid();
   // A ring block has few key tiles: split each (key tile, KV head) item over
   // query-head subsets until there are two items per SM (the subsets add
   // into the float32 accumulators with atomics).  The whole-stream backward

@@ -650,7 +650,7 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int grid = num_sms();
+  const int grid = persistent_grid();
   e = launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, mq, mk, mv, p,
                        reinterpret_cast<const int2*>(ws + L.tiles),
                        reinterpret_cast<const int*>(ws + L.order));

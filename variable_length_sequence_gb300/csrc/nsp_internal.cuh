@@ -147,6 +147,10 @@ cudaError_t launch_permute(const void* in, void* out, int64_t T, int H, int d, i
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// Grid of the persistent attention kernels (num_sms(), or fewer CTAs when
+// the environment variable NSP_PERSISTENT_CTAS asks for it).
+int persistent_grid();
+
 // Adds n to the library-wide count of kernels launched (nsp_kernel_launches).
 void count_launches(int n);
 

@@ -247,6 +247,8 @@ def nsp_lse_merge_batch(segments, outs_merged, lses_merged=None, stream=None) ->
     """segments: list of (outs, lses) partial lists; outs_merged / lses_merged:
     one tensor per segment (lses_merged entries may be None)."""
     nseg = len(segments)
+    if len({o.dtype for o in outs_merged}) != 1:
+        raise ValueError("nsp_lse_merge_batch: every merged output must have the same dtype")
     counts = (C.c_int32 * nseg)(*[len(o) for o, _ in segments])
     po = [_ptr(o) for os_, _ in segments for o in os_]
     pl = [_ptr(l) for _, ls in segments for l in ls]
