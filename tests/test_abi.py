@@ -235,3 +235,19 @@ int main(void) {
     st, pairs, tiles, version = out.stdout.split(maxsplit=3)
     assert (int(st), int(pairs), int(tiles)) == (nsp.NSP_OK, 6 + 10, 1)
     assert "sm_103a" in version
+
+
+def test_binding_arity_matches_header(lib):
+    """Every ctypes signature in the binding has as many arguments as the
+    header's declaration of that function (a shifted argument would pass
+    the wrong pointer)."""
+    import re
+    with open(nsp.HEADER) as f:
+        src = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    decls = {}
+    for m in re.finditer(r"\b(nsp_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src):
+        params = m.group(2).strip()
+        decls[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    for name, (_, args) in nsp._SIGNATURES.items():
+        assert name in decls, name
+        assert len(args) == decls[name], (name, len(args), decls[name])
