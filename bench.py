@@ -59,9 +59,6 @@ CONFIG_LEGS = {2: ("fwd", "bwd", "ring_partials", "merge", "permute"),
 RING_SHARDS = 8
 PERMUTE_GROUPS = 8
 L2_FLUSH_BYTES = 256 << 20
-# ncu DRAM read + write bytes of one main-forward launch of this workload
-# (374.1 MB + 234.7 MB), taken on the current forward kernel.
-FWD_LAUNCH_DRAM_BYTES = 608.8e6
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -143,24 +140,18 @@ class ClockSampler:
             self.lines.append((time.perf_counter(), line.strip()))
 
     def mark(self, t0: float, t1: float):
-        """The timed region, in time.perf_counter() seconds: only samples that
-        arrive inside it (plus one sampling interval) are reported."""
+        """The main timed region, in time.perf_counter() seconds: only samples
+        that arrive inside it (plus one sampling interval) are reported by
+        stop()."""
         self.window = (t0, t1 + 0.06)
 
-    def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.t:
-            self.t.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+    def summary(self, t0: float, t1: float) -> dict:
+        """Median SM clock, max clock and throttle reasons of the samples that
+        arrived inside [t0, t1] (plus one sampling interval)."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.lines:
-            if self.window is not None and not (self.window[0] <= t <= self.window[1]):
+        sm, smax, reasons = [], [], set()
+        for t, ln in list(self.lines):
+            if not (t0 <= t <= t1 + 0.06):
                 continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
@@ -176,6 +167,66 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        if self.window is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return self.summary(*self.window)
+
+
+# ----------------------------------------------------------------------------- ncu traffic
+
+KERNEL_SOURCES = {"attn_fwd_tc_kernel": "attn_fwd_tc.cu", "attn_bwd_dkdv_tc_kernel": "attn_bwd_tc.cu",
+                  "attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu", "lse_merge_kernel": "merge.cu",
+                  "permute_vec_kernel": "permute.cu"}
+
+
+def source_sha(kernel: str) -> str:
+    """First 12 hex digits of the sha256 of the kernel's source file and of
+    the headers every kernel includes (a profile taken on other sources is
+    stale)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "variable_length_sequence_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES[kernel], "tc_ptx.cuh", "nsp_internal.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic() -> dict:
+    """DRAM bytes per launch from the committed ncu summaries: every line
+    'traffic: KERNEL WORKLOAD BYTES SHA' in profiles/*.md.  Kept only when SHA
+    is the current source_sha(KERNEL): counters of an older kernel are not
+    reported."""
+    out = {}
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return out
+    for f in sorted(os.listdir(d)):
+        if not f.endswith(".md"):
+            continue
+        with open(os.path.join(d, f)) as fh:
+            for ln in fh:
+                ln = ln.strip().strip("`")
+                if not ln.startswith("traffic:"):
+                    continue
+                parts = ln.split()
+                if len(parts) != 5 or parts[1] not in KERNEL_SOURCES:
+                    continue
+                kern, wl, nbytes, sha = parts[1], parts[2], float(parts[3]), parts[4]
+                if sha == source_sha(kern):
+                    out[(kern, wl)] = nbytes
+    return out
 
 
 # ----------------------------------------------------------------------------- workload
@@ -409,6 +460,7 @@ class Problem:
         library kernels one step launches."""
         self.graphs = {}
         n0 = self.nsp.nsp_kernel_launches()
+        tc0, cc0 = self.nsp.nsp_path_launches(True), self.nsp.nsp_path_launches(False)
         side = torch.cuda.Stream(stream.device)
         side.wait_stream(stream)
         for leg in legs or self.LEGS:
@@ -419,10 +471,144 @@ class Problem:
         stream.wait_stream(side)
         torch.cuda.synchronize()
         self.launches_per_step = self.nsp.nsp_kernel_launches() - n0
+        # attention kernels of one step on each path: a CUDA-core launch here
+        # would mean the tensor-core path was not taken
+        self.path_per_step = {"tensor_core": self.nsp.nsp_path_launches(True) - tc0,
+                              "cuda_core": self.nsp.nsp_path_launches(False) - cc0}
         return self.launches_per_step
 
 
 # ----------------------------------------------------------------------------- our arm
+
+def time_steps(prob, stream, flush, K: int, warmup: int, settle: int = 2):
+    """W warm-up steps, capture of each leg as a CUDA graph, `settle` replays,
+    then K timed steps, each preceded by an L2 flush outside its timed
+    region, with CUDA events on the launching stream around the step and
+    around each leg.  Returns (step_ms [K], leg_ms [K, legs], launches per
+    step, (t0, t1) of the timed region in time.perf_counter() seconds)."""
+    for _ in range(warmup):
+        flush.zero_()
+        prob.step(stream)
+    torch.cuda.synchronize()
+    launches_per_step = prob.capture(stream)  # legs replayed as CUDA graphs from here on
+    for _ in range(settle):
+        flush.zero_()
+        prob.step(stream)
+    torch.cuda.synchronize()
+    nlegs = len(prob.LEGS)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    leg_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nlegs)] for _ in range(K)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()                       # L2 flush, outside the timed region
+        step_ev[i][0].record(stream)
+        prob.step(stream, leg_ev[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    step_ms = [x.elapsed_time(y) for x, y in step_ev]
+    leg_ms = np.array([[x.elapsed_time(y) for x, y in legs] for legs in leg_ev])
+    return step_ms, leg_ms, launches_per_step, (t0, t1)
+
+
+def leg_records(prob, legs: dict, peaks: dict) -> dict:
+    """Time, achieved rate and fraction of the measured peak of each leg."""
+    out = {}
+    for k, flop in (("fwd", prob.fwd_flop), ("bwd", prob.bwd_flop),
+                    ("ring_partials", prob.ring_flop)):
+        if k in legs:
+            out[k] = {"ms": legs[k], "tflops": flop / legs[k] / 1e9}
+            out[k]["frac_bf16"] = out[k]["tflops"] / peaks["bf16_tflops"]
+    if "ring_partials" in legs:
+        out["ring_partials"]["pairs"] = len(prob.ring_pairs)
+    for k, nbytes in (("merge", prob.merge_bytes), ("permute", prob.permute_bytes)):
+        if k in legs:
+            out[k] = {"ms": legs[k], "gbs": nbytes / legs[k] / 1e6,
+                      "frac_hbm": nbytes / legs[k] / 1e6 / peaks["hbm_gbs"]}
+    if "fwd" in legs and "bwd" in legs:
+        fb = (prob.fwd_flop + prob.bwd_flop) / (legs["fwd"] + legs["bwd"]) / 1e9
+        out["fwd+bwd"] = {"ms": legs["fwd"] + legs["bwd"], "tflops": fb,
+                          "frac_bf16": fb / peaks["bf16_tflops"]}
+    return out
+
+
+def roof_entry(kernel, cid, leg, bound, achieved, peak, unit, work, work_unit, launches,
+               traffic_map, peak_kind="burst"):
+    wl = CONFIGS[cid].name
+    tr = traffic_map.get((kernel, wl))
+    return {"kernel": kernel, "workload": wl, "leg": leg, "bound": bound,
+            "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_kind": peak_kind, "algorithmic_per_launch": work / max(1, launches),
+            "algorithmic_unit": work_unit, "launches_per_step": launches,
+            "traffic": tr, "traffic_unit": "DRAM bytes per launch (ncu)" if tr else None}
+
+
+def sub_config(nsp, cid, device, stream, flush, peaks, clocks, K, warmup, traffic_map):
+    """One other config's legs, timed like the step (own clocks); inputs drawn
+    on the device (seeded) to keep the default run short."""
+    from variable_length_sequence_gb300.workloads import make_workload_device
+    w = make_workload_device(cid, device)
+    prob = Problem(nsp, w, device, CONFIG_LEGS[cid])
+    step_ms, leg_ms, lps, (t0, t1) = time_steps(prob, stream, flush, K, warmup, settle=1)
+    legs = dict(zip(prob.LEGS, leg_ms.mean(0).tolist()))
+    rec = {"workload": CONFIGS[cid].name, "tokens": prob.T, "docs": len(w.lengths),
+           "steps": K, "warmup": warmup, "ms_per_step": float(np.mean(step_ms)),
+           "legs": leg_records(prob, legs, peaks), "clocks": clocks.summary(t0, t1),
+           "gpu_launches_per_step": lps,
+           "attention_launches_per_step": prob.path_per_step,
+           "data": "synthetic (seeded lengths; Q/K/V/dOut N(0,1) drawn on the GPU, bf16)"}
+    roofs = []
+    if "fwd" in legs:
+        roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "fwd", "tensor",
+                                rec["legs"]["fwd"]["tflops"], peaks["bf16_tflops"], "TFLOP/s",
+                                prob.fwd_flop, "FLOP", 1, traffic_map))
+    if "bwd" in legs:
+        roofs.append(roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd",
+                                "tensor", rec["legs"]["bwd"]["tflops"], peaks["bf16_tflops"],
+                                "TFLOP/s", prob.bwd_flop, "FLOP", 1, traffic_map))
+    if "ring_partials" in legs:
+        roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "ring_partials", "tensor",
+                                rec["legs"]["ring_partials"]["tflops"], peaks["bf16_tflops"],
+                                "TFLOP/s", prob.ring_flop, "FLOP", len(prob.ring_pairs),
+                                traffic_map))
+    for k, kern in (("merge", "lse_merge_kernel"), ("permute", "permute_vec_kernel")):
+        if k in legs:
+            nb = prob.merge_bytes if k == "merge" else prob.permute_bytes
+            roofs.append(roof_entry(kern, cid, k, "hbm", rec["legs"][k]["gbs"], peaks["hbm_gbs"],
+                                    "GB/s", nb, "bytes", 1 if k == "merge" else 2, traffic_map))
+    if cid == 5:
+        # short documents are HBM-bound by their arithmetic intensity: the
+        # compulsory bytes of each call against the copy rate
+        cost = nsp.nsp_attn_cost(w.cu_seqlens, prob.Hq, prob.Hkv, prob.d)
+        for k, nb in (("fwd", cost["fwd_bytes"]), ("bwd", cost["bwd_bytes"])):
+            gbs = nb / legs[k] / 1e6
+            rec["legs"][k]["compulsory_gb"] = nb / 1e9
+            rec["legs"][k]["gbs_compulsory"] = gbs
+            rec["legs"][k]["frac_hbm"] = gbs / peaks["hbm_gbs"]
+        roofs = [roof_entry("attn_fwd_tc_kernel", cid, "fwd", "hbm",
+                            rec["legs"]["fwd"]["gbs_compulsory"], peaks["hbm_gbs"], "GB/s",
+                            cost["fwd_bytes"], "compulsory bytes", 1, traffic_map),
+                 roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd", "hbm",
+                            rec["legs"]["bwd"]["gbs_compulsory"], peaks["hbm_gbs"], "GB/s",
+                            cost["bwd_bytes"], "compulsory bytes", 1, traffic_map)]
+    if cid == 3 and not getattr(sub_config, "skip_extra", False):
+        reps = 5
+        ta = time.perf_counter()
+        ms = _time_leg(prob.ring_accumulate, stream, flush, reps)
+        tb = time.perf_counter()
+        tf = prob.ring_flop / ms / 1e9
+        rec["legs"]["ring_accumulate"] = {"ms": ms, "tflops": tf,
+                                          "frac_bf16": tf / peaks["bf16_tflops"],
+                                          "blocks": len(prob.ring_pairs),
+                                          "clocks": clocks.summary(ta, tb)}
+    launches = lps * K
+    del prob, w
+    torch.cuda.empty_cache()
+    return rec, roofs, launches
+
 
 def run_ours(args, world, rank, local):
     from variable_length_sequence_gb300 import build as nsp_build
@@ -441,46 +627,21 @@ def run_ours(args, world, rank, local):
     prob = Problem(nsp, w, device, CONFIG_LEGS[cid])
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    nlegs = len(prob.LEGS)
 
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
     clocks.start()                          # nvidia-smi takes a while to start sampling
-    for _ in range(args.warmup):
-        flush.zero_()
-        prob.step(stream)
-    torch.cuda.synchronize()
-    launches_per_step = prob.capture(stream)  # legs replayed as CUDA graphs from here on
-    for _ in range(2):
-        flush.zero_()
-        prob.step(stream)
-    torch.cuda.synchronize()
-
     K = args.steps
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    leg_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(nlegs)] for _ in range(K)]
     barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush.zero_()                       # L2 flush, outside the timed region
-        step_ev[i][0].record(stream)
-        prob.step(stream, leg_ev[i])
-        step_ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms, leg_ms, launches_per_step, (wall0, wall1) = time_steps(prob, stream, flush, K,
+                                                                    args.warmup)
     barrier(world)
-    wall1 = time.perf_counter()
     wall = wall1 - wall0
     clocks.mark(wall0, wall1)
-    clk = clocks.stop()
     # graph replays do not pass through the library's host launch counter:
     # the kernels of one step were counted while the graphs were recorded
     launches = launches_per_step * K
 
-    step_ms = [s.elapsed_time(e) for s, e in step_ev]
-    leg_ms = np.array([[s.elapsed_time(e) for s, e in legs] for legs in leg_ev])  # [K, nlegs]
     total_ms = reduce_max(sum(step_ms), world, device)
     ms_per_step = total_ms / K
     useful = prob.fwd_flop + prob.bwd_flop + prob.ring_flop
@@ -488,42 +649,48 @@ def run_ours(args, world, rank, local):
 
     peaks = measured_peaks()
     legs = dict(zip(prob.LEGS, leg_ms.mean(0).tolist()))
-    leg_stats = {}
-    for k, flop in (("fwd", prob.fwd_flop), ("bwd", prob.bwd_flop),
-                    ("ring_partials", prob.ring_flop)):
-        if k in legs:
-            leg_stats[k] = {"ms": legs[k], "tflops": flop / legs[k] / 1e9}
-            leg_stats[k]["frac_bf16"] = leg_stats[k]["tflops"] / peaks["bf16_tflops"]
-    if "ring_partials" in legs:
-        leg_stats["ring_partials"]["pairs"] = len(prob.ring_pairs)
-    for k, nbytes in (("merge", prob.merge_bytes), ("permute", prob.permute_bytes)):
-        if k in legs:
-            leg_stats[k] = {"ms": legs[k], "gbs": nbytes / legs[k] / 1e6,
-                            "frac_hbm": nbytes / legs[k] / 1e6 / peaks["hbm_gbs"]}
-    if "fwd" in legs and "bwd" in legs:
-        fb = (prob.fwd_flop + prob.bwd_flop) / (legs["fwd"] + legs["bwd"]) / 1e9
-        leg_stats["fwd+bwd"] = {"ms": legs["fwd"] + legs["bwd"], "tflops": fb,
-                                "frac_bf16": fb / peaks["bf16_tflops"]}
-    # Roofline of the kernel with the largest share of the step's GPU time
-    # (an ncu launch list of this step: the attention forward kernel, main
-    # forward plus ring partials), on its main-forward launch: useful FLOP of
-    # that launch / its duration, timed with CUDA events on the launching
-    # stream (the duration includes the small tile-schedule kernel of the call).
-    main_fwd = "fwd" in legs
-    ach = leg_stats["fwd" if main_fwd else "ring_partials"]["tflops"]
-    roof = {"bound": "tensor",
-            "kernel": "attn_fwd_tc_kernel (" + ("main forward launch" if main_fwd
-                                                else "ring partial launches") + ")",
-            "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": ach / peaks["bf16_tflops"],
-            # DRAM bytes (read + write) of this launch from one ncu capture of
-            # the bench workload (dram__bytes_read.sum + dram__bytes_write.sum);
-            # compulsory bytes (Q, K, V, out, lse) are 607 MB.
-            "traffic": FWD_LAUNCH_DRAM_BYTES if cid == CONFIG_ID else None,
-            "traffic_unit": "bytes per launch",
-            "algorithmic_flop": prob.fwd_flop if main_fwd else prob.ring_flop}
-    roof["peak_source"] = peaks["source"] + " (burst)"
+    leg_stats = leg_records(prob, legs, peaks)
+    traffic_map = profiled_traffic()
 
+    # Roofline of the kernel with the largest share of the step's GPU time
+    # (ncu launch list of this step: attn_fwd_tc_kernel, the main forward plus
+    # the ring partials): useful FLOP of all its launches in a step / their
+    # CUDA-event time on the launching stream (each call's time includes its
+    # small tile-schedule kernel).  Every other kernel follows in "kernels".
+    roofs = []
+    if "fwd" in legs and "ring_partials" in legs:
+        ach = (prob.fwd_flop + prob.ring_flop) / (legs["fwd"] + legs["ring_partials"]) / 1e9
+        roof = roof_entry("attn_fwd_tc_kernel", cid, "fwd + ring_partials", "tensor", ach,
+                          peaks["bf16_tflops"], "TFLOP/s", prob.fwd_flop + prob.ring_flop, "FLOP",
+                          1 + len(prob.ring_pairs), traffic_map)
+        roof["traffic"] = None       # per-launch DRAM bytes differ between main and ring launches
+        roof["traffic_unit"] = None
+    else:
+        k0 = "fwd" if "fwd" in legs else "ring_partials"
+        roof = roof_entry("attn_fwd_tc_kernel", cid, k0, "tensor", leg_stats[k0]["tflops"],
+                          peaks["bf16_tflops"], "TFLOP/s",
+                          prob.fwd_flop if k0 == "fwd" else prob.ring_flop, "FLOP", 1, traffic_map)
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    if "fwd" in legs:
+        roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "fwd", "tensor",
+                                leg_stats["fwd"]["tflops"], peaks["bf16_tflops"], "TFLOP/s",
+                                prob.fwd_flop, "FLOP", 1, traffic_map))
+    if "ring_partials" in legs:
+        roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "ring_partials", "tensor",
+                                leg_stats["ring_partials"]["tflops"], peaks["bf16_tflops"],
+                                "TFLOP/s", prob.ring_flop, "FLOP", len(prob.ring_pairs),
+                                traffic_map))
+    if "bwd" in legs:
+        roofs.append(roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd",
+                                "tensor", leg_stats["bwd"]["tflops"], peaks["bf16_tflops"],
+                                "TFLOP/s", prob.bwd_flop, "FLOP", 1, traffic_map))
+    for k, kern in (("merge", "lse_merge_kernel"), ("permute", "permute_vec_kernel")):
+        if k in legs:
+            nb = prob.merge_bytes if k == "merge" else prob.permute_bytes
+            roofs.append(roof_entry(kern, cid, k, "hbm", leg_stats[k]["gbs"], peaks["hbm_gbs"],
+                                    "GB/s", nb, "bytes", 1 if k == "merge" else 2, traffic_map))
+
+    prob_path = prob.path_per_step
     e2e = None
     if "bwd" in legs and not args.no_e2e:
         e2e = run_e2e(args, prob, nsp, w, device, stream, world)
@@ -533,27 +700,59 @@ def run_ours(args, world, rank, local):
         extra = time_extra_legs(prob, stream, flush, K, peaks)
         extra["ring_accumulate"]["partials_plus_merge_ms"] = legs["ring_partials"] + legs["merge"]
 
+    # the other configs' legs (rank 0's GPU; replicas only), each with its clocks
+    configs = {}
+    if cid == CONFIG_ID and not args.no_configs:
+        del prob
+        torch.cuda.empty_cache()
+        for c, k_sub in ((3, 30), (4, 3), (5, 200)):
+            rec, rr, n = sub_config(nsp, c, device, stream, flush, peaks, clocks, k_sub, 3,
+                                    traffic_map)
+            configs[str(c)] = rec
+            roofs.extend(rr)
+    targets = None
+    if configs:
+        fb = {"2": leg_stats["fwd+bwd"]["frac_bf16"]}
+        fb.update({c: configs[c]["legs"]["fwd+bwd"]["frac_bf16"] for c in ("4", "5")})
+        targets = {
+            "attention fwd+bwd frac_bf16 (target >= 0.55 on configs 2-4)": fb,
+            "config 3 ring forward frac_bf16 (it defines no backward)": {
+                k: configs["3"]["legs"][k]["frac_bf16"]
+                for k in ("ring_partials", "ring_accumulate") if k in configs["3"]["legs"]},
+            "merge frac_hbm (target >= 0.75)": {"2": leg_stats["merge"]["frac_hbm"],
+                                                "3": configs["3"]["legs"]["merge"]["frac_hbm"]},
+            "permute frac_hbm (target >= 0.75)": {
+                "2": leg_stats["permute"]["frac_hbm"],
+                "3": configs["3"]["legs"]["permute"]["frac_hbm"]},
+            "config 5 compulsory-bytes frac_hbm (HBM-bound; no target)": {
+                k: configs["5"]["legs"][k]["frac_hbm"] for k in ("fwd", "bwd")}}
+    clk = clocks.stop()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and cid == CONFIG_ID:
         cpu = cpu_baseline(w, args.cpu_seconds)
 
     if rank == 0:
+        roof["kernels"] = roofs
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded; lengths, Q/K/V/dOut N(0,1) rounded to bf16)",
-            "config": {"workload": CONFIGS[cid].name, "tokens": prob.T,
-                       "docs": len(w.lengths), "heads_q": prob.Hq, "heads_kv": prob.Hkv,
-                       "head_dim": prob.d, "causal": True, "ring_shards": RING_SHARDS,
-                       "permute_groups": PERMUTE_GROUPS,
-                       "step": " + ".join(prob.LEGS),
+            "config": {"workload": CONFIGS[cid].name, "tokens": int(w.T),
+                       "docs": len(w.lengths), "heads_q": CONFIGS[cid].Hq,
+                       "heads_kv": CONFIGS[cid].Hkv, "head_dim": CONFIGS[cid].d, "causal": True,
+                       "ring_shards": RING_SHARDS, "permute_groups": PERMUTE_GROUPS,
+                       "step": " + ".join(CONFIG_LEGS[cid]),
                        "l2": "flushed (256 MiB write) before every timed step",
                        "parallelism": f"replicas x{world}"},
             "useful_flop_per_step": useful,
             "legs": leg_stats,
             "extra_legs": extra,
+            "configs": configs or None,
+            "targets": targets,
             "roofline": roof,
+            "attention_launches_per_step": prob_path,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": int(launches),
@@ -759,6 +958,8 @@ def main():
                     help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the legs timed outside the step (ring accumulate / backward)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the sub-records of configs 3, 4 and 5")
     ap.add_argument("--config", type=int, choices=sorted(CONFIG_LEGS), default=CONFIG_ID,
                     help="workload (default: config 2, the bench workload)")
     args = ap.parse_args()

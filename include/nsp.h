@@ -81,6 +81,31 @@ const char* nsp_version(void);
  * benchmarks count the library's own launches. */
 int64_t nsp_kernel_launches(void);
 
+/* Number of attention kernels (forward, dK/dV and dQ kernels) this library
+ * has launched in this process on the tensor-core path (tensor_core = 1:
+ * tcgen05, TMEM, TMA) or on the CUDA-core path (tensor_core = 0: float32
+ * I/O, d = 64, odd head groupings, or no tensor-map support in the driver).
+ * Lets a caller see which path its calls took. */
+int64_t nsp_path_launches(int32_t tensor_core);
+
+/* Bound, in GPU clock cycles, of every wait inside the tensor-core attention
+ * kernels (a thread waiting for a copy, a product or another role of its
+ * block).  When a wait runs longer, the kernel records NSP_ERR_TIMEOUT in the
+ * workspace status word (read it with nsp_status_query), every role of the
+ * block stops, waits for the copies and products it already issued, frees its
+ * tensor memory and returns: the context stays usable and the next call on
+ * the same workspace starts afresh.  The outputs of the failed call are
+ * unspecified.
+ *
+ * It makes the kernels' failure detection testable: the default (cycles < 0
+ * restores it) is 4e9 cycles, about 2 s,
+ * far beyond any legitimate wait; a tiny bound (0 to a few hundred cycles)
+ * makes a call's first wait that is not already satisfied expire.
+ * Process-wide; applies to calls issued after it returns (not to calls
+ * already enqueued).  Returns the previous bound.  No counterpart on the
+ * pages, which describe no device-side failure handling. */
+int64_t nsp_set_wait_timeout_cycles(int64_t cycles);
+
 /* ------------------------------------------------------------------------
  * Varlen attention forward  ([BASP] Sec. II-A; [HSAP] Sec. 2.1, 2.2.1).
  *
@@ -370,6 +395,29 @@ int32_t nsp_seq2head_permute(const void* in, void* out, int64_t T, int32_t H, in
 
 int32_t nsp_seq2head_permute_validate(const void* in, const void* out, int64_t T, int32_t H,
                                       int32_t d, int32_t P, int32_t elem_bytes);
+
+/* ------------------------------------------------------------------------
+ * Batch-aware subgroup all-to-all layout ([BASP] Sec. IV, "Batch-aware
+ * group formation", "Batch Aware Sequence Partitioning" (Alg. 2),
+ * "Subgroup all-to-all"): a micro-batch of B sequences of L tokens on
+ * N = B K ranks, where each sequence is sharded over its own group of K ranks
+ * and each group runs an independent K-way all-to-all.  With the batch
+ * stacked on one device, the receive side of all B groups:
+ *   inverse = 0:  out[b][g][t][j][:] = in[b L + t][g H/K + j][:]
+ *   inverse = 1:  in[b L + t][g H/K + j][:] = out[b][g][t][j][:] (roles of
+ *                 the buffers swapped: `in` is [B][K][L][H/K][d])
+ *   in:  device [B L][H][d] elements of elem_bytes (1, 2, 4 or 8 bytes);
+ *   out: device [B][K][L][H/K][d].
+ * Each group's block is the nsp_seq2head_permute of its own sequence with
+ * P = K (B = 1 is exactly that call); no data crosses sequences.  Bit-exact
+ * data movement, one launch for all B groups.  Errors as
+ * nsp_seq2head_permute on the whole [B L, H, d] batch (K must divide H;
+ * in, out 16-byte aligned, not overlapping); B < 1 or L < 0 is
+ * NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int32_t nsp_seq2head_permute_groups(const void* in, void* out, int32_t B, int64_t L, int32_t H,
+                                    int32_t d, int32_t K, int32_t elem_bytes, int32_t inverse,
+                                    nsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Status word of the last call that used `workspace`.  Synchronises `stream`

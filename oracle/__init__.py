@@ -37,9 +37,10 @@ differences; none is "parity unpinned".
 from .attention import (allowed_interval, attn_fwd, attn_fwd_rows, attn_probs,
                         attn_bwd, attn_bwd_block, attn_bwd_dq_rows, attn_bwd_dkv_rows)
 from .merge import lse_merge
-from .permute import seq2head, head2seq
+from .permute import seq2head, head2seq, seq2head_groups, head2seq_groups
 
 __all__ = [
     "allowed_interval", "attn_fwd", "attn_fwd_rows", "attn_probs", "attn_bwd", "attn_bwd_block",
     "attn_bwd_dq_rows", "attn_bwd_dkv_rows", "lse_merge", "seq2head", "head2seq",
+    "seq2head_groups", "head2seq_groups",
 ]

@@ -425,4 +425,28 @@ def pin_permutation(att, mrg, prm):
     np.testing.assert_array_equal(prm.seq2head(x, 8)[:, :, 0], x.transpose(1, 0, 2))
 
 
+def pin_permutation_groups(att, mrg, prm):
+    """BASP subgroup all-to-all: B = 1 is the plain permutation with P = K;
+    round trip; hand-checked positions; each group's output is made of its
+    own sequence's rows only (changing another sequence leaves it alone)."""
+    L, H, d = 5, 6, 2
+    x = np.arange(3 * L * H * d).reshape(3 * L, H, d)
+    np.testing.assert_array_equal(prm.seq2head_groups(x[:L], 1, 3)[0], prm.seq2head(x[:L], 3))
+    for B, K in ((1, 2), (3, 1), (3, 2), (3, 3), (3, 6)):
+        y = prm.seq2head_groups(x, B, K)
+        assert y.shape == (B, K, 3 * L // B, H // K, d)
+        np.testing.assert_array_equal(prm.head2seq_groups(y, B, K), x)
+    y = prm.seq2head_groups(x, 3, 2)     # h = 3
+    # token 4 of sequence 2 is row 14; its head 4 is group 1, local head 1
+    np.testing.assert_array_equal(y[2, 1, 4, 1], x[14, 4])
+    np.testing.assert_array_equal(y[1, 0, 0, 2], x[5, 2])
+    np.testing.assert_array_equal(y[0, 1, 3, 0], x[3, 3])
+    x2 = x.copy()
+    x2[L:2 * L] += 1000                  # sequence 1 only
+    y2 = prm.seq2head_groups(x2, 3, 2)
+    np.testing.assert_array_equal(y2[0], y[0])
+    np.testing.assert_array_equal(y2[2], y[2])
+    assert (y2[1] != y[1]).all()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

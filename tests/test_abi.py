@@ -134,6 +134,36 @@ def test_accumulate_rejects_on_host(lib):
     assert call(A + (1 << 16), acc=A + 16388) == nsp.NSP_ERR_ALIGN
 
 
+def test_noalloc_rejects_on_host_like_fwd(lib):
+    """nsp_attn_fwd_noalloc returns the same codes as nsp_attn_fwd for
+    out-of-range sizes and scales (all refused before any CUDA call), and
+    NSP_ERR_WORKSPACE for problems whose scheduler state exceeds its static
+    scratch."""
+    def noalloc(q_len, scale=0.088):
+        return lib.nsp_attn_fwd_noalloc(A, A, A, A, 1, 0, q_len, 0, q_len, 8, 2, 128, scale, 1,
+                                        nsp.NSP_BF16, A, nsp.NSP_BF16, None, None, None)
+
+    def fwd(q_len):
+        return lib.nsp_attn_fwd(A, A, A, A, 1, 0, q_len, 0, q_len, 8, 2, 128, 0.088, 1,
+                                nsp.NSP_BF16, A, nsp.NSP_BF16, None, A, 1 << 40, None)
+    for q_len in (1 << 31, (1 << 62) + 5):
+        assert noalloc(q_len) == fwd(q_len) == nsp.NSP_ERR_UNSUPPORTED
+    assert noalloc(-1) == fwd(-1) == nsp.NSP_ERR_INVALID
+    assert noalloc(1 << 24) == nsp.NSP_ERR_WORKSPACE          # 16M tokens: beyond 1 MiB
+    assert noalloc(1000, scale=0.0) == nsp.NSP_ERR_INVALID
+
+
+def test_wait_timeout_setter(lib):
+    """The bound of device waits: a process-wide setting, default restored by
+    a negative value; each call returns the previous bound."""
+    prev = nsp.nsp_set_wait_timeout_cycles(777)
+    try:
+        assert nsp.nsp_set_wait_timeout_cycles(-5) == 777
+        assert nsp.nsp_set_wait_timeout_cycles(prev) == 4000000000
+    finally:
+        nsp.nsp_set_wait_timeout_cycles(prev)
+
+
 def _brute_cost(cu, qa, qb, ka, kb, causal):
     """Allowed pairs and 128 x 128 tiles holding one, by enumeration."""
     cu = np.asarray(cu, np.int64)

@@ -1,14 +1,19 @@
 """Varlen attention backward on the GPU against the fp64 oracle's analytic
 gradients: every element on small inputs and on config 5, sampled dQ rows
 and dK/dV key rows (all heads) on configs 2 and 4.  Relative L2 per tensor
-<= 1e-2."""
+<= 1e-2; on config 5, also every (row, head) within the internal per-row
+bar.  The sampled key rows include keys deep inside the longest documents,
+whose key-stationary work items accumulate over many query tiles and heads:
+the first keys of config 2's longest document (seen by all of its queries)
+and, on config 4, keys about 2560 queries before the end of the
+262144-token document."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_common import (TOL_GRAD, f64, oracle_inputs, rel_l2, sample_rows, timed, to_dev,
-                        workload)
+from gpu_common import (TOL_GRAD, assert_rows_close, f64, oracle_inputs, rel_l2, sample_rows,
+                        timed, to_dev, workload)
 from variable_length_sequence_gb300.workloads import make_custom
 
 pytestmark = pytest.mark.gpu
@@ -59,9 +64,24 @@ def test_config5_whole(nsp):
                        128 ** -0.5, True)
     for n, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         _check(f"C5 {n}", f64(g), r)
+        assert_rows_close(f64(g), r, label=f"C5 {n} per row")
 
 
-def _sampled(nsp, cid, n_rows, n_keys):
+def deep_keys(cu, depth: int, seed: int, n_random: int = 8) -> list:
+    """Keys of the longest document whose visible queries reach `depth` rows
+    deep: the 4 keys `depth` rows before the document's end and seeded keys
+    between there and the end (a depth of the whole document gives its first
+    keys, seen by every query of it)."""
+    lens = np.diff(cu)
+    b = int(np.argmax(lens))
+    start = int(cu[b + 1]) - min(depth, int(lens[b]))
+    keys = set(range(start, start + 4))
+    rng = np.random.default_rng(seed)
+    keys.update(int(x) for x in rng.integers(start, int(cu[b + 1]), n_random))
+    return sorted(keys)
+
+
+def _sampled(nsp, cid, n_rows, n_keys, depth):
     w = workload(cid)
     dq, dk, dv = run_fwd_bwd(nsp, w)
     q, k, v, do = oracle_inputs(w)
@@ -81,6 +101,10 @@ def _sampled(nsp, cid, n_rows, n_keys):
     r = np.random.default_rng(20 + cid)
     for b in r.choice(short, min(len(short), n_keys), replace=False):
         keys.add(int(r.integers(cu[b], cu[b + 1])))
+    deep = deep_keys(cu, depth, seed=30 + cid)
+    print(f"[C{cid}] deep keys {deep[:4]}.. (up to {depth} queries of the longest document "
+          f"see them)")
+    keys.update(deep)
     keys = np.array(sorted(keys))
     kidx = torch.from_numpy(keys).cuda()
     for g in range(w.cfg.Hkv):
@@ -91,9 +115,10 @@ def _sampled(nsp, cid, n_rows, n_keys):
 
 
 def test_config2_sampled(nsp):
-    _sampled(nsp, 2, 512, 24)
+    # depth = whole document: its first keys, seen by all of its queries
+    _sampled(nsp, 2, 512, 24, depth=1 << 30)
 
 
 @pytest.mark.slow
 def test_config4_sampled(nsp):
-    _sampled(nsp, 4, 128, 16)
+    _sampled(nsp, 4, 128, 16, depth=2560)

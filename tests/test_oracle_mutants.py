@@ -50,6 +50,10 @@ MUTANTS = [
     ("merge.py", "m_safe + np.log(", "np.log(", "max not added back into merged lse"),
     ("permute.py", "out[g, t, j, :] = x[t, g * h + j, :]", "out[g, t, j, :] = x[t, j * P + g, :]",
      "strided head groups"),
+    ("permute.py", "out[b, g, t, j, :] = x[b * L + t, g * h + j, :]",
+     "out[b, g, t, j, :] = x[g * L + t, b * h + j, :]", "subgroup exchange across sequences"),
+    ("permute.py", "out[b, g, t, j, :] = x[b * L + t, g * h + j, :]",
+     "out[b, g, t, j, :] = x[t * B + b, g * h + j, :]", "sequences interleaved by token"),
 ]
 
 

@@ -5,7 +5,11 @@
   must be bit-identical whatever the number of CTAs.  The grid is shrunk
   through the NSP_PERSISTENT_CTAS environment variable; a race between CTAs
   (a shared buffer, a counter, a schedule read before it is written) shows
-  up as a bit difference.
+  up as a bit difference.  One entry point is grid-dependent by design: the
+  ring-block backward splits its dK/dV items over query-head subsets when
+  the block has few key tiles for the grid, and the subsets add into the
+  float32 accumulators with atomics, so its dk/dv may differ in the last
+  bits between grids; it is compared within the gradient bar instead.
 * Guard zones: every output is a view into a larger buffer whose guard bytes
   before and after hold a pattern; after the calls the guards must be
   unchanged, so no kernel writes past the rows, heads or tiles it owns.
@@ -15,7 +19,7 @@ import os
 import pytest
 import torch
 
-from gpu_common import to_dev
+from gpu_common import f64, rel_l2, to_dev
 from variable_length_sequence_gb300.workloads import make_custom
 
 pytestmark = pytest.mark.gpu
@@ -25,18 +29,37 @@ PATTERN = 0x5A
 
 
 def _run_all(nsp, w, dev):
-    """Forward, backward, a ring partial block and the head-grouped forward."""
+    """Bit-identical across grids: forward, backward, a ring partial block,
+    the ring accumulation in place, the head-grouped forward and the
+    forward without a workspace.  Returned last: the ring-block backward's
+    (dq, dk, dv), grid-dependent in the last bits."""
     sc = w.cfg.d ** -0.5
+    T, Hq, Hkv = w.T, w.cfg.Hq, w.cfg.Hkv
     out, lse = nsp.attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], scale=sc)
     dq, dk, dv = nsp.attn_bwd(dev["q"], dev["k"], dev["v"], out, dev["dout"], lse, dev["cu"],
                               scale=sc)
     qa, ka = 200, 64
     po, pl = nsp.attn_fwd(dev["q"][qa:], dev["k"][ka:], dev["v"][ka:], dev["cu"], scale=sc,
                           out_dtype=torch.float32, q_start=qa, kv_start=ka)
+    acc, lacc = nsp.ring_accumulate_init(T - qa, Hq, w.cfg.d, "cuda")
+    for a, b in ((ka, T), (0, ka)):
+        nsp.attn_fwd_accumulate(dev["q"][qa:], dev["k"][a:b], dev["v"][a:b], dev["cu"], acc, lacc,
+                                scale=sc, q_start=qa, kv_start=a)
     og, lg = nsp.attn_fwd_headgroups(nsp.seq2head(dev["q"], 2), dev["k"], dev["v"], dev["cu"],
                                      scale=sc)
+    on, ln = torch.empty_like(out), torch.empty_like(lse)
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    nsp.nsp_attn_fwd_noalloc(dev["q"], dev["k"], dev["v"], dev["cu"], len(w.lengths), 0, T, 0, T,
+                             Hq, Hkv, w.cfg.d, sc, True, on, ln, st)
+    gq = torch.zeros((T - qa, Hq, w.cfg.d), dtype=torch.float32, device="cuda")
+    gk = torch.zeros((T - ka, Hkv, w.cfg.d), dtype=torch.float32, device="cuda")
+    gv = torch.zeros_like(gk)
+    nsp.attn_bwd_accumulate(dev["q"][qa:], dev["k"][ka:], dev["v"][ka:], out[qa:], dev["dout"][qa:],
+                            lse[:, qa:].contiguous(), dev["cu"], gq, gk, gv, scale=sc,
+                            q_start=qa, kv_start=ka)
     torch.cuda.synchronize()
-    return [out, lse, dq, dk, dv, po, pl, og, lg]
+    assert int(st.item()) == 0
+    return [out, lse, dq, dk, dv, po, pl, acc, lacc, og, lg, on, ln], (gq, gk, gv)
 
 
 @pytest.mark.parametrize("lens", [[100, 1, 300, 60, 250, 0, 517], [33] * 40 + [700]],
@@ -44,14 +67,17 @@ def _run_all(nsp, w, dev):
 def test_results_do_not_depend_on_the_grid(nsp, lens):
     w = make_custom(lens, 8, 2, 128, seed=70)
     dev = to_dev(w)
-    ref = _run_all(nsp, w, dev)
+    ref, ref_ring = _run_all(nsp, w, dev)
     old = os.environ.get("NSP_PERSISTENT_CTAS")
     try:
         for ctas in ("1", "7", "64"):
             os.environ["NSP_PERSISTENT_CTAS"] = ctas
-            got = _run_all(nsp, w, dev)
+            got, got_ring = _run_all(nsp, w, dev)
             for i, (a, b) in enumerate(zip(ref, got)):
                 assert torch.equal(a, b), f"output {i} differs with {ctas} CTAs"
+            for name, a, b in zip(("dq", "dk", "dv"), ref_ring, got_ring):
+                e = rel_l2(f64(b), f64(a))
+                assert e <= 1e-5, f"ring-block {name} differs by {e} with {ctas} CTAs"
     finally:
         if old is None:
             os.environ.pop("NSP_PERSISTENT_CTAS", None)

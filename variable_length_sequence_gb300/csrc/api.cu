@@ -15,6 +15,17 @@ std::atomic<long long> g_kernel_launches{0};
 
 void count_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
 
+std::atomic<long long> g_path_launches[2] = {{0}, {0}};
+
+void count_path(bool tensor_core) {
+  g_path_launches[tensor_core ? 1 : 0].fetch_add(1, std::memory_order_relaxed);
+}
+
+constexpr long long kDefaultWaitBudget = 4000000000LL;     // about 2 s at 2 GHz
+std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+
+int64_t wait_budget_cycles() { return g_wait_budget.load(std::memory_order_relaxed); }
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -30,8 +41,12 @@ int num_sms() {
 // CTAs of the persistent attention kernels: one per SM, or the positive
 // integer in the environment variable NSP_PERSISTENT_CTAS (read at every
 // launch, capped at the SM count).  Each work item is computed whole by one
-// CTA, so results do not depend on the grid: tests run several grids and
-// compare bits to expose scheduling races.
+// CTA, so results do not depend on the grid (tests run several grids and
+// compare bits to expose scheduling races), with one exception: the
+// ring-block backward (nsp_attn_bwd_accumulate) splits its dK/dV items over
+// query-head subsets when the block has few key tiles for the grid, and the
+// subsets add into the float32 accumulators with atomics, so its dk/dv may
+// differ in the last bits between grids.
 int persistent_grid() {
   const int n = num_sms();
   const char* e = std::getenv("NSP_PERSISTENT_CTAS");
@@ -53,9 +68,6 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool dtype_ok(int32_t t) { return t == NSP_F32 || t == NSP_BF16; }
 
 constexpr int64_t kMaxTokens = (int64_t)1 << 30;   // keeps tile counts in int32
-
-// The softmax scale must be a positive finite number (a temperature).
-inline bool scale_ok(float scale) { return scale > 0.f && scale <= 3.0e38f; }
 
 int32_t check_common(int32_t ndoc, int32_t Hq, int32_t Hkv, int32_t d, int32_t causal,
                      int32_t io_dtype) {
@@ -87,6 +99,15 @@ const char* nsp_status_str(int32_t status) {
 const char* nsp_version(void) { return "nsp 0.1 sm_103a"; }
 
 int64_t nsp_kernel_launches(void) { return (int64_t)g_kernel_launches.load(); }
+
+int64_t nsp_path_launches(int32_t tensor_core) {
+  return (int64_t)g_path_launches[tensor_core ? 1 : 0].load();
+}
+
+int64_t nsp_set_wait_timeout_cycles(int64_t cycles) {
+  const long long v = cycles < 0 ? kDefaultWaitBudget : (long long)cycles;
+  return (int64_t)g_wait_budget.exchange(v);
+}
 
 size_t nsp_attn_fwd_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t Hkv,
                                    int32_t d) {
@@ -416,6 +437,22 @@ int32_t nsp_seq2head_permute(const void* in, void* out, int64_t T, int32_t H, in
   if (T == 0) return NSP_OK;
   if (launch_permute(in, out, T, H, d, P, elem_bytes, inverse,
                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  return NSP_OK;
+}
+
+int32_t nsp_seq2head_permute_groups(const void* in, void* out, int32_t B, int64_t L, int32_t H,
+                                    int32_t d, int32_t K, int32_t elem_bytes, int32_t inverse,
+                                    nsp_stream_t stream) {
+  if (B < 1 || L < 0) return NSP_ERR_INVALID;
+  if ((int64_t)B * L > ((int64_t)1 << 40)) return NSP_ERR_UNSUPPORTED;
+  // the checks of the whole batch as one [B L, H, d] permutation
+  int32_t st = nsp_seq2head_permute_validate(in, out, (int64_t)B * L, H, d, K, elem_bytes);
+  if (st != NSP_OK) return st;
+  if (inverse != 0 && inverse != 1) return NSP_ERR_INVALID;
+  if (L == 0) return NSP_OK;
+  if (launch_permute_groups(in, out, B, L, H, d, K, elem_bytes, inverse,
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NSP_ERR_CUDA;
   return NSP_OK;
 }

@@ -102,13 +102,6 @@ __device__ __forceinline__ void mma_t_split(uint32_t d_tmem, uint32_t a_tmem, ui
   }
 }
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitTimeoutCycles) return;
-  }
-}
-
 __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
                                                  float scale) {
   uint32_t w[16];
@@ -223,8 +216,9 @@ struct __align__(1024) SmemKV {
   uint64_t dkv_full, dkv_empty;
   uint64_t item_full[2], item_empty[2];
   KvItem items[2];
+  uint64_t drain1, drain2;      // each MMA stream's own barrier for its final drain
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wait;
 };
 static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memory");
 
@@ -266,7 +260,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(&sm.dk_done, 1);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, kKvSoftmaxWarps);
-    sm.abort_flag = 0;
+    mbar_init(&sm.drain1, 1);
+    mbar_init(&sm.drain2, 1);
+    wait_ctl_init(&sm.wait, p.wait_budget);
     fence_mbar_init();
   }
   if (warp == kKvWarpMma1) {
@@ -284,7 +280,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tc_fence_after();
 
   const uint32_t tmem = sm.tmem_base;
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* const wc = &sm.wait;
   const int G = p.Hq / p.Hkv;
   const int64_t n_keys = p.kv_len;           // keys of the range (row index of K, V, dK, dV)
   const int n_per_tile = p.Hkv * a.hsplit;   // items per key tile
@@ -315,7 +311,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           }
           const uint32_t slot = it_count & 1;
           if (it_count >= 2 &&
-              !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
+              !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -324,7 +320,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           ++it_count;
           if (it.steps < 0) break;
           if (it.steps == 0) continue;            // no query of the range sees these keys
-          if (kv_count >= 1 && !mbar_wait(&sm.kv_empty, (kv_count - 1) & 1, abort_flag, hdr)) {
+          if (kv_count >= 1 && !mbar_wait(&sm.kv_empty, (kv_count - 1) & 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -342,7 +338,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const uint32_t fill = q_count >> 1;             // fill index of both slots
             const uint32_t sq = q_count & 3, sd = (q_count + 2) & 3;
             if (q_count >= 2 &&
-                !mbar_wait(&sm.slot_empty[sq], (fill - 1) & 1, abort_flag, hdr)) {
+                !mbar_wait(&sm.slot_empty[sq], (fill - 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
@@ -361,7 +357,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             bulk_load(sm.vec[sq], a.nlse2 + row, 128 * sizeof(float), &sm.slot_full[sq]);
             ++loads;
             if (q_count >= 2 &&
-                !mbar_wait(&sm.slot_empty[sd], (fill - 1) & 1, abort_flag, hdr)) {
+                !mbar_wait(&sm.slot_empty[sd], (fill - 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
@@ -374,8 +370,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             ++q_count;
           }
         }
-        if (!ok) {
-          // abort: every copy issued so far completes on its stage barrier
+        {
+          // leaving, normally or on an abort: every copy issued so far lands on
+          // its stage barrier before the CTA exits
           if (kv_count >= 1) drain_wait(&sm.kv_full, (kv_count - 1) & 1);
           // load l: step l / 2, Q (l even) or dOut (l odd)
           for (uint32_t l = (loads > 4 ? loads - 4 : 0); l < loads; ++l) {
@@ -394,25 +391,25 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         bool ok = true;
         while (ok) {
           const uint32_t slot = it_count & 1;
-          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
           const KvItem it = sm.items[slot];
           mbar_arrive(&sm.item_empty[slot]);
           ++it_count;
           if (it.steps < 0) break;
           if (it.steps == 0) continue;
-          if (!mbar_wait(&sm.kv_full, items_done & 1, abort_flag, hdr)) break;
+          if (!mbar_wait(&sm.kv_full, items_done & 1, wc, hdr)) break;
           for (int n = 0; n < it.steps; ++n) {
             const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
-            if (!mbar_wait(&sm.slot_full[sq], fp, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.slot_full[sq], fp, wc, hdr)) { ok = false; break; }
             // region rb held the previous dP^T: free once the softmax has read it
-            if (qc >= 1 && !mbar_wait(&sm.dp_free, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+            if (qc >= 1 && !mbar_wait(&sm.dp_free, (qc - 1) & 1, wc, hdr)) { ok = false; break; }
             tc_fence_after();
             mma_kk(tmem + 128 * rb, k_s, smem_u32(sm.qd[sq]), false);         // S^T = K Q^T
             mma_commit(&sm.s_full);
             mma_commit(&sm.slot_empty[sq]);
-            if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.slot_full[sd], fp, wc, hdr)) { ok = false; break; }
             // region rb ^ 1 held the previous P^T: free once dV has read it
-            if (qc >= 1 && !mbar_wait(&sm.dv_done[rb ^ 1], ((qc - 1) >> 1) & 1, abort_flag, hdr)) {
+            if (qc >= 1 && !mbar_wait(&sm.dv_done[rb ^ 1], ((qc - 1) >> 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
@@ -426,6 +423,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mma_commit(&sm.kv_empty);
           ++items_done;
         }
+        mma_drain(&sm.drain1);            // every product done before TMEM is freed
       }
     } else if (warp == kKvWarpMma2) {
       // ------------------------------------------------------------ stream 2: dV, dK
@@ -435,7 +433,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         bool ok = true;
         while (ok) {
           const uint32_t slot = it_count & 1;
-          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+          if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
           const KvItem it = sm.items[slot];
           mbar_arrive(&sm.item_empty[slot]);
           ++it_count;
@@ -443,13 +441,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (it.steps == 0) continue;
           for (int n = 0; n < it.steps; ++n) {
             const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
-            if (!mbar_wait(&sm.p_ready[rb], fp, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.p_ready[rb], fp, wc, hdr)) { ok = false; break; }
             if (n == 0 && items_done > 0 &&
-                !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, abort_flag, hdr)) {
+                !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
-            if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.slot_full[sd], fp, wc, hdr)) { ok = false; break; }
             tc_fence_after();
             // a ring block with one item per (key tile, KV head) adds onto the
             // preloaded running dK / dV
@@ -457,7 +455,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
             mma_commit(&sm.dv_done[rb]);
             mma_commit(&sm.slot_empty[sd]);
-            if (!mbar_wait(&sm.ds_ready, qc & 1, abort_flag, hdr)) { ok = false; break; }
+            if (!mbar_wait(&sm.ds_ready, qc & 1, wc, hdr)) { ok = false; break; }
             tc_fence_after();
             {
               // dK += dS^T Q: A = dS^T K-major (rows = keys), B = Q MN-major
@@ -478,6 +476,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mma_commit(&sm.dkv_full);
           ++items_done;
         }
+        mma_drain(&sm.drain2);
       }
     }
   } else {
@@ -504,7 +503,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     bool ok = true;
     while (ok) {
       const uint32_t slot = it_count & 1;
-      if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+      if (!mbar_wait_warp(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
       const KvItem it = sm.items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
@@ -561,8 +560,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
         const uint32_t s_tm = tmem + lane_base + 128 * rb + cg * 32;
         const uint32_t dp_tm = tmem + lane_base + 128 * (rb ^ 1) + cg * 32;
-        if (!mbar_wait(&sm.slot_full[sq], fp, abort_flag, hdr)) { ok = false; break; }
-        if (!mbar_wait(&sm.s_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.slot_full[sq], fp, wc, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full, qc & 1, wc, hdr)) { ok = false; break; }
         tc_fence_after();
         uint32_t x[32];
         tmem_ld16x256_x4(s_tm, x);
@@ -630,8 +629,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           mbar_arrive(&sm.slot_empty[sq]);                  // lse read
         }
         // phase 2: dS = P (dP - delta); masked P is zero, so dS is too
-        if (!mbar_wait(&sm.slot_full[sd], fp, abort_flag, hdr)) { ok = false; break; }
-        if (!mbar_wait(&sm.dp_full, qc & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.slot_full[sd], fp, wc, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.dp_full, qc & 1, wc, hdr)) { ok = false; break; }
         tc_fence_after();
         tmem_ld16x256_x4(dp_tm, x);
         tmem_ld16x256_x4(dp_tm + (16u << 16), x + 16);
@@ -646,7 +645,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.dp_free);
         // the dS^T buffer is free once dK has read the previous one
-        if (qc >= 1 && !mbar_wait(&sm.dk_done, (qc - 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        if (qc >= 1 && !mbar_wait_warp(&sm.dk_done, (qc - 1) & 1, wc, hdr)) { ok = false; break; }
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int j = (k >> 1) & 3;
@@ -670,7 +669,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (!ok) break;
       // item epilogue: warps of column groups 0-1 write dV, 2-3 write dK (64
       // columns each), TMEM lane = key row
-      if (!mbar_wait(&sm.dkv_full, items_done & 1, abort_flag, hdr)) break;
+      if (!mbar_wait_warp(&sm.dkv_full, items_done & 1, wc, hdr)) break;
       tc_fence_after();
       {
         const int64_t key = (int64_t)it.ktile * 128 + r;
@@ -727,18 +726,19 @@ struct __align__(1024) SmemQ {
   uint64_t dp_full, dp_free, o_full, epi_done;
   uint64_t item_full[2], item_empty[2];
   QItem items[2];
+  uint64_t drain1, drain2;      // each MMA stream's own barrier for its final drain
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wait;
 };
 static_assert(sizeof(SmemQ) <= kSmemLimit, "dQ tile set exceeds shared memory");
 
 // dP = dOut V^T for tile jc (any stream): dP region free once the softmax
 // has read the previous dP.
 __device__ __forceinline__ bool issue_dp(SmemQ& sm, uint32_t tmem, uint32_t jc,
-                                         volatile int* abort_flag, WsHeader* hdr) {
+                                         WaitCtl* wc, WsHeader* hdr) {
   const uint32_t vst = jc % V_NS, vuse = jc / V_NS;
-  if (!mbar_wait(&sm.v_full[vst], vuse & 1, abort_flag, hdr)) return false;
-  if (jc >= 1 && !mbar_wait(&sm.dp_free, (jc - 1) & 1, abort_flag, hdr)) return false;
+  if (!mbar_wait(&sm.v_full[vst], vuse & 1, wc, hdr)) return false;
+  if (jc >= 1 && !mbar_wait(&sm.dp_free, (jc - 1) & 1, wc, hdr)) return false;
   tc_fence_after();
   mma_kk(tmem + 256, smem_u32(sm.dout), smem_u32(sm.v[vst]), false);
   mma_commit(&sm.dp_full);
@@ -793,7 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.dp_free, 256);
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.epi_done, 256);
-    sm.abort_flag = 0;
+    mbar_init(&sm.drain1, 1);
+    mbar_init(&sm.drain2, 1);
+    wait_ctl_init(&sm.wait, p.wait_budget);
     fence_mbar_init();
   }
   if (warp == kWarpMma1) {
@@ -811,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   const uint32_t tmem = sm.tmem_base;
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* const wc = &sm.wait;
   const int G = p.Hq / p.Hkv;
   const int64_t T = p.q_len;
   // a ring block's query tiles that see no key add nothing: not work items
@@ -837,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t slot = it_count & 1;
         if (it_count >= 2 &&
-            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
+            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, wc, hdr)) {
           ok = false;
           break;
         }
@@ -848,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it.n_kv < 0) break;
           continue;
         }
-        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, abort_flag, hdr)) {
+        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, wc, hdr)) {
           ok = false;
           break;
         }
@@ -868,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int key0 = (it.j_lo + jj) * 128;
           {
             const uint32_t st = k_count % K_NS, use = k_count / K_NS;
-            if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
@@ -880,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           {
             const uint32_t st = v_count % V_NS, use = v_count / V_NS;
-            if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+            if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, wc, hdr)) {
               ok = false;
               break;
             }
@@ -892,7 +894,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      {
+        // leaving, normally or on an abort: every issued copy lands first
         if (q_count >= 1) drain_wait(&sm.q_full, (q_count - 1) & 1);
         for (uint32_t j = (k_count > K_NS ? k_count - K_NS : 0); j < k_count; ++j)
           drain_wait(&sm.k_full[j % K_NS], (j / K_NS) & 1);
@@ -908,19 +911,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok) {
         const uint32_t slot = it_count & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
         const QItem it = sm.items[slot];
         mbar_arrive(&sm.item_empty[slot]);
         ++it_count;
         if (it.n_kv < 0) break;
         if (it.n_kv == 0) continue;
-        if (!mbar_wait(&sm.q_full, q_count & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.q_full, q_count & 1, wc, hdr)) break;
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = jc % K_NS, use = jc / K_NS, b = jc & 1;
-          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+          if (!mbar_wait(&sm.k_full[st], use & 1, wc, hdr)) { ok = false; break; }
           // S buffer b is free once dQ has read the dS written over it two tiles ago
-          if (jc >= 2 && !mbar_wait(&sm.dq_done[b], ((jc - 2) >> 1) & 1, abort_flag, hdr)) {
+          if (jc >= 2 && !mbar_wait(&sm.dq_done[b], ((jc - 2) >> 1) & 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -928,12 +931,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_kk(tmem + 128 * b, q_s, smem_u32(sm.k[st]), false);        // S = Q K^T
           mma_commit(&sm.s_full[b]);
           mma_commit(&sm.k_empty[st]);
-          if ((jj & 1) == 0 && !issue_dp(sm, tmem, jc, abort_flag, hdr)) { ok = false; break; }
+          if ((jj & 1) == 0 && !issue_dp(sm, tmem, jc, wc, hdr)) { ok = false; break; }
           ++jc;
         }
         if (!ok) break;
         mma_commit(&sm.q_empty);
       }
+      mma_drain(&sm.drain1);              // every product done before TMEM is freed
     }
   } else if (warp == kWarpMma2) {
     // ------------------------------------------------------------ stream 2: dP of odd tiles, dQ
@@ -942,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok) {
         const uint32_t slot = it_count & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
         const QItem it = sm.items[slot];
         mbar_arrive(&sm.item_empty[slot]);
         ++it_count;
@@ -953,13 +957,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dP of the next tile when its in-item index is odd: it is due
           // before this tile's dQ (the softmax frees dP mid-tile)
           if (((jj + 1) & 1) == 1 && jj + 1 < it.n_kv &&
-              !issue_dp(sm, tmem, jc + 1, abort_flag, hdr)) {
+              !issue_dp(sm, tmem, jc + 1, wc, hdr)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&sm.p_full[b], (jc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+          if (!mbar_wait(&sm.p_full[b], (jc >> 1) & 1, wc, hdr)) { ok = false; break; }
           if (jj == 0 && items_done > 0 &&
-              !mbar_wait(&sm.epi_done, (items_done - 1) & 1, abort_flag, hdr)) {
+              !mbar_wait(&sm.epi_done, (items_done - 1) & 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -976,6 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&sm.o_full);
         ++items_done;
       }
+      mma_drain(&sm.drain2);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + dQ epilogue
@@ -988,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok) {
       const uint32_t slot = it_count & 1;
-      if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+      if (!mbar_wait_warp(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
       const QItem it = sm.items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
@@ -1023,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b = jc & 1;
         const uint32_t s_tm = tmem + lane_base + 128 * b + wg * 64;
         const uint32_t dp_tm = tmem + lane_base + 256 + wg * 64;
-        if (!mbar_wait(&sm.s_full[b], (jc >> 1) & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full[b], (jc >> 1) & 1, wc, hdr)) { ok = false; break; }
         tc_fence_after();
         // phase 1: P = exp2(S sl2 - nlse2), masked to the row's visible keys
         uint32_t pf[64];
@@ -1047,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // phase 2: dS = P (dP - delta) in bf16 over S (masked P is zero)
-        if (!mbar_wait(&sm.dp_full, jc & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.dp_full, jc & 1, wc, hdr)) { ok = false; break; }
         tc_fence_after();
         uint32_t dp[64];
         tmem_ld32(dp_tm, *reinterpret_cast<uint32_t(*)[32]>(dp));
@@ -1076,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: dQ = scale * accumulated dS K, written once in bf16 (my half of d)
       __nv_bfloat16* dst = a.dq + qo_offset(p, row, h) + wg * 64;
       if (it.n_kv > 0) {
-        if (!mbar_wait(&sm.o_full, items_done & 1, abort_flag, hdr)) break;
+        if (!mbar_wait_warp(&sm.o_full, items_done & 1, wc, hdr)) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -1164,6 +1169,7 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   if (e != cudaSuccess) return e;
   BwdArgs a;
   a.p = p;
+  a.p.wait_budget = wait_budget_cycles();
   a.nlse2 = nlse2;
   a.delta = delta;
   a.Tp = L.Tp;
@@ -1199,10 +1205,12 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   e = launch_dependent(attn_bwd_dkdv_tc_kernel, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq,
                        mdo, mk, mv, a);
   count_launches(1);
+  count_path(true);
   if (e != cudaSuccess) return e;
   e = launch_dependent(attn_bwd_dq_tc_kernel, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo,
                        mk, mv, a);
   count_launches(1);
+  count_path(true);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -85,8 +85,9 @@ struct __align__(1024) Smem {
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t item_full[2], item_empty[2];
   Item items[2];
+  uint64_t mma_drain_bar;
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wait;
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;      // + alignment slack
@@ -120,14 +121,6 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   for (int kk = 0; kk < BN / 16; ++kk) {
     mma_ts(d_tmem, p_tmem + kk * 8, vd + ((kk * 2048) >> 4), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
-  }
-}
-
-// Long bounded wait used only to drain in-flight TMA copies after an abort.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitTimeoutCycles) return;
   }
 }
 
@@ -193,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.item_full[t], 1);
       mbar_init(&sm.item_empty[t], 1 + 8);
     }
-    sm.abort_flag = 0;
+    mbar_init(&sm.mma_drain_bar, 1);
+    wait_ctl_init(&sm.wait, p.wait_budget);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -210,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   const uint32_t tmem = sm.tmem_base;
-  volatile int* abort_flag = &sm.abort_flag;
+  WaitCtl* const wc = &sm.wait;
   const int n_pairs = p.Hq >> 1;
   const int G = p.Hq / p.Hkv;
   // query tiles no key of the range reaches are not work items: the softmax
@@ -240,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t slot = it_count & 1;
         if (it_count >= 2 &&
-            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, abort_flag, hdr)) {
+            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, wc, hdr)) {
           ok = false;
           break;
         }
@@ -251,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (it.n_kv < 0) break;
           continue;
         }
-        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, abort_flag, hdr)) {
+        if (q_count >= 1 && !mbar_wait(&sm.q_empty, (q_count - 1) & 1, wc, hdr)) {
           ok = false;
           break;
         }
@@ -272,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
           const int key0 = (it.j_lo + jj) * BN;
-          if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+          if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -281,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < 2; ++cb)
             tma_load_2d(sm.k[st] + cb * kColBlockBytes, &tm_k, &sm.k_full[st], it.g * HD + cb * 64,
                         key0);
-          if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, hdr)) {
+          if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, wc, hdr)) {
             // the K copy just issued is in flight: drain it before leaving
             drain_wait(&sm.k_full[st], use & 1);
             ok = false;
@@ -295,8 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kv_count;
         }
       }
-      if (!ok) {
-        // Abort: wait (bounded) for every copy still in flight to land.
+      {
+        // Leaving, normally or on an abort: wait (bounded) for every copy still
+        // in flight to land (after a normal end these phases completed long ago).
         if (q_count >= 1) drain_wait(&sm.q_full, (q_count - 1) & 1);
         for (uint32_t s = 0; s < NSTAGE && s < kv_count; ++s) {
           const uint32_t last = kv_count - 1 - ((kv_count - 1 - s) % NSTAGE);
@@ -313,18 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_saddr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
       while (true) {
         const uint32_t slot = it_count & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
         const Item it = sm.items[slot];
         mbar_arrive(&sm.item_empty[slot]);
         ++it_count;
         if (it.n_kv < 0) break;
         if (it.n_kv == 0) continue;
-        if (!mbar_wait(&sm.q_full, q_count & 1, abort_flag, hdr)) break;
+        if (!mbar_wait(&sm.q_full, q_count & 1, wc, hdr)) break;
         ++q_count;
         bool ok = true;
         {
           const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
-          if (!mbar_wait(&sm.k_full[st], use & 1, abort_flag, hdr)) break;
+          if (!mbar_wait(&sm.k_full[st], use & 1, wc, hdr)) break;
           tc_fence_after();
           const uint32_t ks = smem_u32(sm.k[st]);
           issue_qk(tmem + col_s(0), q_saddr[0], ks);
@@ -338,12 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = (kv_count + jj) % NSTAGE, use = (kv_count + jj) / NSTAGE;
           const bool has_next = jj + 1 < it.n_kv;
           const uint32_t stn = (kv_count + jj + 1) % NSTAGE, usen = (kv_count + jj + 1) / NSTAGE;
-          if (!mbar_wait(&sm.v_full[st], use & 1, abort_flag, hdr)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[st], use & 1, wc, hdr)) { ok = false; break; }
           const uint32_t vs = smem_u32(sm.v[st]);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!ok) continue;
-            if (!mbar_wait(&sm.p_full[t], p_count[t] & 1, abort_flag, hdr)) { ok = false; continue; }
+            if (!mbar_wait(&sm.p_full[t], p_count[t] & 1, wc, hdr)) { ok = false; continue; }
             ++p_count[t];
             tc_fence_after();
             // a ring accumulation's O starts as the preloaded running output
@@ -354,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               continue;
             }
             if (t == 0) {
-              if (!mbar_wait(&sm.k_full[stn], usen & 1, abort_flag, hdr)) { ok = false; continue; }
+              if (!mbar_wait(&sm.k_full[stn], usen & 1, wc, hdr)) { ok = false; continue; }
               tc_fence_after();
             }
             issue_qk(tmem + col_s(t), q_saddr[t], smem_u32(sm.k[stn]));
@@ -368,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         kv_count += it.n_kv;
       }
+      mma_drain(&sm.mma_drain_bar);        // every product done before TMEM is freed
     }
   }
   } else {
@@ -410,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     while (true) {
       const uint32_t slot = it_count & 1;
-      if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, abort_flag, hdr)) break;
+      if (!mbar_wait_warp(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
       const Item it = sm.items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
@@ -470,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       for (int jj = 0; jj < it.n_kv; ++jj) {
-        if (!mbar_wait(&sm.s_full[t], s_count & 1, abort_flag, hdr)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full[t], s_count & 1, wc, hdr)) { ok = false; break; }
         ++s_count;
         tc_fence_after();
         const int key0 = (it.j_lo + jj) * BN;
@@ -548,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       TO* dst = out + qo_offset(p, row, h);
       if (it.n_kv > 0) {
-        if (!mbar_wait(&sm.o_full[t], o_count & 1, abort_flag, hdr)) break;
+        if (!mbar_wait_warp(&sm.o_full[t], o_count & 1, wc, hdr)) break;
         ++o_count;
         tc_fence_after();
         if constexpr (sizeof(TO) == 4) {
@@ -655,6 +651,7 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
                        reinterpret_cast<const int2*>(ws + L.tiles),
                        reinterpret_cast<const int*>(ws + L.order));
   count_launches(1);
+  count_path(true);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -672,8 +669,10 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
       !make_map(&mv, p.v, p.kv_len, (int64_t)p.Hkv * HD))
     return cudaSuccess;                       // no tensor-map support: CUDA-core path
   *launched = true;
-  return p.out_dtype == NSP_F32 ? launch_typed<float>(p, L, ws, s, mq, mk, mv)
-                                : launch_typed<__nv_bfloat16>(p, L, ws, s, mq, mk, mv);
+  AttnProblem pk = p;
+  pk.wait_budget = wait_budget_cycles();
+  return pk.out_dtype == NSP_F32 ? launch_typed<float>(pk, L, ws, s, mq, mk, mv)
+                                 : launch_typed<__nv_bfloat16>(pk, L, ws, s, mq, mk, mv);
 }
 
 }  // namespace nsp

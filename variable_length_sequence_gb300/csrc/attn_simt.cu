@@ -311,6 +311,7 @@ template <typename TI, typename TO, int D>
 cudaError_t fwd_dispatch(const AttnProblem& p, cudaStream_t s) {
   dim3 grid((unsigned)ceil_div(p.q_len, kFwdBM), (unsigned)p.Hq);
   attn_fwd_simt_kernel<TI, TO, D><<<grid, kFwdThreads, 0, s>>>(p); count_launches(1);
+  count_path(false);
   return cudaGetLastError();
 }
 
@@ -338,6 +339,7 @@ cudaError_t bwd_dispatch(const AttnProblem& p, const void* out, const void* dout
       p, reinterpret_cast<const TI*>(dout), lse, delta, L.Tp, dq_acc, reinterpret_cast<TI*>(dk),
       reinterpret_cast<TI*>(dv), reinterpret_cast<float*>(dk), reinterpret_cast<float*>(dv));
   count_launches(1);
+  count_path(false);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.accumulate) return e;
   return launch_dq_convert(dq_acc, dq, T * p.Hq * D, p.io_dtype, p.hdr, s);

@@ -64,15 +64,16 @@ extern "C" int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void
                                         int32_t causal, int32_t io_dtype, void* out,
                                         int32_t out_dtype, float* lse, int32_t* device_status,
                                         nsp_stream_t stream) {
-  if (q_len < 0 || kv_len < 0) return NSP_ERR_INVALID;
-  if (fwd_ws_layout(q_len, kv_len).total > kNoAllocScratchBytes) return NSP_ERR_WORKSPACE;
-  // Host checks of nsp_attn_fwd; a placeholder stands for the static scratch.
+  // The host checks of nsp_attn_fwd, with a placeholder standing for the
+  // static scratch and its size as the workspace size: they bound the sizes
+  // first and return NSP_ERR_WORKSPACE when the call's scheduler state would
+  // not fit, so every error code matches nsp_attn_fwd's.
   int32_t st = nsp_attn_fwd_validate(q, k, v, cu_seqlens, ndoc, q_start, q_len, kv_start, kv_len,
                                      Hq, Hkv, d, causal, io_dtype, out, out_dtype,
                                      reinterpret_cast<const void*>(uintptr_t(256)),
                                      kNoAllocScratchBytes);
   if (st != NSP_OK) return st;
-  if (!(scale > 0.f && scale <= 3.0e38f)) return NSP_ERR_INVALID;
+  if (!scale_ok(scale)) return NSP_ERR_INVALID;
   if ((lse && (reinterpret_cast<uintptr_t>(lse) & 15u)) ||
       (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)))
     return NSP_ERR_ALIGN;

@@ -26,6 +26,9 @@ constexpr int kTileM = 128;        // query rows per tile (tcgen05 M)
 constexpr int kTileN = 128;        // keys per KV tile
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The softmax scale must be a positive finite number (a temperature).
+inline bool scale_ok(float scale) { return scale > 0.f && scale <= 3.0e38f; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Forward workspace layout (all offsets from the workspace base).
@@ -110,6 +113,10 @@ struct AttnProblem {
   // Query-side layout (q, out, dout, dq): 1 = [q_len, Hq, d]; P > 1 = the
   // head-group-major [P][q_len][Hq / P][d] layout an all-to-all delivers.
   int32_t q_groups = 1;
+  // Cycles a bounded device wait may last before the kernel records
+  // NSP_ERR_TIMEOUT and leaves (set by the launchers from
+  // nsp_set_wait_timeout_cycles).
+  int64_t wait_budget = 4000000000LL;
 };
 
 // ---- launchers implemented in the .cu files (return cudaError_t) ----
@@ -143,6 +150,9 @@ cudaError_t launch_lse_merge_segments(int nseg, const int* counts, const float* 
                                       cudaStream_t s);
 cudaError_t launch_permute(const void* in, void* out, int64_t T, int H, int d, int P,
                            int elem_bytes, int inverse, cudaStream_t s);
+// nb independent permutations of T-token groups stacked in memory.
+cudaError_t launch_permute_groups(const void* in, void* out, int64_t nb, int64_t T, int H, int d,
+                                  int P, int elem_bytes, int inverse, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();
@@ -153,6 +163,13 @@ int persistent_grid();
 
 // Adds n to the library-wide count of kernels launched (nsp_kernel_launches).
 void count_launches(int n);
+
+// Counts one attention kernel launch on the tensor-core path (true) or the
+// CUDA-core path (false) (nsp_path_launches).
+void count_path(bool tensor_core);
+
+// The process-wide bound of device waits (nsp_set_wait_timeout_cycles).
+int64_t wait_budget_cycles();
 
 }  // namespace nsp
 

@@ -12,11 +12,28 @@
 namespace nsp {
 namespace tc {
 
-// ~2 s at 2 GHz: far beyond any legitimate wait inside one kernel.
+// ~2 s at 2 GHz: far beyond any legitimate wait inside one kernel.  The
+// default bound of every wait; a call may set a shorter one (AttnProblem
+// wait_budget), and drains after an abort always use this one.
 constexpr long long kWaitTimeoutCycles = 4000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Per-CTA state of the bounded waits, in shared memory, written by thread 0
+// before the CTA's first barrier.
+struct WaitCtl {
+  int abort;            // raised by the first wait that expires; every role then leaves
+  uint32_t hint_ns;     // hardware suspend hint of one probe of a bounded wait
+  long long budget;     // cycles a bounded wait may last
+};
+
+__device__ __forceinline__ void wait_ctl_init(WaitCtl* w, long long budget) {
+  w->abort = 0;
+  w->budget = budget;
+  // a probe may suspend the thread for up to hint_ns: keep it below the budget
+  w->hint_ns = budget >= 80000 ? 20000u : (uint32_t)(budget > 0 ? budget / 4 : 0);
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -41,36 +58,59 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx
 }
 
 // One bounded probe of the phase; the thread may be suspended in hardware
-// for up to kSuspendHintNs waiting for it (instead of spinning on issue slots).
+// for up to hint_ns waiting for it (instead of spinning on issue slots).
 constexpr uint32_t kSuspendHintNs = 20000;
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and raises the CTA's abort flag) if the bound expires or another
-// role already aborted; the caller then leaves its loop.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, WsHeader* hdr) {
-  if (mbar_try_wait(bar, parity)) return true;
+// false (and raises the CTA's abort flag, recording NSP_ERR_TIMEOUT) when the
+// budget expires, or false at once when another role already aborted; the
+// caller then leaves its loop.  Single-thread roles only: a warp whose lanes
+// all wait uses mbar_wait_warp.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl* wc,
+                                          WsHeader* hdr) {
+  // the bound and the hint are re-read from shared memory on the slow path
+  // only, so a waiting role keeps no extra registers live
+  volatile WaitCtl* w = wc;
+  if (mbar_try_wait(bar, parity, w->hint_ns)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
-      *abort_flag = 1;
+    if (mbar_try_wait(bar, parity, w->hint_ns)) return true;
+    if (w->abort) return false;
+    if (clock64() - t0 > w->budget) {
+      w->abort = 1;
       atomicExch(&hdr->status, (int)NSP_ERR_TIMEOUT);
       return false;
     }
+  }
+}
+
+// The same for a whole warp: every lane gets false when any lane's wait
+// failed, so lanes never part before a warp-collective instruction (a
+// .sync.aligned TMEM access, a shuffle, __syncwarp).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, WaitCtl* wc,
+                                               WsHeader* hdr) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, hdr));
+}
+
+// Wait used only while leaving: for copies or products already issued (they
+// always complete), bounded by the default budget whatever the call's.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitTimeoutCycles) return;
   }
 }
 
@@ -156,6 +196,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// Leaving a role that issued MMAs: wait until every tcgen05 operation this
+// thread issued (and the arrivals its earlier commits promised) has
+// completed, so that no product still writes tensor memory or signals a
+// barrier of this CTA once it deallocates and exits.  `bar` is a barrier of
+// its own (count 1) used for nothing else.
+__device__ __forceinline__ void mma_drain(uint64_t* bar) {
+  mma_commit(bar);
+  drain_wait(bar, 0);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, f32 D, dense.

@@ -31,6 +31,8 @@ _SIGNATURES = {
     "nsp_status_str": (C.c_char_p, [_i32]),
     "nsp_version": (C.c_char_p, []),
     "nsp_kernel_launches": (_i64, []),
+    "nsp_set_wait_timeout_cycles": (_i64, [_i64]),
+    "nsp_path_launches": (_i64, [_i32]),
     "nsp_attn_fwd_workspace_size": (_sz, [_i64, _i64, _i32, _i32, _i32]),
     "nsp_attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32,
                             _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -59,6 +61,8 @@ _SIGNATURES = {
     "nsp_lse_merge_validate": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _vp, _i32, _vp]),
     "nsp_seq2head_permute": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
     "nsp_seq2head_permute_validate": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _i32]),
+    "nsp_seq2head_permute_groups": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32,
+                                           _vp]),
     "nsp_status_query": (_i32, [_vp, _vp]),
     "nsp_attn_pairs": (_i32, [_vp, _i32, _i32, C.POINTER(C.c_double)]),
     "nsp_attn_cost": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
@@ -272,8 +276,27 @@ def nsp_seq2head_permute(inp, out, T, H, d, P, inverse=False, stream=None) -> in
     return _check("nsp_seq2head_permute", st)
 
 
+def nsp_seq2head_permute_groups(inp, out, B, L, H, d, K, inverse=False, stream=None) -> int:
+    st = load().nsp_seq2head_permute_groups(_ptr(inp), _ptr(out), int(B), int(L), int(H), int(d),
+                                            int(K), inp.element_size(), int(bool(inverse)),
+                                            _stream(stream))
+    return _check("nsp_seq2head_permute_groups", st)
+
+
 def nsp_kernel_launches() -> int:
     return int(load().nsp_kernel_launches())
+
+
+def nsp_path_launches(tensor_core: bool) -> int:
+    """Attention kernels launched so far on the tensor-core (True) or the
+    CUDA-core (False) path."""
+    return int(load().nsp_path_launches(int(bool(tensor_core))))
+
+
+def nsp_set_wait_timeout_cycles(cycles: int) -> int:
+    """Bound of the kernels' device waits in GPU cycles (< 0: the default);
+    returns the previous bound."""
+    return int(load().nsp_set_wait_timeout_cycles(int(cycles)))
 
 
 def nsp_status_query(workspace, stream=None) -> int:
@@ -423,6 +446,23 @@ def seq2head(x, P, stream=None):
     T, H, d = x.shape
     out = torch.empty((P, T, H // P, d), dtype=x.dtype, device=x.device)
     nsp_seq2head_permute(x, out, T, H, d, P, False, stream)
+    return out
+
+
+def seq2head_groups(x, B, K, stream=None):
+    """[B L, H, d] -> [B, K, L, H / K, d]: the receive side of B independent
+    K-way (batch-aware subgroup) all-to-alls."""
+    BL, H, d = x.shape
+    L = BL // B
+    out = torch.empty((B, K, L, H // K, d), dtype=x.dtype, device=x.device)
+    nsp_seq2head_permute_groups(x, out, B, L, H, d, K, False, stream)
+    return out
+
+
+def head2seq_groups(y, stream=None):
+    B, K, L, h, d = y.shape
+    out = torch.empty((B * L, K * h, d), dtype=y.dtype, device=y.device)
+    nsp_seq2head_permute_groups(y, out, B, L, K * h, d, K, True, stream)
     return out
 
 

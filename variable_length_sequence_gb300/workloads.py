@@ -151,6 +151,29 @@ def make_workload(cid: int, shuffle: bool = False, with_dout: Optional[bool] = N
     return Workload(cfg, lens, cu_from_lengths(lens), q, k, v, dout)
 
 
+def make_workload_device(cid: int, device, seed: Optional[int] = None) -> Workload:
+    """Config `cid` with its seeded lengths (the same draw as make_workload)
+    and its tensors drawn on `device` by torch's seeded generator: the same
+    shapes and N(0, 1) values rounded to bf16, generated in milliseconds
+    instead of minutes for the large configs.  Not the same numbers as
+    make_workload (the benchmark needs the distribution, not the bits)."""
+    cfg = CONFIGS[cid]
+    s = seed_of(cid) if seed is None else seed
+    lens = draw_lengths(cfg, np.random.default_rng(s))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(s)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    T = cfg.T
+
+    def draw(shape):
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(dt)
+    q = draw((T, cfg.Hq, cfg.d))
+    k = draw((T, cfg.Hkv, cfg.d))
+    v = draw((T, cfg.Hkv, cfg.d))
+    dout = draw((T, cfg.Hq, cfg.d)) if cfg.bwd else None
+    return Workload(cfg, lens, cu_from_lengths(lens), q, k, v, dout)
+
+
 def make_custom(lengths, Hq: int, Hkv: int, d: int, dtype: str = "bf16", seed: int = 0,
                 with_dout: bool = True) -> Workload:
     """A small seeded workload with explicit document lengths (edge cases)."""
@@ -163,6 +186,29 @@ def make_custom(lengths, Hq: int, Hkv: int, d: int, dtype: str = "bf16", seed: i
     v = _normal(rng, (T, Hkv, d), dtype)
     dout = _normal(rng, (T, Hq, d), dtype) if with_dout else None
     return Workload(cfg, lens, cu_from_lengths(lens), q, k, v, dout)
+
+
+def make_growing(lengths, Hq: int, Hkv: int, d: int, seed: int = 0, gain: float = 8.0,
+                 ramp: float = 4.0, with_dout: bool = True) -> Workload:
+    """make_custom's bf16 draws with one component overwritten so that scores
+    rise along every document: component 0 of every query is ``gain`` and
+    component 0 of key j is ``ramp * (j - start of j's document) / 128``.
+    Against later keys of its document a query's scores then climb by about
+    gain * ramp / sqrt(d) per 128 keys (at the usual scale 1/sqrt(d)), on top
+    of the N(0, 1) noise of the other components, so a row's running maximum
+    keeps growing as key tiles are visited in order: inputs that drive the
+    online softmax's rescaling of a running output."""
+    w = make_custom(lengths, Hq, Hkv, d, dtype="bf16", seed=seed, with_dout=with_dout)
+    cu = w.cu_seqlens.astype(np.int64)
+    pos = np.arange(w.T, dtype=np.int64) - np.repeat(cu[:-1], np.diff(cu))
+    q = w.q.float()
+    k = w.k.float()
+    q[:, :, 0] = gain
+    k[:, :, 0] = torch.from_numpy((ramp * pos / 128.0).astype(np.float32))[:, None]
+    w.q = q.to(torch.bfloat16)
+    w.k = k.to(torch.bfloat16)
+    w.extra.update(gain=gain, ramp=ramp)
+    return w
 
 
 def shard_bounds(T: int, shards: int) -> list:
