@@ -10,9 +10,9 @@
 // bwd_delta_kernel in padded [Hq, Tp] rows.
 //
 // Both kernels use 128 x 128 x 128 products only, and issue them from two
-// threads (two tcgen05 streams): one M = 128 MMA stream keeps only about
-// half of an SM's tensor core busy, two independent streams keep most of it
-// busy.
+// threads (two tcgen05 streams): products of one thread run in issue order,
+// so a product that must wait for the softmax would otherwise hold up the
+// independent products queued behind it.
 //
 // dK/dV kernel (key-stationary).  Work item: one 128-key tile of one KV
 // head; it walks every (query head of the group, 128-row query tile that
