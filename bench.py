@@ -426,6 +426,22 @@ class Problem:
                                          True, self._hg_dq, self._hg_dk, self._hg_dv, self.ws_b,
                                          stream)
 
+    def fwd_mha(self, stream):
+        """The forward with the pages' own head layout, multi-head attention:
+        as many key/value heads as query heads (the paired-tile tensor-core
+        path), on the same documents and q."""
+        if not hasattr(self, "_mha_k"):
+            g = torch.Generator(device=self.q.device)
+            g.manual_seed(77)
+            shape = (self.T, self.Hq, self.d)
+            self._mha_k = torch.randn(shape, generator=g, device=self.q.device).to(torch.bfloat16)
+            self._mha_v = torch.randn(shape, generator=g, device=self.q.device).to(torch.bfloat16)
+            self._mha_o = torch.empty_like(self.q)
+            self._mha_l = torch.empty_like(self.lse)
+        self.nsp.nsp_attn_fwd(self.q, self._mha_k, self._mha_v, self.cu, len(self.w.lengths), 0,
+                              self.T, 0, self.T, self.Hq, self.Hq, self.d, self.scale, True,
+                              self._mha_o, self._mha_l, self.ws_f, stream)
+
     def merged_l_view(self, qs):
         # [Hq, T] is not sliceable per shard contiguously; merge into a per-shard buffer
         if not hasattr(self, "_ml"):
@@ -789,7 +805,8 @@ def time_extra_legs(prob, stream, flush, K, peaks):
     """Entry points outside the step, timed alone the same way (graph replay,
     L2 flushed before each timed call, CUDA events on the stream):
     fwd_headgroups / bwd_headgroups, forward and backward on the all-to-all's
-    receive layout;
+    receive layout; fwd_mha, the forward with multi-head attention (as many
+    key/value heads as query heads);
     ring_accumulate, the ring legs with the merge fused into attention, and
     ring_bwd, the ring backward (its three float32 accumulators are zeroed
     inside the timed region, by PyTorch)."""
@@ -806,6 +823,11 @@ def time_extra_legs(prob, stream, flush, K, peaks):
             extra["bwd_headgroups"] = {"ms": ms, "tflops": tf,
                                        "frac_bf16": tf / peaks["bf16_tflops"],
                                        "layout": "q, out, dout, dq grouped; k, v, dk, dv packed"}
+    if prob.fwd_flop > 0:
+        ms = _time_leg(prob.fwd_mha, stream, flush, reps)
+        tf = prob.fwd_flop / ms / 1e9
+        extra["fwd_mha"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
+                            "heads": f"{prob.Hq} query / {prob.Hq} key-value (multi-head)"}
     ms = _time_leg(prob.ring_accumulate, stream, flush, reps)
     tf = prob.ring_flop / ms / 1e9
     extra["ring_accumulate"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],

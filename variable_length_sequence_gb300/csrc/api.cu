@@ -153,7 +153,7 @@ int32_t nsp_attn_fwd(const void* q, const void* k, const void* v, const int32_t*
   if (lse && !aligned16(lse)) return NSP_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
-  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len);
+  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len, fwd_tile_rows(io_dtype, d, Hq, Hkv));
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;
@@ -182,7 +182,7 @@ int32_t nsp_attn_fwd_headgroups(const void* q, const void* k, const void* v,
   if (lse && !aligned16(lse)) return NSP_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
-  const FwdWsLayout L = fwd_ws_layout(T, T);
+  const FwdWsLayout L = fwd_ws_layout(T, T, fwd_tile_rows(io_dtype, d, Hq, Hkv));
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
@@ -213,7 +213,7 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
   if (!aligned16(lse_acc)) return NSP_ERR_ALIGN;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
-  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len);
+  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len, fwd_tile_rows(io_dtype, d, Hq, Hkv));
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;

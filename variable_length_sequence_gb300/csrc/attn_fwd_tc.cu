@@ -12,8 +12,13 @@
 // 128-key tiles its rows may see, and orders the query tiles by that count,
 // longest first.  A work item is (query tile, pair of query heads of one
 // KV group): both heads read the same K/V tiles, so every K/V tile loaded
-// into shared memory feeds two 128x128x128 QK^T and two PV products.  A
-// persistent grid of one CTA per SM takes items from an atomic counter.
+// into shared memory feeds two 128x128x128 QK^T and two PV products.  With
+// an odd number of query heads per KV head (multi-head attention among
+// them) a work item is instead (two adjacent 128-row query tiles, one
+// head): the scheduler lists 256-row tiles, whose key range is the union of
+// its two halves', and the two halves take the two softmax roles (a half
+// whose rows cannot see a key tile gets P = 0 there).  A persistent grid of
+// one CTA per SM takes items from an atomic counter.
 //
 // CTA roles (384 threads, three warpgroups):
 //   warps 0-3  softmax for head h0 (TMEM lanes 0-127, one query row each)
@@ -68,8 +73,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Item {
-  int qtile;      // query tile index (-1: none)
-  int h0;         // first of the two query heads
+  int qtile;      // scheduled query tile (-1: none): 128 rows, or 256 with paired tiles
+  int h0;         // first of the two query heads (paired tiles: the one head)
   int g;          // key/value head
   int j_lo;       // first KV tile
   int n_kv;       // number of KV tiles (0: no key visible; -1: stop)
@@ -205,11 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t tmem = sm.tmem_base;
   WaitCtl* const wc = &sm.wait;
-  const int n_pairs = p.Hq >> 1;
   const int G = p.Hq / p.Hkv;
+  // odd G (multi-head attention among them): an item is two adjacent
+  // 128-row tiles of one head instead of one tile and two heads
+  const bool pair_tiles = (G & 1) != 0;
+  const int per_tile = pair_tiles ? p.Hq : (p.Hq >> 1);         // items per scheduled tile
+  const int tile_rows = pair_tiles ? 2 * BM : BM;
   // query tiles no key of the range reaches are not work items: the softmax
   // warps zero-fill them up front (or, accumulating, leave them alone)
-  const int n_items = hdr->n_nonempty * n_pairs;
+  const int n_items = hdr->n_nonempty * per_tile;
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -223,12 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
         it.qtile = -1; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
         if (idx < n_items) {
-          const int qt = order[idx / n_pairs];
-          const int pair = idx - (idx / n_pairs) * n_pairs;
+          const int qt = order[idx / per_tile];
+          const int sub = idx - (idx / per_tile) * per_tile;
           const int2 tr = tiles[qt];
           it.qtile = qt;
-          it.h0 = 2 * pair;
-          it.g = (2 * pair) / G;
+          it.h0 = pair_tiles ? sub : 2 * sub;
+          it.g = it.h0 / G;
           it.j_lo = tr.x;
           it.n_kv = tr.y - tr.x + 1;
         }
@@ -255,12 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hpg = p.Hq / p.q_groups;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int grp = (it.h0 + t) / hpg;
-          const int row0 = (int)(grp * p.q_len) + it.qtile * BM;
+          // role t: head h0 + t of the tile, or (paired tiles) half t of the
+          // 256-row tile for head h0 (a half past the range reads rows that
+          // are never stored)
+          const int head = pair_tiles ? it.h0 : it.h0 + t;
+          const int grp = head / hpg;
+          const int row0 = (int)(grp * p.q_len) + it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
             tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full,
-                        (it.h0 + t - grp * hpg) * HD + cb * 64, row0);
+                        (head - grp * hpg) * HD + cb * 64, row0);
         }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
@@ -385,15 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every CTA in a grid-stride loop over (tile, head, 32-row group), one
       // whole row per 16-byte lane group, before the first work item.
       const int n_empty = hdr->n_items - hdr->n_nonempty;
-      const int64_t units = (int64_t)n_empty * p.Hq * 4;
+      const int groups = tile_rows / 32;                        // 32-row groups per tile
+      const int64_t units = (int64_t)n_empty * p.Hq * groups;
       constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
       constexpr int kRowsPerPass = 32 / kLanesPerRow;
       const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
       for (int64_t u = (int64_t)blockIdx.x * 8 + warp; u < units; u += (int64_t)gridDim.x * 8) {
-        const int e = (int)(u / (p.Hq * 4));
-        const int rem = (int)(u - (int64_t)e * p.Hq * 4);
-        const int hz = rem >> 2;
-        const int64_t r0 = (int64_t)order[hdr->n_nonempty + e] * BM + (rem & 3) * 32;
+        const int e = (int)(u / (p.Hq * groups));
+        const int rem = (int)(u - (int64_t)e * p.Hq * groups);
+        const int hz = rem / groups;
+        const int64_t r0 = (int64_t)order[hdr->n_nonempty + e] * tile_rows + (rem % groups) * 32;
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = r0 + rr + sub;
@@ -412,8 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.n_kv < 0) break;
-      const int h = it.h0 + t;
-      const int64_t row = (int64_t)it.qtile * BM + r;         // query-range relative
+      const int h = pair_tiles ? it.h0 : it.h0 + t;
+      // first row of this role's 128-row tile, query-range relative
+      const int64_t tile_base = (int64_t)it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
+      const int64_t row = tile_base + r;
       const bool valid = row < p.q_len;
       int lo = 0, hi = 0;                                      // key-range relative [lo, hi)
       if (valid) {
@@ -567,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
-              const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + 8 * i + (lane >> 2);
+              const int64_t grow = tile_base + wq * 32 + 8 * i + (lane >> 2);
               if (grow < p.q_len && (!p.accumulate || wpr[i] != 0.f))
                 *reinterpret_cast<float2*>(out + qo_offset(p, grow, h) + c * 32 +
                                            8 * ((k >> 1) & 3) + 2 * (lane & 3)) =
@@ -592,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
-          const int64_t grow = (int64_t)it.qtile * BM + wq * 32 + rr + sub;
+          const int64_t grow = tile_base + wq * 32 + rr + sub;
           if (grow < p.q_len)
             reinterpret_cast<uint4*>(out + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
         }
@@ -661,7 +677,7 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                cudaStream_t s, bool* launched) {
   *launched = false;
-  if (p.io_dtype != NSP_BF16 || p.d != HD || (p.Hq / p.Hkv) % 2 != 0) return cudaSuccess;
+  if (p.io_dtype != NSP_BF16 || p.d != HD) return cudaSuccess;
   if (p.q_len <= 0 || p.kv_len <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, p.q, p.q_len * p.q_groups, (int64_t)(p.Hq / p.q_groups) * HD) ||

@@ -83,7 +83,7 @@ extern "C" int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(scratch);
-  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len);
+  const FwdWsLayout L = fwd_ws_layout(q_len, kv_len, fwd_tile_rows(io_dtype, d, Hq, Hkv));
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = q_start; p.q_len = q_len; p.kv_start = kv_start; p.kv_len = kv_len;

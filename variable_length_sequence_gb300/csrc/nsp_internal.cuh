@@ -31,18 +31,32 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline bool scale_ok(float scale) { return scale > 0.f && scale <= 3.0e38f; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Forward workspace layout (all offsets from the workspace base).
+// Forward workspace layout (all offsets from the workspace base).  The
+// scheduled query tiles are tile_rows = 128 rows, or 256 when the
+// tensor-core forward pairs two 128-row tiles of one head per work item
+// (fwd_tile_rows); the size of the 128-row layout bounds both.
 struct FwdWsLayout {
   size_t tiles;        // int2 [n_qtiles]: first/last KV tile of each query tile
   size_t order;        // int32 [n_qtiles]: query tiles, most KV tiles first
   size_t hist;         // int32 [n_kvtiles + 2]: counting-sort buckets
   size_t total;
   int64_t n_qtiles, n_kvtiles;
+  int32_t tile_rows;
 };
 
-inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len) {
+// Rows of a scheduled forward query tile: 256 when the tensor-core forward
+// takes the problem (bf16, d = 128) with an odd number of query heads per
+// KV head (multi-head attention among them): a work item is then two
+// adjacent 128-row tiles of one head, which read the same K/V tiles; 128
+// otherwise (a work item is one tile and two heads of a KV group).
+inline int32_t fwd_tile_rows(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
+  return (io_dtype == NSP_BF16 && d == 128 && Hkv > 0 && ((Hq / Hkv) & 1)) ? 2 * kTileM : kTileM;
+}
+
+inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t tile_rows = kTileM) {
   FwdWsLayout L;
-  L.n_qtiles = ceil_div(q_len, kTileM);
+  L.tile_rows = tile_rows;
+  L.n_qtiles = ceil_div(q_len, tile_rows);
   L.n_kvtiles = ceil_div(kv_len, kTileN);
   size_t off = sizeof(WsHeader);
   L.tiles = off;  off = align_up(off + sizeof(int2) * (size_t)L.n_qtiles, 256);

@@ -47,6 +47,7 @@ struct SchedArgs {
   int32_t n_tiles;     // tiles to schedule
   int32_t n_buckets;   // max cost + 1 (cost = number of listed tiles)
   int32_t gran;        // granularity (rows or keys) of the listed tiles
+  int32_t tile_rows;   // mode 0: rows of a scheduled query tile (128 or 256)
   WsHeader* hdr;
   int32_t second;      // write counters into counter2 / n_items2
 };
@@ -93,8 +94,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
     int lo_t = 0, hi_t = -1;
     if (a.mode == 0) {
-      const int64_t r0 = a.q_start + (int64_t)i * kTileM;
-      const int64_t r1 = min(r0 + kTileM, q_end) - 1;          // last row of the tile
+      const int64_t r0 = a.q_start + (int64_t)i * a.tile_rows;
+      const int64_t r1 = min(r0 + a.tile_rows, q_end) - 1;     // last row of the tile
       const int b0 = doc_of(a.cu, a.ndoc, r0), b1 = doc_of(a.cu, a.ndoc, r1);
       const int64_t lo = max((int64_t)a.cu[b0], a.kv_start);
       const int64_t hi = min(a.causal ? r1 + 1 : (int64_t)a.cu[b1 + 1], kv_end);  // exclusive
@@ -177,6 +178,7 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
                                 cudaStream_t s) {
   SchedArgs a;
   a.gran = kTileN;
+  a.tile_rows = L.tile_rows;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
   a.causal = p.causal; a.mode = 0; a.validate = 1;
@@ -196,7 +198,7 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   SchedArgs a;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
-  a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub;
+  a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub; a.tile_rows = kTileM;
   a.tiles = reinterpret_cast<int2*>(ws + L.qtiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.qorder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.qhist);
