@@ -8,9 +8,10 @@ bf16 inputs, float32 accumulation):
 
   1. nsp_attn_fwd    -- schedule + varlen causal attention forward (out, lse)
   2. nsp_attn_bwd    -- dq, dk, dv from out, lse, dout
-  3. ring legs       -- the stream split into 8 shards of 4096 tokens; one
-                        nsp_attn_fwd partial per non-empty causal (q-shard,
-                        kv-shard) pair (float32 out), nsp_lse_merge per shard
+  3. ring legs       -- the stream split into 8 shards of 4096 tokens; the
+                        float32 partial of every non-empty causal (q-shard,
+                        kv-shard) block in one nsp_attn_fwd_blocks call, then
+                        one nsp_lse_merge_batch over every shard
   4. nsp_seq2head_permute -- q seq->head (8 groups) and back (head->seq)
 
 ``value`` = useful attention TFLOP/s of the whole step: (4 d fwd + 10 d bwd
@@ -329,13 +330,19 @@ class Problem:
                               self.scale, True, self.dq, self.dk, self.dv, self.ws_b, stream)
 
     def ring_partials(self, stream):
+        """Every non-empty causal (q-shard, kv-shard) block's float32 partial,
+        all in one batched call (nsp_attn_fwd_blocks)."""
         n = self.T // RING_SHARDS
-        for qs, ks, _ in self.ring_pairs:
-            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
-            self.nsp.nsp_attn_fwd(self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n],
-                                  self.cu, len(self.w.lengths), qa, n, ka, n, self.Hq, self.Hkv,
-                                  self.d, self.scale, True, self.part_o[(qs, ks)],
-                                  self.part_l[(qs, ks)], self.ws_r, stream)
+        if not hasattr(self, "_ring_blocks"):
+            self._ring_blocks = [(self.bounds[qs][0], n, self.bounds[ks][0], n,
+                                  self.part_o[(qs, ks)], self.part_l[(qs, ks)])
+                                 for qs, ks, _ in self.ring_pairs]
+            self._ws_blocks = torch.empty(self.nsp.nsp_attn_fwd_blocks_workspace_size(
+                self._ring_blocks, self.Hq, self.Hkv, self.d), dtype=torch.uint8,
+                device=self.q.device)
+        self.nsp.nsp_attn_fwd_blocks(self.q, self.k, self.v, self.cu, len(self.w.lengths), self.T,
+                                     self._ring_blocks, self.Hq, self.Hkv, self.d, self.scale, True,
+                                     False, self._ws_blocks, stream)
 
     def merge(self, stream):
         """Every shard's partials merged in one launch (nsp_lse_merge_batch)."""
@@ -350,25 +357,27 @@ class Problem:
         self.nsp.nsp_lse_merge_batch(segments, outs, lses, stream)
 
     def ring_accumulate(self, stream):
-        """The ring legs with the merge fused into the attention epilogue: per
-        query shard the diagonal block is a plain float32 partial (it writes the
-        running result), every other block is merged into it in place by
-        nsp_attn_fwd_accumulate.  Result: float32 out and lse per shard."""
+        """The ring legs with the merge fused into the attention epilogue, one
+        batched call per ring step: step s meets query shard i with key shard
+        i - s (the non-empty causal blocks); step 0 (the diagonal blocks)
+        writes each shard's running float32 out and lse, the later steps merge
+        into them in place."""
         n = self.T // RING_SHARDS
-        started = set()
-        # a ring meets its own (diagonal) block first: that one writes the
-        # running result; the blocks received after it are merged into it
-        order = sorted(self.ring_pairs, key=lambda e: (e[0], e[1] != e[0], e[1]))
-        for qs, ks, _ in order:
-            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
-            args = (self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n], self.cu,
-                    len(self.w.lengths), qa, n, ka, n, self.Hq, self.Hkv, self.d, self.scale,
-                    True, self.acc_o[qa:qa + n], self.acc_l[qs], self.ws_r, stream)
-            if qs in started:
-                self.nsp.nsp_attn_fwd_accumulate(*args)
-            else:
-                self.nsp.nsp_attn_fwd(*args)
-                started.add(qs)
+        if not hasattr(self, "_acc_steps"):
+            pairs = {(qs, ks) for qs, ks, _ in self.ring_pairs}
+            self._acc_steps = []
+            for st in range(RING_SHARDS):
+                bl = [(self.bounds[qs][0], n, self.bounds[qs - st][0], n,
+                       self.acc_o[self.bounds[qs][0]:self.bounds[qs][0] + n], self.acc_l[qs])
+                      for qs in range(st, RING_SHARDS) if (qs, qs - st) in pairs]
+                if bl:
+                    ws = torch.empty(self.nsp.nsp_attn_fwd_blocks_workspace_size(
+                        bl, self.Hq, self.Hkv, self.d), dtype=torch.uint8, device=self.q.device)
+                    self._acc_steps.append((st > 0, bl, ws))
+        for acc, bl, ws in self._acc_steps:
+            self.nsp.nsp_attn_fwd_blocks(self.q, self.k, self.v, self.cu, len(self.w.lengths),
+                                         self.T, bl, self.Hq, self.Hkv, self.d, self.scale, True,
+                                         acc, ws, stream)
 
     def ring_bwd(self, stream):
         """The ring backward: every causal (q-shard, kv-shard) block's dq/dk/dv

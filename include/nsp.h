@@ -212,6 +212,47 @@ int32_t nsp_attn_fwd_headgroups(const void* q, const void* k, const void* v,
                                 void* workspace, size_t workspace_bytes, nsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Batched ring blocks: several (query range, key range) blocks of the same
+ * packed stream in one call ([HSAP] Sec. 2.2.1, InterSP: each rank's query
+ * shard meets every key/value shard; Sec. 3.2, attention blocks A1-A5).  On
+ * one GPU holding every shard, a ring step (or a whole ring) is one schedule
+ * and one persistent launch instead of one call per block.
+ *
+ *   q: device [T][Hq][d], k, v: device [T][Hkv][d]: the whole packed stream;
+ *      a block's rows are addressed by global token ids.
+ *   blocks: host array of nblocks (1..64) descriptors, read during the call:
+ *      q_start, q_len: the block's query rows; kv_start, kv_len: its keys;
+ *      out: device float32 [q_len][Hq][d]; lse: device float32 [Hq][q_len]
+ *      (required when accumulate = 1, else optional).
+ *   accumulate = 0: each block's out / lse are written with the partial of
+ *      its rows against its keys, exactly as nsp_attn_fwd with out_dtype =
+ *      NSP_F32, q / k / v pointing at the block's rows and
+ *      q_start / kv_start as given (bit-identical results).
+ *   accumulate = 1: each block's partial is merged into its out / lse in
+ *      place, as nsp_attn_fwd_accumulate does.
+ * The blocks' outputs must not share bytes (NSP_ERR_INVALID otherwise): a
+ * ring step's blocks have distinct query shards.  Rows of a block that see
+ * no key of it get out = 0, lse = -inf (accumulate: left unchanged).
+ * Workspace: at least nsp_attn_fwd_blocks_workspace_size(nblocks, blocks,
+ * ...) bytes.  Other arguments, kernel choice and errors as nsp_attn_fwd;
+ * ranges outside [0, T) are NSP_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t q_start, q_len, kv_start, kv_len;
+  void* out;
+  float* lse;
+} nsp_block_t;
+
+size_t nsp_attn_fwd_blocks_workspace_size(int32_t nblocks, const nsp_block_t* blocks, int32_t Hq,
+                                          int32_t Hkv, int32_t d);
+
+int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t nblocks,
+                            const nsp_block_t* blocks, int32_t Hq, int32_t Hkv, int32_t d,
+                            float scale, int32_t causal, int32_t io_dtype, int32_t accumulate,
+                            void* workspace, size_t workspace_bytes, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * nsp_attn_fwd without a workspace argument.  No page has a counterpart of
  * this entry point: it exists for callers that cannot allocate device
  * memory where they run attention (code inside a custom allocator or

@@ -153,6 +153,42 @@ def test_noalloc_rejects_on_host_like_fwd(lib):
     assert noalloc(1000, scale=0.0) == nsp.NSP_ERR_INVALID
 
 
+def test_fwd_blocks_rejects_on_host(lib):
+    """nsp_attn_fwd_blocks: block count, ranges inside [0, T), required and
+    aligned outputs, and outputs that share bytes are refused before any
+    launch."""
+    T, Hq, d = 1000, 4, 128
+    row = Hq * d * 4
+
+    def call(blocks, accumulate=0, nb=None):
+        arr = nsp._block_array(blocks)
+        ws = nsp.nsp_attn_fwd_blocks_workspace_size(blocks, Hq, 2, d) if blocks else 0
+        return lib.nsp_attn_fwd_blocks(A, A, A, A, 2, T, len(blocks) if nb is None else nb,
+                                       C.cast(arr, C.c_void_p), Hq, 2, d, 0.088, 1, nsp.NSP_BF16,
+                                       accumulate, A, max(ws, 1 << 20), None)
+
+    class P:                       # a fake device pointer the binding passes through
+        def __init__(self, addr):
+            self.addr = addr
+
+        def data_ptr(self):
+            return self.addr
+
+        def is_contiguous(self):
+            return True
+    out0, out1 = P(A), P(A + 200 * row)
+    ok = [(0, 100, 0, 100, out0, None), (100, 100, 0, 200, out1, None)]
+    assert nsp.nsp_attn_fwd_blocks_workspace_size(ok, Hq, 2, d) > 0
+    assert call(ok, nb=0) == nsp.NSP_ERR_INVALID
+    assert call(ok, nb=65) == nsp.NSP_ERR_INVALID
+    assert call([(0, 100, 950, 100, out0, None)]) == nsp.NSP_ERR_INVALID      # keys past T
+    assert call([(-1, 10, 0, 10, out0, None)]) == nsp.NSP_ERR_INVALID
+    assert call([(0, 100, 0, 100, out0, None)], accumulate=1) == nsp.NSP_ERR_INVALID  # lse needed
+    assert call([(0, 100, 0, 100, P(A + 4), None)]) == nsp.NSP_ERR_ALIGN
+    overlapping = [(0, 100, 0, 100, out0, None), (100, 100, 0, 200, P(A + 50 * row), None)]
+    assert call(overlapping) == nsp.NSP_ERR_INVALID
+
+
 def test_wait_timeout_setter(lib):
     """The bound of device waits: a process-wide setting, default restored by
     a negative value; each call returns the previous bound."""

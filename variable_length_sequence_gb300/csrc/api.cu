@@ -229,6 +229,114 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
   return NSP_OK;
 }
 
+namespace {
+
+// Host checks of a batched forward's block table: sizes, ranges inside
+// [0, T), aligned outputs, and no two blocks writing the same bytes.
+int32_t check_blocks(int64_t T, int32_t nblocks, const nsp_block_t* blocks, int32_t Hq,
+                     int32_t d, int32_t accumulate) {
+  if (nblocks < 1 || nblocks > kMaxBlocks || !blocks) return NSP_ERR_INVALID;
+  for (int32_t i = 0; i < nblocks; ++i) {
+    const nsp_block_t& b = blocks[i];
+    if (b.q_start < 0 || b.q_len < 0 || b.kv_start < 0 || b.kv_len < 0) return NSP_ERR_INVALID;
+    if (b.q_start + b.q_len > T || b.kv_start + b.kv_len > T) return NSP_ERR_INVALID;
+    if (b.q_len > 0 && (!b.out || (accumulate && !b.lse))) return NSP_ERR_INVALID;
+    if (!aligned16(b.out) || !aligned16(b.lse)) return NSP_ERR_ALIGN;
+  }
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+  };
+  for (int32_t i = 0; i < nblocks; ++i)
+    for (int32_t j = i + 1; j < nblocks; ++j) {
+      const nsp_block_t &a = blocks[i], &b = blocks[j];
+      const size_t oa = (size_t)a.q_len * Hq * d * 4, ob = (size_t)b.q_len * Hq * d * 4;
+      const size_t la = a.lse ? (size_t)a.q_len * Hq * 4 : 0, lb = b.lse ? (size_t)b.q_len * Hq * 4 : 0;
+      if (overlap(a.out, oa, b.out, ob) || overlap(a.lse, la, b.lse, lb) ||
+          overlap(a.out, oa, b.lse, lb) || overlap(a.lse, la, b.out, ob))
+        return NSP_ERR_INVALID;
+    }
+  return NSP_OK;
+}
+
+FwdBlocks table_of(int32_t nblocks, const nsp_block_t* blocks) {
+  FwdBlocks B;
+  B.n = nblocks;
+  B.global_rows = 1;
+  for (int32_t i = 0; i < nblocks; ++i) {
+    B.b[i].q_start = (int32_t)blocks[i].q_start; B.b[i].q_len = (int32_t)blocks[i].q_len;
+    B.b[i].kv_start = (int32_t)blocks[i].kv_start; B.b[i].kv_len = (int32_t)blocks[i].kv_len;
+    B.b[i].tile0 = 0; B.b[i].pad = 0;
+    B.b[i].out = blocks[i].out; B.b[i].lse = blocks[i].lse;
+  }
+  return B;
+}
+
+}  // namespace
+
+size_t nsp_attn_fwd_blocks_workspace_size(int32_t nblocks, const nsp_block_t* blocks, int32_t Hq,
+                                          int32_t Hkv, int32_t d) {
+  (void)Hq; (void)Hkv; (void)d;
+  if (nblocks < 1 || nblocks > kMaxBlocks || !blocks) return 0;
+  for (int32_t i = 0; i < nblocks; ++i)
+    if (blocks[i].q_len < 0 || blocks[i].kv_len < 0 || blocks[i].q_len > kMaxTokens ||
+        blocks[i].kv_len > kMaxTokens)
+      return 0;
+  FwdBlocks B = table_of(nblocks, blocks);
+  return fwd_ws_layout_blocks(B, kTileM).total;
+}
+
+int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
+                            const int32_t* cu_seqlens, int32_t ndoc, int64_t T, int32_t nblocks,
+                            const nsp_block_t* blocks, int32_t Hq, int32_t Hkv, int32_t d,
+                            float scale, int32_t causal, int32_t io_dtype, int32_t accumulate,
+                            void* workspace, size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = check_common(ndoc, Hq, Hkv, d, causal, io_dtype);
+  if (st != NSP_OK) return st;
+  if (T < 0 || (accumulate != 0 && accumulate != 1)) return NSP_ERR_INVALID;
+  if (T > kMaxTokens) return NSP_ERR_UNSUPPORTED;
+  if (!scale_ok(scale) || !cu_seqlens) return NSP_ERR_INVALID;
+  if (T > 0 && (!q || !k || !v)) return NSP_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cu_seqlens)) return NSP_ERR_ALIGN;
+  st = check_blocks(T, nblocks, blocks, Hq, d, accumulate);
+  if (st != NSP_OK) return st;
+  if (!workspace ||
+      workspace_bytes < nsp_attn_fwd_blocks_workspace_size(nblocks, blocks, Hq, Hkv, d))
+    return NSP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NSP_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  FwdBlocks B = table_of(nblocks, blocks);
+  const FwdWsLayout L = fwd_ws_layout_blocks(B, fwd_tile_rows(io_dtype, d, Hq, Hkv));
+  AttnProblem p;                       // whole-stream q / k / v; ranges and outputs per block
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = NSP_F32; p.out = nullptr; p.lse = nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.accumulate = accumulate;
+  if (launch_fwd_schedule(p, L, ws, s, &B) != cudaSuccess) return NSP_ERR_CUDA;
+  if (T == 0) return NSP_OK;
+  bool launched = false;
+  if (launch_attn_fwd_tc(p, L, ws, s, &launched, &B) != cudaSuccess) return NSP_ERR_CUDA;
+  if (launched) return NSP_OK;
+  // CUDA-core path (float32 I/O, d = 64): one launch per block, on pointers
+  // to the block's own rows
+  const size_t es = io_dtype == NSP_BF16 ? 2 : 4;
+  for (int32_t i = 0; i < nblocks; ++i) {
+    const nsp_block_t& b = blocks[i];
+    if (b.q_len == 0) continue;
+    AttnProblem pb = p;
+    pb.q = reinterpret_cast<const char*>(q) + (size_t)b.q_start * Hq * d * es;
+    pb.k = reinterpret_cast<const char*>(k) + (size_t)b.kv_start * Hkv * d * es;
+    pb.v = reinterpret_cast<const char*>(v) + (size_t)b.kv_start * Hkv * d * es;
+    pb.q_start = b.q_start; pb.q_len = b.q_len; pb.kv_start = b.kv_start; pb.kv_len = b.kv_len;
+    pb.out = b.out; pb.lse = b.lse;
+    if (launch_attn_fwd_simt(pb, s) != cudaSuccess) return NSP_ERR_CUDA;
+  }
+  return NSP_OK;
+}
+
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
                                    int32_t io_dtype) {
   if (T < 0 || Hq < 1 || Hkv < 1 || d < 1) return 0;

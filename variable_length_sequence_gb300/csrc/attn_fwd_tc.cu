@@ -78,8 +78,20 @@ struct Item {
   int g;          // key/value head
   int j_lo;       // first KV tile
   int n_kv;       // number of KV tiles (0: no key visible; -1: stop)
-  int pad[3];
+  int blk;        // block of the call (batched forward; 0 otherwise)
+  int pad[2];
 };
+
+// Block of scheduled tile t: the largest index whose tile0 <= t (a block
+// without tiles shares tile0 with the next one).
+__device__ __forceinline__ int block_of(const FwdBlocks& B, int t) {
+  int lo = 0, hi = B.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (B.b[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 struct __align__(1024) Smem {
   uint8_t q[2][kTileBytes];
@@ -166,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnProblem p,
-                       const int2* __restrict__ tiles, const int* __restrict__ order) {
+                       const int2* __restrict__ tiles, const int* __restrict__ order,
+                       const __grid_constant__ FwdBlocks blks) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -230,12 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok) {
         const int idx = atomicAdd(&hdr->counter, 1);
         Item it;
-        it.qtile = -1; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
+        it.qtile = -1; it.h0 = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1; it.blk = 0;
         if (idx < n_items) {
           const int qt = order[idx / per_tile];
           const int sub = idx - (idx / per_tile) * per_tile;
           const int2 tr = tiles[qt];
-          it.qtile = qt;
+          it.blk = block_of(blks, qt);
+          it.qtile = qt - blks.b[it.blk].tile0;             // tile within its block
           it.h0 = pair_tiles ? sub : 2 * sub;
           it.g = it.h0 / G;
           it.j_lo = tr.x;
@@ -260,7 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
         // packed layout: map [q_len, Hq d]; head groups: map [P q_len, (Hq/P) d],
-        // head h at column block h % (Hq/P) of rows (h / (Hq/P)) q_len + row
+        // head h at column block h % (Hq/P) of rows (h / (Hq/P)) q_len + row;
+        // a batched call's maps span the whole stream (rows = global ids)
+        const FwdBlock& bk = blks.b[it.blk];
+        const int q_row_base = blks.global_rows ? bk.q_start : 0;
+        const int k_row_base = blks.global_rows ? bk.kv_start : 0;
         const int hpg = p.Hq / p.q_groups;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -269,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // are never stored)
           const int head = pair_tiles ? it.h0 : it.h0 + t;
           const int grp = head / hpg;
-          const int row0 = (int)(grp * p.q_len) + it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
+          const int row0 = q_row_base + grp * bk.q_len + it.qtile * tile_rows +
+                           (pair_tiles ? t * BM : 0);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
             tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full,
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = kv_count % NSTAGE, use = kv_count / NSTAGE;
-          const int key0 = (it.j_lo + jj) * BN;
+          const int key0 = k_row_base + (it.j_lo + jj) * BN;
           if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, wc, hdr)) {
             ok = false;
             break;
@@ -389,9 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_tm = tmem + lane_base + col_s(t);
     const uint32_t o_tm = tmem + lane_base + col_o(t);
     const float sl2 = p.scale * kLog2e;
-    const int64_t kv_end = p.kv_start + p.kv_len;
     uint32_t it_count = 0, s_count = 0, o_count = 0;
-    TO* const out = reinterpret_cast<TO*>(p.out);
     if (!p.accumulate) {
       // Query tiles that see no key of the range (listed last by the
       // schedule): out = 0 and lse = -inf, written by the softmax warps of
@@ -407,15 +424,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = (int)(u / (p.Hq * groups));
         const int rem = (int)(u - (int64_t)e * p.Hq * groups);
         const int hz = rem / groups;
-        const int64_t r0 = (int64_t)order[hdr->n_nonempty + e] * tile_rows + (rem % groups) * 32;
+        const int tile = order[hdr->n_nonempty + e];
+        const FwdBlock& bz = blks.b[block_of(blks, tile)];
+        TO* const out = reinterpret_cast<TO*>(bz.out);
+        const int64_t r0 = (int64_t)(tile - bz.tile0) * tile_rows + (rem % groups) * 32;
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = r0 + rr + sub;
-          if (grow < p.q_len)
+          if (grow < bz.q_len)
             reinterpret_cast<uint4*>(out + qo_offset(p, grow, hz))[part] = make_uint4(0, 0, 0, 0);
         }
-        if (p.lse != nullptr && r0 + lane < p.q_len)
-          p.lse[(int64_t)hz * p.q_len + r0 + lane] = -INFINITY;
+        if (bz.lse != nullptr && r0 + lane < bz.q_len)
+          bz.lse[(int64_t)hz * bz.q_len + r0 + lane] = -INFINITY;
       }
     }
     while (true) {
@@ -426,19 +446,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.n_kv < 0) break;
+      // the item's block: its ranges (global ids) and outputs
+      const FwdBlock& bk = blks.b[it.blk];
+      const int64_t q_len = bk.q_len, q_start = bk.q_start, kv_start = bk.kv_start;
+      const int64_t kv_end = kv_start + bk.kv_len;
+      TO* const out = reinterpret_cast<TO*>(bk.out);
+      float* const lse_out = bk.lse;
       const int h = pair_tiles ? it.h0 : it.h0 + t;
       // first row of this role's 128-row tile, query-range relative
       const int64_t tile_base = (int64_t)it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
       const int64_t row = tile_base + r;
-      const bool valid = row < p.q_len;
+      const bool valid = row < q_len;
       int lo = 0, hi = 0;                                      // key-range relative [lo, hi)
       if (valid) {
-        const int64_t tg = p.q_start + row;
+        const int64_t tg = q_start + row;
         const int b = doc_of(p.cu, p.ndoc, tg);
-        const int64_t glo = max((int64_t)__ldg(p.cu + b), p.kv_start);
+        const int64_t glo = max((int64_t)__ldg(p.cu + b), kv_start);
         const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1), kv_end);
-        lo = (int)(glo - p.kv_start);
-        hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
+        lo = (int)(glo - kv_start);
+        hi = (int)max(ghi - kv_start, glo - kv_start);
       }
       float m = -INFINITY, l = 0.f;
       // Ring accumulation: a row that sees a key of this block (acc_row)
@@ -453,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (sizeof(TO) == 4) {
         if (p.accumulate && it.n_kv > 0) {
           float la2 = -INFINITY;
-          if (acc_row) la2 = p.lse[(int64_t)h * p.q_len + row] * kLog2e;
+          if (acc_row) la2 = lse_out[(int64_t)h * q_len + row] * kLog2e;
           const float4* arow = reinterpret_cast<const float4*>(out + qo_offset(p, row, h));
           {
             // the whole 512-byte row in flight at once (one DRAM round trip;
@@ -584,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
               const int64_t grow = tile_base + wq * 32 + 8 * i + (lane >> 2);
-              if (grow < p.q_len && (!p.accumulate || wpr[i] != 0.f))
+              if (grow < q_len && (!p.accumulate || wpr[i] != 0.f))
                 *reinterpret_cast<float2*>(out + qo_offset(p, grow, h) + c * 32 +
                                            8 * ((k >> 1) & 3) + 2 * (lane & 3)) =
                     make_float2(__uint_as_float(x[2 * k]) * wpr[i],
@@ -609,12 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = tile_base + wq * 32 + rr + sub;
-          if (grow < p.q_len)
+          if (grow < q_len)
             reinterpret_cast<uint4*>(out + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
         }
       }
-      if (valid && p.lse != nullptr && (!p.accumulate || acc_row))
-        p.lse[(int64_t)h * p.q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid && lse_out != nullptr && (!p.accumulate || acc_row))
+        lse_out[(int64_t)h * q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -657,7 +683,8 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 
 template <typename TO>
 cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, cudaStream_t s,
-                         const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv) {
+                         const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const FwdBlocks& B) {
   auto kern = attn_fwd_tc_kernel<TO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
@@ -665,7 +692,7 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
   const int grid = persistent_grid();
   e = launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, mq, mk, mv, p,
                        reinterpret_cast<const int2*>(ws + L.tiles),
-                       reinterpret_cast<const int*>(ws + L.order));
+                       reinterpret_cast<const int*>(ws + L.order), B);
   count_launches(1);
   count_path(true);
   if (e != cudaSuccess) return e;
@@ -675,7 +702,7 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
 }  // namespace
 
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
-                               cudaStream_t s, bool* launched) {
+                               cudaStream_t s, bool* launched, const FwdBlocks* blocks) {
   *launched = false;
   if (p.io_dtype != NSP_BF16 || p.d != HD) return cudaSuccess;
   if (p.q_len <= 0 || p.kv_len <= 0) return cudaSuccess;
@@ -687,8 +714,9 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
   *launched = true;
   AttnProblem pk = p;
   pk.wait_budget = wait_budget_cycles();
-  return pk.out_dtype == NSP_F32 ? launch_typed<float>(pk, L, ws, s, mq, mk, mv)
-                                 : launch_typed<__nv_bfloat16>(pk, L, ws, s, mq, mk, mv);
+  const FwdBlocks B = blocks ? *blocks : single_block(p);
+  return pk.out_dtype == NSP_F32 ? launch_typed<float>(pk, L, ws, s, mq, mk, mv, B)
+                                 : launch_typed<__nv_bfloat16>(pk, L, ws, s, mq, mk, mv, B);
 }
 
 }  // namespace nsp

@@ -53,6 +53,26 @@ inline int32_t fwd_tile_rows(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hk
   return (io_dtype == NSP_BF16 && d == 128 && Hkv > 0 && ((Hq / Hkv) & 1)) ? 2 * kTileM : kTileM;
 }
 
+// One (query range, key range) block of a forward call, and the table of a
+// call's blocks, passed to the schedule and attention kernels by value.
+// The single-range entry points use one block whose q / k / v pointers are
+// the block's own first rows (global_rows = 0); the batched entry point
+// (nsp_attn_fwd_blocks) addresses whole-stream q / k / v by global token ids
+// (global_rows = 1).  Token ids fit in int32 (at most 2^30 tokens).
+constexpr int kMaxBlocks = 64;
+struct FwdBlock {
+  int32_t q_start, q_len, kv_start, kv_len;   // global token ids
+  int32_t tile0;                              // first scheduled query tile of the block
+  int32_t pad;
+  void* out;                                  // [q_len, Hq, d]
+  float* lse;                                 // [Hq, q_len] or null
+};
+struct FwdBlocks {
+  int32_t n;
+  int32_t global_rows;
+  FwdBlock b[kMaxBlocks];
+};
+
 inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t tile_rows = kTileM) {
   FwdWsLayout L;
   L.tile_rows = tile_rows;
@@ -63,6 +83,19 @@ inline FwdWsLayout fwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t tile_row
   L.order = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_qtiles, 256);
   L.hist = off;   off = align_up(off + sizeof(int32_t) * (size_t)(L.n_kvtiles + 2), 256);
   L.total = off;
+  return L;
+}
+
+// Layout of a batched forward: the query tiles of every block, one sort;
+// fills in each block's tile0.
+inline FwdWsLayout fwd_ws_layout_blocks(FwdBlocks& B, int32_t tile_rows) {
+  int64_t n_q = 0, max_kv = 0;
+  for (int i = 0; i < B.n; ++i) {
+    B.b[i].tile0 = (int32_t)n_q;
+    n_q += ceil_div(B.b[i].q_len, tile_rows);
+    max_kv = B.b[i].kv_len > max_kv ? B.b[i].kv_len : max_kv;
+  }
+  FwdWsLayout L = fwd_ws_layout(n_q * tile_rows, max_kv, tile_rows);
   return L;
 }
 
@@ -134,13 +167,17 @@ struct AttnProblem {
 };
 
 // ---- launchers implemented in the .cu files (return cudaError_t) ----
+// The forward's blocks: `blocks` (n >= 1), or when null the one block
+// [q_start, +q_len) x [kv_start, +kv_len) of p with p's out and lse.
 cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
-                                cudaStream_t s);
+                                cudaStream_t s, const FwdBlocks* blocks = nullptr);
 cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
                                  cudaStream_t s);
 cudaError_t launch_attn_fwd_simt(const AttnProblem& p, cudaStream_t s);
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
-                               cudaStream_t s, bool* launched);
+                               cudaStream_t s, bool* launched, const FwdBlocks* blocks = nullptr);
+// The single block of a single-range call.
+FwdBlocks single_block(const AttnProblem& p);
 cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const void* dout,
                                  const float* lse, void* dq, void* dk, void* dv,
                                  const BwdWsLayout& L, char* ws, cudaStream_t s);

@@ -50,9 +50,12 @@ struct SchedArgs {
   int32_t tile_rows;   // mode 0: rows of a scheduled query tile (128 or 256)
   WsHeader* hdr;
   int32_t second;      // write counters into counter2 / n_items2
+  // mode 0: the blocks whose query tiles are listed; tile i belongs to the
+  // block with the largest tile0 <= i (the range fields above are unused)
+  FwdBlocks blks;
 };
 
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_constant__ SchedArgs a) {
   extern __shared__ int s_hist_dyn[];       // n_buckets ints when they fit
   __shared__ int s_bad;
   __shared__ int s_max;
@@ -67,7 +70,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     if (tid == 0) {
       if (a.ndoc < 1 || a.cu[0] != 0) s_bad = 1;
       const int64_t total = a.cu[a.ndoc];
-      if (total < a.q_start + a.q_len || total < a.kv_start + a.kv_len) s_bad = 1;
+      if (a.mode == 0) {
+        for (int bi = 0; bi < a.blks.n; ++bi) {
+          const FwdBlock& B = a.blks.b[bi];
+          if (total < (int64_t)B.q_start + B.q_len || total < (int64_t)B.kv_start + B.kv_len)
+            s_bad = 1;
+        }
+      } else if (total < a.q_start + a.q_len || total < a.kv_start + a.kv_len) {
+        s_bad = 1;
+      }
     }
     for (int i = tid; i < a.ndoc; i += kSchedThreads)
       if (a.cu[i] > a.cu[i + 1]) s_bad = 1;
@@ -94,14 +105,23 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   for (int i = tid; i < a.n_tiles; i += kSchedThreads) {
     int lo_t = 0, hi_t = -1;
     if (a.mode == 0) {
-      const int64_t r0 = a.q_start + (int64_t)i * a.tile_rows;
-      const int64_t r1 = min(r0 + a.tile_rows, q_end) - 1;     // last row of the tile
+      // the block of tile i: the largest index whose tile0 <= i (blocks
+      // without tiles share tile0 with the next one)
+      int bl = 0, bh = a.blks.n - 1;
+      while (bl < bh) {
+        const int mid = (bl + bh + 1) >> 1;
+        if (a.blks.b[mid].tile0 <= i) bl = mid; else bh = mid - 1;
+      }
+      const FwdBlock& B = a.blks.b[bl];
+      const int64_t ks = B.kv_start, ke = (int64_t)B.kv_start + B.kv_len;
+      const int64_t r0 = (int64_t)B.q_start + (int64_t)(i - B.tile0) * a.tile_rows;
+      const int64_t r1 = min(r0 + a.tile_rows, (int64_t)B.q_start + B.q_len) - 1;  // last row
       const int b0 = doc_of(a.cu, a.ndoc, r0), b1 = doc_of(a.cu, a.ndoc, r1);
-      const int64_t lo = max((int64_t)a.cu[b0], a.kv_start);
-      const int64_t hi = min(a.causal ? r1 + 1 : (int64_t)a.cu[b1 + 1], kv_end);  // exclusive
+      const int64_t lo = max((int64_t)a.cu[b0], ks);
+      const int64_t hi = min(a.causal ? r1 + 1 : (int64_t)a.cu[b1 + 1], ke);  // exclusive
       if (hi > lo) {
-        lo_t = (int)((lo - a.kv_start) / a.gran);
-        hi_t = (int)((hi - 1 - a.kv_start) / a.gran);
+        lo_t = (int)((lo - ks) / a.gran);
+        hi_t = (int)((hi - 1 - ks) / a.gran);
       }
     } else {
       const int64_t k0 = a.kv_start + (int64_t)i * kTileN;
@@ -174,9 +194,21 @@ size_t sched_smem(const SchedArgs& a) {
 
 }  // namespace
 
+FwdBlocks single_block(const AttnProblem& p) {
+  FwdBlocks B;
+  B.n = 1;
+  B.global_rows = 0;
+  B.b[0].q_start = (int32_t)p.q_start; B.b[0].q_len = (int32_t)p.q_len;
+  B.b[0].kv_start = (int32_t)p.kv_start; B.b[0].kv_len = (int32_t)p.kv_len;
+  B.b[0].tile0 = 0; B.b[0].pad = 0;
+  B.b[0].out = p.out; B.b[0].lse = p.lse;
+  return B;
+}
+
 cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
-                                cudaStream_t s) {
+                                cudaStream_t s, const FwdBlocks* blocks) {
   SchedArgs a;
+  a.blks = blocks ? *blocks : single_block(p);
   a.gran = kTileN;
   a.tile_rows = L.tile_rows;
   a.cu = p.cu; a.ndoc = p.ndoc;
@@ -199,6 +231,7 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
   a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub; a.tile_rows = kTileM;
+  a.blks = single_block(p);
   a.tiles = reinterpret_cast<int2*>(ws + L.qtiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.qorder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.qhist);

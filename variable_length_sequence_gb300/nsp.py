@@ -40,6 +40,9 @@ _SIGNATURES = {
                                        _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_headgroups": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                        _f32, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "nsp_attn_fwd_blocks_workspace_size": (_sz, [_i32, _vp, _i32, _i32, _i32]),
+    "nsp_attn_fwd_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _i32, _i32, _i32, _f32,
+                                   _i32, _i32, _i32, _vp, _sz, _vp]),
     "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
     "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
@@ -68,6 +71,12 @@ _SIGNATURES = {
     "nsp_attn_cost": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                              _vp]),
 }
+
+
+class Block(C.Structure):
+    """nsp_block_t: one (query range, key range) block of a batched forward."""
+    _fields_ = [("q_start", C.c_int64), ("q_len", C.c_int64), ("kv_start", C.c_int64),
+                ("kv_len", C.c_int64), ("out", C.c_void_p), ("lse", C.c_void_p)]
 
 
 class AttnCost(C.Structure):
@@ -145,6 +154,31 @@ def _check(fn: str, st: int) -> int:
 
 def nsp_attn_fwd_workspace_size(q_len: int, kv_len: int, Hq: int, Hkv: int, d: int) -> int:
     return int(load().nsp_attn_fwd_workspace_size(q_len, kv_len, Hq, Hkv, d))
+
+
+def _block_array(blocks):
+    """blocks: sequence of (q_start, q_len, kv_start, kv_len, out, lse)."""
+    arr = (Block * len(blocks))()
+    for i, (qs, ql, ks, kl, out, lse) in enumerate(blocks):
+        arr[i] = Block(int(qs), int(ql), int(ks), int(kl), _ptr(out), _ptr(lse))
+    return arr
+
+
+def nsp_attn_fwd_blocks_workspace_size(blocks, Hq: int, Hkv: int, d: int) -> int:
+    arr = _block_array(blocks)
+    return int(load().nsp_attn_fwd_blocks_workspace_size(len(blocks), C.cast(arr, C.c_void_p),
+                                                         int(Hq), int(Hkv), int(d)))
+
+
+def nsp_attn_fwd_blocks(q, k, v, cu_seqlens, ndoc, T, blocks, Hq, Hkv, d, scale, causal,
+                        accumulate, workspace, stream=None) -> int:
+    arr = _block_array(blocks)
+    st = load().nsp_attn_fwd_blocks(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), int(ndoc),
+                                    int(T), len(blocks), C.cast(arr, C.c_void_p), int(Hq),
+                                    int(Hkv), int(d), float(scale), int(bool(causal)), _dtype(q),
+                                    int(bool(accumulate)), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check("nsp_attn_fwd_blocks", st)
 
 
 def nsp_attn_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int, io_dtype: int = NSP_BF16) -> int:
@@ -401,6 +435,22 @@ def attn_fwd_accumulate(q, k, v, cu_seqlens, acc, lse_acc, scale=None, causal=Tr
                             kv_start, kv_len, Hq, Hkv, d, scale, causal, acc, lse_acc,
                             workspace, stream)
     return acc, lse_acc
+
+
+def attn_fwd_blocks(q, k, v, cu_seqlens, blocks, scale=None, causal=True, accumulate=False,
+                    workspace=None, stream=None):
+    """Batched blocks of the whole stream q [T, Hq, d], k/v [T, Hkv, d]:
+    blocks = [(q_start, q_len, kv_start, kv_len, out, lse), ...] with float32
+    out [q_len, Hq, d] and lse [Hq, q_len] written (accumulate=False) or
+    merged into (accumulate=True)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_fwd_blocks_workspace_size(blocks, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q.device)
+    nsp_attn_fwd_blocks(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, T, blocks, Hq, Hkv, d, scale,
+                        causal, accumulate, workspace, stream)
 
 
 def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, workspace=None,
