@@ -173,7 +173,12 @@ __device__ __forceinline__ void store_row_chunk<float>(float* dst, const uint32_
   }
 }
 
-template <typename TO>
+// PAIR: an item is two adjacent tiles of one head (odd Hq / Hkv) instead of
+// one tile and two heads.  MULTI: the batched call, ranges and outputs per
+// block of the table and q / k / v rows addressed by global token ids;
+// otherwise the single range and outputs of p.  Both are compile-time so the
+// common case (one range, head pairs) carries none of their bookkeeping.
+template <typename TO, bool PAIR, bool MULTI>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -226,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
   // odd G (multi-head attention among them): an item is two adjacent
   // 128-row tiles of one head instead of one tile and two heads
-  const bool pair_tiles = (G & 1) != 0;
+  constexpr bool pair_tiles = PAIR;
   const int per_tile = pair_tiles ? p.Hq : (p.Hq >> 1);         // items per scheduled tile
-  const int tile_rows = pair_tiles ? 2 * BM : BM;
+  constexpr int tile_rows = pair_tiles ? 2 * BM : BM;
   // query tiles no key of the range reaches are not work items: the softmax
   // warps zero-fill them up front (or, accumulating, leave them alone)
   const int n_items = hdr->n_nonempty * per_tile;
@@ -248,8 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qt = order[idx / per_tile];
           const int sub = idx - (idx / per_tile) * per_tile;
           const int2 tr = tiles[qt];
-          it.blk = block_of(blks, qt);
-          it.qtile = qt - blks.b[it.blk].tile0;             // tile within its block
+          if constexpr (MULTI) {
+            it.blk = block_of(blks, qt);
+            it.qtile = qt - blks.b[it.blk].tile0;           // tile within its block
+          } else {
+            it.qtile = qt;
+          }
           it.h0 = pair_tiles ? sub : 2 * sub;
           it.g = it.h0 / G;
           it.j_lo = tr.x;
@@ -276,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed layout: map [q_len, Hq d]; head groups: map [P q_len, (Hq/P) d],
         // head h at column block h % (Hq/P) of rows (h / (Hq/P)) q_len + row;
         // a batched call's maps span the whole stream (rows = global ids)
-        const FwdBlock& bk = blks.b[it.blk];
-        const int q_row_base = blks.global_rows ? bk.q_start : 0;
-        const int k_row_base = blks.global_rows ? bk.kv_start : 0;
+        const int q_row_base = MULTI ? blks.b[it.blk].q_start : 0;
+        const int k_row_base = MULTI ? blks.b[it.blk].kv_start : 0;
+        const int q_len_b = MULTI ? blks.b[it.blk].q_len : (int)p.q_len;
         const int hpg = p.Hq / p.q_groups;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // are never stored)
           const int head = pair_tiles ? it.h0 : it.h0 + t;
           const int grp = head / hpg;
-          const int row0 = q_row_base + grp * bk.q_len + it.qtile * tile_rows +
+          const int row0 = q_row_base + grp * q_len_b + it.qtile * tile_rows +
                            (pair_tiles ? t * BM : 0);
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb)
@@ -425,17 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rem = (int)(u - (int64_t)e * p.Hq * groups);
         const int hz = rem / groups;
         const int tile = order[hdr->n_nonempty + e];
-        const FwdBlock& bz = blks.b[block_of(blks, tile)];
-        TO* const out = reinterpret_cast<TO*>(bz.out);
-        const int64_t r0 = (int64_t)(tile - bz.tile0) * tile_rows + (rem % groups) * 32;
+        const int bz = MULTI ? block_of(blks, tile) : 0;
+        TO* const out = reinterpret_cast<TO*>(MULTI ? blks.b[bz].out : p.out);
+        float* const lse_z = MULTI ? blks.b[bz].lse : p.lse;
+        const int64_t q_len_z = MULTI ? (int64_t)blks.b[bz].q_len : p.q_len;
+        const int64_t r0 = (int64_t)(tile - (MULTI ? blks.b[bz].tile0 : 0)) * tile_rows +
+                           (rem % groups) * 32;
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = r0 + rr + sub;
-          if (grow < bz.q_len)
+          if (grow < q_len_z)
             reinterpret_cast<uint4*>(out + qo_offset(p, grow, hz))[part] = make_uint4(0, 0, 0, 0);
         }
-        if (bz.lse != nullptr && r0 + lane < bz.q_len)
-          bz.lse[(int64_t)hz * bz.q_len + r0 + lane] = -INFINITY;
+        if (lse_z != nullptr && r0 + lane < q_len_z)
+          lse_z[(int64_t)hz * q_len_z + r0 + lane] = -INFINITY;
       }
     }
     while (true) {
@@ -446,20 +458,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.n_kv < 0) break;
-      // the item's block: its ranges (global ids) and outputs
-      const FwdBlock& bk = blks.b[it.blk];
-      const int64_t q_len = bk.q_len, q_start = bk.q_start, kv_start = bk.kv_start;
-      const int64_t kv_end = kv_start + bk.kv_len;
-      TO* const out = reinterpret_cast<TO*>(bk.out);
-      float* const lse_out = bk.lse;
+      // the item's ranges (global ids) and outputs: its block's (batched
+      // call) or the call's, read where they are used (kernel parameters,
+      // so no register holds them across the tile loop)
+      const int blk = it.blk;
+#define NSP_BLK(field, whole) (MULTI ? (int64_t)blks.b[blk].field : (int64_t)p.whole)
+#define NSP_OUT (reinterpret_cast<TO*>(MULTI ? blks.b[blk].out : p.out))
+#define NSP_LSE (MULTI ? blks.b[blk].lse : p.lse)
       const int h = pair_tiles ? it.h0 : it.h0 + t;
       // first row of this role's 128-row tile, query-range relative
       const int64_t tile_base = (int64_t)it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
       const int64_t row = tile_base + r;
-      const bool valid = row < q_len;
+      const bool valid = row < NSP_BLK(q_len, q_len);
       int lo = 0, hi = 0;                                      // key-range relative [lo, hi)
       if (valid) {
-        const int64_t tg = q_start + row;
+        const int64_t kv_start = NSP_BLK(kv_start, kv_start);
+        const int64_t kv_end = kv_start + NSP_BLK(kv_len, kv_len);
+        const int64_t tg = NSP_BLK(q_start, q_start) + row;
         const int b = doc_of(p.cu, p.ndoc, tg);
         const int64_t glo = max((int64_t)__ldg(p.cu + b), kv_start);
         const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1), kv_end);
@@ -479,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (sizeof(TO) == 4) {
         if (p.accumulate && it.n_kv > 0) {
           float la2 = -INFINITY;
-          if (acc_row) la2 = lse_out[(int64_t)h * q_len + row] * kLog2e;
-          const float4* arow = reinterpret_cast<const float4*>(out + qo_offset(p, row, h));
+          if (acc_row) la2 = NSP_LSE[(int64_t)h * NSP_BLK(q_len, q_len) + row] * kLog2e;
+          const float4* arow = reinterpret_cast<const float4*>(NSP_OUT + qo_offset(p, row, h));
           {
             // the whole 512-byte row in flight at once (one DRAM round trip;
             // S's registers are not live yet)
@@ -584,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- epilogue: out = O / l, lse = (m + log2 l) ln 2
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      TO* dst = out + qo_offset(p, row, h);
+      TO* dst = NSP_OUT + qo_offset(p, row, h);
       if (it.n_kv > 0) {
         if (!mbar_wait_warp(&sm.o_full[t], o_count & 1, wc, hdr)) break;
         ++o_count;
@@ -610,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
               const int64_t grow = tile_base + wq * 32 + 8 * i + (lane >> 2);
-              if (grow < q_len && (!p.accumulate || wpr[i] != 0.f))
-                *reinterpret_cast<float2*>(out + qo_offset(p, grow, h) + c * 32 +
+              if (grow < NSP_BLK(q_len, q_len) && (!p.accumulate || wpr[i] != 0.f))
+                *reinterpret_cast<float2*>(NSP_OUT + qo_offset(p, grow, h) + c * 32 +
                                            8 * ((k >> 1) & 3) + 2 * (lane & 3)) =
                     make_float2(__uint_as_float(x[2 * k]) * wpr[i],
                                 __uint_as_float(x[2 * k + 1]) * wpr[i]);
@@ -635,12 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += kRowsPerPass) {
           const int64_t grow = tile_base + wq * 32 + rr + sub;
-          if (grow < q_len)
-            reinterpret_cast<uint4*>(out + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
+          if (grow < NSP_BLK(q_len, q_len))
+            reinterpret_cast<uint4*>(NSP_OUT + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
         }
       }
-      if (valid && lse_out != nullptr && (!p.accumulate || acc_row))
-        lse_out[(int64_t)h * q_len + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid && NSP_LSE != nullptr && (!p.accumulate || acc_row))
+        NSP_LSE[(int64_t)h * NSP_BLK(q_len, q_len) + row] =
+            l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+#undef NSP_BLK
+#undef NSP_OUT
+#undef NSP_LSE
     }
   }
 
@@ -681,11 +700,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TO>
+template <typename TO, bool PAIR, bool MULTI>
 cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, cudaStream_t s,
                          const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdBlocks& B) {
-  auto kern = attn_fwd_tc_kernel<TO>;
+  auto kern = attn_fwd_tc_kernel<TO, PAIR, MULTI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -715,8 +734,15 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
   AttnProblem pk = p;
   pk.wait_budget = wait_budget_cycles();
   const FwdBlocks B = blocks ? *blocks : single_block(p);
-  return pk.out_dtype == NSP_F32 ? launch_typed<float>(pk, L, ws, s, mq, mk, mv, B)
-                                 : launch_typed<__nv_bfloat16>(pk, L, ws, s, mq, mk, mv, B);
+  const bool pair = ((p.Hq / p.Hkv) & 1) != 0;
+  if (blocks != nullptr)            // batched blocks: float32 partials or accumulators
+    return pair ? launch_typed<float, true, true>(pk, L, ws, s, mq, mk, mv, B)
+                : launch_typed<float, false, true>(pk, L, ws, s, mq, mk, mv, B);
+  if (pk.out_dtype == NSP_F32)
+    return pair ? launch_typed<float, true, false>(pk, L, ws, s, mq, mk, mv, B)
+                : launch_typed<float, false, false>(pk, L, ws, s, mq, mk, mv, B);
+  return pair ? launch_typed<__nv_bfloat16, true, false>(pk, L, ws, s, mq, mk, mv, B)
+              : launch_typed<__nv_bfloat16, false, false>(pk, L, ws, s, mq, mk, mv, B);
 }
 
 }  // namespace nsp
