@@ -84,7 +84,7 @@ int64_t nsp_kernel_launches(void);
 /* Number of attention kernels (forward, dK/dV and dQ kernels) this library
  * has launched in this process on the tensor-core path (tensor_core = 1:
  * tcgen05, TMEM, TMA) or on the CUDA-core path (tensor_core = 0: float32
- * I/O, d = 64, odd head groupings, or no tensor-map support in the driver).
+ * I/O, d = 64, or no tensor-map support in the driver).
  * Lets a caller see which path its calls took. */
 int64_t nsp_path_launches(int32_t tensor_core);
 
@@ -129,6 +129,13 @@ int64_t nsp_set_wait_timeout_cycles(int64_t cycles);
  *   out_dtype (NSP_F32 or io_dtype); lse device float32 [Hq, q_len] (may be
  *   NULL when not needed); workspace device, at least
  *   nsp_attn_fwd_workspace_size(...) bytes, contents need no initialisation.
+ *
+ * Kernel choice: bf16 with d = 128 runs on the tensor cores (tcgen05, TMEM,
+ * TMA), any Hq / Hkv (an even ratio pairs two query heads of a KV group per
+ * work item, an odd one, multi-head attention among them, pairs two
+ * adjacent query tiles of one head).  float32 I/O and d = 64 run on the
+ * CUDA cores: a correct but much slower path (nsp_path_launches tells which
+ * ran).
  * ---------------------------------------------------------------------- */
 size_t nsp_attn_fwd_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t Hkv,
                                    int32_t d);
@@ -200,7 +207,7 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
  * arithmetic), without either permutation pass: the kernels address the
  * grouped rows directly (TMA coordinates of a [P T, (Hq/P) d] map).
  * P must divide Hq; P T must fit in int32.  Kernel choice as nsp_attn_fwd
- * (tensor cores for bf16, d = 128, even Hq / Hkv; CUDA cores otherwise).
+ * (tensor cores for bf16, d = 128; CUDA cores otherwise).
  * Other arguments and errors: as nsp_attn_fwd
  * with q_start = kv_start = 0, q_len = kv_len = T (workspace sized by
  * nsp_attn_fwd_workspace_size(T, T, ...)); a bad P is NSP_ERR_INVALID.
