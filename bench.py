@@ -381,31 +381,26 @@ class Problem:
 
     def ring_bwd(self, stream):
         """The ring backward: every causal (q-shard, kv-shard) block's dq/dk/dv
-        added into float32 accumulators (zeroed first) by nsp_attn_bwd_accumulate,
-        with the forward's out and lse of the query shard."""
+        added into whole-stream float32 accumulators (zeroed first) in one
+        nsp_attn_bwd_blocks call, with the forward's out and lse."""
         n = self.T // RING_SHARDS
         if not hasattr(self, "_rb"):
             dev = self.q.device
+            ranges = [(self.bounds[qs][0], n, self.bounds[ks][0], n) for qs, ks, _ in self.ring_pairs]
             self._rb = {
                 "dq": torch.zeros((self.T, self.Hq, self.d), dtype=torch.float32, device=dev),
                 "dk": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
                 "dv": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
-                "lse": [torch.empty((self.Hq, n), dtype=torch.float32, device=dev)
-                        for _ in range(RING_SHARDS)],
-                "ws": torch.empty(self.nsp.nsp_attn_bwd_accumulate_workspace_size(
-                    n, n, self.Hq, self.Hkv, self.d), dtype=torch.uint8, device=dev)}
-            for qs, (qa, qb) in enumerate(self.bounds):
-                self._rb["lse"][qs].copy_(self.lse[:, qa:qb])
+                "ranges": ranges,
+                "ws": torch.empty(self.nsp.nsp_attn_bwd_blocks_workspace_size(
+                    self.T, ranges, self.Hq, self.Hkv, self.d), dtype=torch.uint8, device=dev)}
         rb = self._rb
         for t in (rb["dq"], rb["dk"], rb["dv"]):
             t.zero_()
-        for qs, ks, _ in self.ring_pairs:
-            qa, ka = self.bounds[qs][0], self.bounds[ks][0]
-            self.nsp.nsp_attn_bwd_accumulate(
-                self.q[qa:qa + n], self.k[ka:ka + n], self.v[ka:ka + n], self.out[qa:qa + n],
-                self.dout[qa:qa + n], rb["lse"][qs], self.cu, len(self.w.lengths), qa, n, ka, n,
-                self.Hq, self.Hkv, self.d, self.scale, True, rb["dq"][qa:qa + n],
-                rb["dk"][ka:ka + n], rb["dv"][ka:ka + n], rb["ws"], stream)
+        self.nsp.nsp_attn_bwd_blocks(self.q, self.k, self.v, self.out, self.dout, self.lse, self.cu,
+                                     len(self.w.lengths), self.T, rb["ranges"], self.Hq, self.Hkv,
+                                     self.d, self.scale, True, rb["dq"], rb["dk"], rb["dv"],
+                                     rb["ws"], stream)
 
     def fwd_headgroups(self, stream):
         """The forward on q in the all-to-all's receive layout [P][T][Hq/P][d]
@@ -817,8 +812,8 @@ def time_extra_legs(prob, stream, flush, K, peaks):
     receive layout; fwd_mha, the forward with multi-head attention (as many
     key/value heads as query heads);
     ring_accumulate, the ring legs with the merge fused into attention, and
-    ring_bwd, the ring backward (its three float32 accumulators are zeroed
-    inside the timed region, by PyTorch)."""
+    ring_bwd, the ring backward in one batched call (its three float32
+    accumulators are zeroed inside the timed region, by PyTorch)."""
     reps = max(3, min(K, 50))
     extra = {}
     if prob.perm is not None and prob.fwd_flop > 0:

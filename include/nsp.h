@@ -260,6 +260,43 @@ int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
                             void* workspace, size_t workspace_bytes, nsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Batched ring-block backward: the gradient contributions of many
+ * (query range, key range) blocks of one packed stream, as
+ * nsp_attn_bwd_accumulate computes them for each block (full-row
+ * probabilities and delta, sums restricted to the block; [HSAP] Sec. 2.2.1
+ * ring InterSP, Sec. 3.2 blocks), in one schedule and one launch of each
+ * backward kernel: a whole ring's backward as one call.
+ *
+ *   q, out, dout: device [T][Hq][d]; k, v: device [T][Hkv][d]: the whole
+ *     stream, rows addressed by global token ids; lse: device float32 [Hq][T],
+ *     the rows' final lse (the forward's over all keys).
+ *   ranges: host array of nranges (1..64) {q_start, q_len, kv_start, kv_len},
+ *     read during the call; blocks may share rows or overlap.
+ *   dq_acc: device float32 [T][Hq][d]; dk_acc, dv_acc: device float32
+ *     [T][Hkv][d]: every block's contributions are ADDED at global rows with
+ *     float atomics (the caller zeroes them first; the order of the
+ *     additions, hence the last bits, may vary between runs).
+ * Tensor cores only: bf16 with d = 128 (other shapes: NSP_ERR_UNSUPPORTED;
+ * use nsp_attn_bwd_accumulate per block).  Every q_start must be a multiple
+ * of 4 (NSP_ERR_UNSUPPORTED otherwise).  Workspace: at least
+ * nsp_attn_bwd_blocks_workspace_size(T, nranges, ranges, Hq, Hkv, d) bytes.
+ * Other arguments and errors as nsp_attn_bwd_accumulate.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int64_t q_start, q_len, kv_start, kv_len;
+} nsp_range_t;
+
+size_t nsp_attn_bwd_blocks_workspace_size(int64_t T, int32_t nranges, const nsp_range_t* ranges,
+                                          int32_t Hq, int32_t Hkv, int32_t d);
+
+int32_t nsp_attn_bwd_blocks(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, const int32_t* cu_seqlens,
+                            int32_t ndoc, int64_t T, int32_t nranges, const nsp_range_t* ranges,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, int32_t causal,
+                            int32_t io_dtype, float* dq_acc, float* dk_acc, float* dv_acc,
+                            void* workspace, size_t workspace_bytes, nsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * nsp_attn_fwd without a workspace argument.  No page has a counterpart of
  * this entry point: it exists for callers that cannot allocate device
  * memory where they run attention (code inside a custom allocator or

@@ -189,6 +189,27 @@ def test_fwd_blocks_rejects_on_host(lib):
     assert call(overlapping) == nsp.NSP_ERR_INVALID
 
 
+def test_bwd_blocks_rejects_on_host(lib):
+    """nsp_attn_bwd_blocks: tensor-core shapes only, q_start a multiple of 4,
+    ranges inside [0, T), a workspace large enough; refused before any
+    launch."""
+    T = 1000
+
+    def call(ranges, io=nsp.NSP_BF16, d=128, nr=None, ws=1 << 26):
+        arr = nsp._range_array(ranges)
+        return lib.nsp_attn_bwd_blocks(A, A, A, A, A, A, A, 2, T, len(ranges) if nr is None else nr,
+                                       C.cast(arr, C.c_void_p), 8, 2, d, 0.088, 1, io, A, A, A,
+                                       A, ws, None)
+    ok = [(0, 500, 0, 500), (500, 500, 0, 1000)]
+    assert nsp.nsp_attn_bwd_blocks_workspace_size(T, ok, 8, 2, 128) > 0
+    assert call(ok, io=nsp.NSP_F32) == nsp.NSP_ERR_UNSUPPORTED
+    assert call(ok, d=64) == nsp.NSP_ERR_UNSUPPORTED
+    assert call([(2, 10, 0, 10)]) == nsp.NSP_ERR_UNSUPPORTED       # q_start not a multiple of 4
+    assert call([(0, 10, 995, 10)]) == nsp.NSP_ERR_INVALID         # keys past T
+    assert call(ok, nr=0) == nsp.NSP_ERR_INVALID
+    assert call(ok, ws=16) == nsp.NSP_ERR_WORKSPACE
+
+
 def test_wait_timeout_setter(lib):
     """The bound of device waits: a process-wide setting, default restored by
     a negative value; each call returns the previous bound."""

@@ -30,8 +30,8 @@ PATTERN = 0x5A
 
 def _run_all(nsp, w, dev):
     """Bit-identical across grids: forward, backward, a ring partial block,
-    the ring accumulation in place, the head-grouped forward and the
-    forward without a workspace.  Returned last: the ring-block backward's
+    the ring accumulation in place, the head-grouped forward, the forward
+    without a workspace and two batched blocks.  Returned last: the ring-block backward's
     (dq, dk, dv), grid-dependent in the last bits."""
     sc = w.cfg.d ** -0.5
     T, Hq, Hkv = w.T, w.cfg.Hq, w.cfg.Hkv
@@ -47,6 +47,11 @@ def _run_all(nsp, w, dev):
                                 scale=sc, q_start=qa, kv_start=a)
     og, lg = nsp.attn_fwd_headgroups(nsp.seq2head(dev["q"], 2), dev["k"], dev["v"], dev["cu"],
                                      scale=sc)
+    bl = [(qa, T - qa, ka, T - ka, torch.empty((T - qa, Hq, w.cfg.d), device="cuda"),
+           torch.empty((Hq, T - qa), device="cuda")),
+          (0, qa, 0, qa, torch.empty((qa, Hq, w.cfg.d), device="cuda"),
+           torch.empty((Hq, qa), device="cuda"))]
+    nsp.attn_fwd_blocks(dev["q"], dev["k"], dev["v"], dev["cu"], bl, scale=sc)
     on, ln = torch.empty_like(out), torch.empty_like(lse)
     st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     nsp.nsp_attn_fwd_noalloc(dev["q"], dev["k"], dev["v"], dev["cu"], len(w.lengths), 0, T, 0, T,
@@ -59,7 +64,8 @@ def _run_all(nsp, w, dev):
                             q_start=qa, kv_start=ka)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    return [out, lse, dq, dk, dv, po, pl, acc, lacc, og, lg, on, ln], (gq, gk, gv)
+    return ([out, lse, dq, dk, dv, po, pl, acc, lacc, og, lg, on, ln] + [t for b in bl for t in b[4:]],
+            (gq, gk, gv))
 
 
 @pytest.mark.parametrize("lens", [[100, 1, 300, 60, 250, 0, 517], [33] * 40 + [700]],
@@ -141,6 +147,16 @@ def test_outputs_stay_inside_their_buffers(nsp):
     mb, mbl = g("mb", (n, Hq, d), torch.float32), g("mbl", (Hq, n), torch.float32)
     mb2 = g("mb2", (n, Hq, d), torch.float32)
     nsp.nsp_lse_merge_batch([([po], [pl]), ([po, po], [pl, pl])], [mb, mb2], [mbl, None])
+    # two batched blocks of the whole stream, and the subgroup permutation
+    b1o, b1l = g("b1o", (n, Hq, d), torch.float32), g("b1l", (Hq, n), torch.float32)
+    b2o, b2l = g("b2o", (qa, Hq, d), torch.float32), g("b2l", (Hq, qa), torch.float32)
+    blocks = [(qa, n, ka, n, b1o, b1l), (0, qa, 0, qa, b2o, b2l)]
+    ws_bl = g("ws_bl", (nsp.nsp_attn_fwd_blocks_workspace_size(blocks, Hq, Hkv, d),), torch.uint8)
+    nsp.nsp_attn_fwd_blocks(dev["q"], dev["k"], dev["v"], dev["cu"], len(w.lengths), T, blocks,
+                            Hq, Hkv, d, sc, True, False, ws_bl)
+    Tg = T - T % 3
+    pg = g("pg", (3, 2, Tg // 3, Hq // 2, d), torch.bfloat16)
+    nsp.nsp_seq2head_permute_groups(dev["q"][:Tg], pg, 3, Tg // 3, Hq, d, 2, False)
     perm = g("perm", (4, T, Hq // 4, d), torch.bfloat16)
     back = g("back", (T, Hq, d), torch.bfloat16)
     nsp.nsp_seq2head_permute(dev["q"], perm, T, Hq, d, 4, False)

@@ -266,7 +266,7 @@ FwdBlocks table_of(int32_t nblocks, const nsp_block_t* blocks) {
   for (int32_t i = 0; i < nblocks; ++i) {
     B.b[i].q_start = (int32_t)blocks[i].q_start; B.b[i].q_len = (int32_t)blocks[i].q_len;
     B.b[i].kv_start = (int32_t)blocks[i].kv_start; B.b[i].kv_len = (int32_t)blocks[i].kv_len;
-    B.b[i].tile0 = 0; B.b[i].pad = 0;
+    B.b[i].tile0 = 0; B.b[i].ktile0 = 0;
     B.b[i].out = blocks[i].out; B.b[i].lse = blocks[i].lse;
   }
   return B;
@@ -335,6 +335,82 @@ int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
     if (launch_attn_fwd_simt(pb, s) != cudaSuccess) return NSP_ERR_CUDA;
   }
   return NSP_OK;
+}
+
+namespace {
+
+FwdBlocks range_table(int32_t nranges, const nsp_range_t* ranges) {
+  FwdBlocks B;
+  B.n = nranges;
+  B.global_rows = 1;
+  for (int32_t i = 0; i < nranges; ++i) {
+    B.b[i].q_start = (int32_t)ranges[i].q_start; B.b[i].q_len = (int32_t)ranges[i].q_len;
+    B.b[i].kv_start = (int32_t)ranges[i].kv_start; B.b[i].kv_len = (int32_t)ranges[i].kv_len;
+    B.b[i].tile0 = 0; B.b[i].ktile0 = 0;
+    B.b[i].out = nullptr; B.b[i].lse = nullptr;
+  }
+  return B;
+}
+
+bool ranges_ok(int64_t T, int32_t nranges, const nsp_range_t* ranges) {
+  if (nranges < 1 || nranges > kMaxBlocks || !ranges) return false;
+  for (int32_t i = 0; i < nranges; ++i) {
+    const nsp_range_t& r = ranges[i];
+    if (r.q_start < 0 || r.q_len < 0 || r.kv_start < 0 || r.kv_len < 0) return false;
+    if (r.q_start + r.q_len > T || r.kv_start + r.kv_len > T) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+size_t nsp_attn_bwd_blocks_workspace_size(int64_t T, int32_t nranges, const nsp_range_t* ranges,
+                                          int32_t Hq, int32_t Hkv, int32_t d) {
+  (void)Hkv; (void)d;
+  if (T < 0 || T > kMaxTokens || Hq < 1 || !ranges_ok(T, nranges, ranges)) return 0;
+  FwdBlocks B = range_table(nranges, ranges);
+  return bwd_ws_layout_blocks(B, T, Hq).total;
+}
+
+int32_t nsp_attn_bwd_blocks(const void* q, const void* k, const void* v, const void* out,
+                            const void* dout, const float* lse, const int32_t* cu_seqlens,
+                            int32_t ndoc, int64_t T, int32_t nranges, const nsp_range_t* ranges,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, int32_t causal,
+                            int32_t io_dtype, float* dq_acc, float* dk_acc, float* dv_acc,
+                            void* workspace, size_t workspace_bytes, nsp_stream_t stream) {
+  int32_t st = check_common(ndoc, Hq, Hkv, d, causal, io_dtype);
+  if (st != NSP_OK) return st;
+  if (T < 0) return NSP_ERR_INVALID;
+  if (T > kMaxTokens) return NSP_ERR_UNSUPPORTED;
+  if (!scale_ok(scale) || !cu_seqlens) return NSP_ERR_INVALID;
+  if (!ranges_ok(T, nranges, ranges)) return NSP_ERR_INVALID;
+  if (!bwd_tc_eligible(io_dtype, d, Hq, Hkv)) return NSP_ERR_UNSUPPORTED;
+  for (int32_t i = 0; i < nranges; ++i)     // whole-stream lse / delta rows are bulk-copied
+    if (ranges[i].q_start % 4 != 0) return NSP_ERR_UNSUPPORTED;
+  if (T > 0 && (!q || !k || !v || !out || !dout || !lse || !dq_acc || !dk_acc || !dv_acc))
+    return NSP_ERR_INVALID;
+  const void* ptrs[] = {q, k, v, out, dout, lse, cu_seqlens, dq_acc, dk_acc, dv_acc};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return NSP_ERR_ALIGN;
+  FwdBlocks B = range_table(nranges, ranges);
+  const BwdWsLayout L = bwd_ws_layout_blocks(B, T, Hq);
+  if (!workspace || workspace_bytes < L.total) return NSP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return NSP_ERR_ALIGN;
+  if (T == 0) return NSP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  AttnProblem p;                       // whole stream; ranges per block
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
+  p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
+  p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.scale = scale; p.causal = causal;
+  p.io_dtype = io_dtype; p.out_dtype = NSP_F32; p.out = nullptr; p.lse = nullptr;
+  p.hdr = reinterpret_cast<WsHeader*>(ws);
+  p.accumulate = 1;
+  if (launch_bwd_schedules(p, L, ws, s, &B) != cudaSuccess) return NSP_ERR_CUDA;
+  return launch_attn_bwd_tc(p, out, dout, lse, dq_acc, dk_acc, dv_acc, L, ws, s, &B) ==
+                 cudaSuccess
+             ? NSP_OK
+             : NSP_ERR_CUDA;
 }
 
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,

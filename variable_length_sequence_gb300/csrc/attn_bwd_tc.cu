@@ -192,10 +192,23 @@ struct BwdArgs {
   const int* korder;
 };
 
+// Block of a batched call's scheduled tile t: the largest index whose first
+// tile (key tiles: ktile0, query tiles: tile0) is <= t.
+template <bool KEY>
+__device__ __forceinline__ int block_of(const FwdBlocks& B, int t) {
+  int lo = 0, hi = B.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((KEY ? B.b[mid].ktile0 : B.b[mid].tile0) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // ================================================================ dK / dV
 
 struct KvItem {
-  int ktile, g, h0, i_lo, n_q, steps, pad[2];   // heads h0 .., steps = heads * n_q; -1 stops
+  int ktile, g, h0, i_lo, n_q, steps;   // heads h0 .., steps = heads * n_q; -1 stops
+  int blk, pad;                         // block of a batched call (MULTI)
 };
 
 struct __align__(1024) SmemKV {
@@ -222,11 +235,16 @@ struct __align__(1024) SmemKV {
 };
 static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memory");
 
+// MULTI: a batched call (nsp_attn_bwd_blocks): the tiles of every block of
+// blks, rows addressed by global token ids, every contribution added into the
+// whole-stream float32 accumulators with atomics (no preload).
+template <bool MULTI>
 __global__ void __launch_bounds__(kKvThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
+                            const __grid_constant__ CUtensorMap tm_v, const BwdArgs a,
+                            const __grid_constant__ FwdBlocks blks) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
@@ -297,12 +315,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         while (ok) {
           const int idx = atomicAdd(&hdr->counter2, 1);
           KvItem it;
-          it.ktile = 0; it.g = 0; it.h0 = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1;
+          it.ktile = 0; it.g = 0; it.h0 = 0; it.i_lo = 0; it.n_q = 0; it.steps = -1; it.blk = 0;
           if (idx < n_items) {
             const int kt = a.korder[idx / n_per_tile];
             const int2 tr = a.ktiles[kt];
             const int rem = idx - (idx / n_per_tile) * n_per_tile;
             it.ktile = kt;
+            if constexpr (MULTI) {
+              it.blk = block_of<true>(blks, kt);
+              it.ktile = kt - blks.b[it.blk].ktile0;         // key tile within its block
+            }
             it.g = rem / a.hsplit;
             it.h0 = it.g * G + (rem - it.g * a.hsplit) * heads_per_item;
             it.i_lo = tr.x;
@@ -325,10 +347,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+          // a batched call's maps span the whole stream (rows = global ids)
+          const int k_base = MULTI ? blks.b[it.blk].kv_start : 0;
+          const int q_base = MULTI ? blks.b[it.blk].q_start : 0;
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
-            tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
-            tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64, it.ktile * 128);
+            tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64,
+                        k_base + it.ktile * 128);
+            tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64,
+                        k_base + it.ktile * 128);
           }
           ++kv_count;
           for (int n = 0; n < it.steps; ++n) {
@@ -344,7 +371,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             mbar_arrive_expect_tx(&sm.slot_full[sq], kTile + 128 * sizeof(float));
             // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
-            int qx = h * HD, qy = i * 128;
+            int qx = h * HD, qy = q_base + i * 128;
             if (p.q_groups > 1) {
               const int hpg = p.Hq / p.q_groups, grp = h / hpg;
               qx = (h - grp * hpg) * HD;
@@ -353,7 +380,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
               tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], qx + cb * 64, qy);
-            const int64_t row = (int64_t)h * a.Tp + (int64_t)i * 128;
+            const int64_t row = (int64_t)h * a.Tp + q_base + (int64_t)i * 128;
             bulk_load(sm.vec[sq], a.nlse2 + row, 128 * sizeof(float), &sm.slot_full[sq]);
             ++loads;
             if (q_count >= 2 &&
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             tc_fence_after();
             // a ring block with one item per (key tile, KV head) adds onto the
             // preloaded running dK / dV
-            const bool acc = n > 0 || (p.accumulate && a.hsplit == 1);
+            const bool acc = n > 0 || (!MULTI && p.accumulate && a.hsplit == 1);
             mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
             mma_commit(&sm.dv_done[rb]);
             mma_commit(&sm.slot_empty[sd]);
@@ -525,22 +552,27 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         continue;
       }
+      // the item's ranges: its block's (batched call) or the call's
+      const int64_t it_kv_start = MULTI ? (int64_t)blks.b[it.blk].kv_start : p.kv_start;
+      const int64_t it_keys = MULTI ? (int64_t)blks.b[it.blk].kv_len : n_keys;
+      const int64_t it_q_start = MULTI ? (int64_t)blks.b[it.blk].q_start : p.q_start;
+      const int64_t it_q_len = MULTI ? (int64_t)blks.b[it.blk].q_len : p.q_len;
       int qlo[4], qhi[4];                                   // queries (range-relative) that see fragment row i
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int64_t key = (int64_t)it.ktile * 128 + wq * 32 + tr + 8 * i;
         qlo[i] = 0;
         qhi[i] = 0;
-        if (key < n_keys) {
-          const int64_t kg = p.kv_start + key;
+        if (key < it_keys) {
+          const int64_t kg = it_kv_start + key;
           const int b = doc_of(p.cu, p.ndoc, kg);
           const int64_t glo = p.causal ? kg : (int64_t)__ldg(p.cu + b);
           const int64_t ghi = __ldg(p.cu + b + 1);
-          qlo[i] = (int)min(max(glo - p.q_start, (int64_t)0), p.q_len);
-          qhi[i] = (int)min(max(ghi - p.q_start, (int64_t)0), p.q_len);
+          qlo[i] = (int)min(max(glo - it_q_start, (int64_t)0), it_q_len);
+          qhi[i] = (int)min(max(ghi - it_q_start, (int64_t)0), it_q_len);
         }
       }
-      if (p.accumulate && a.hsplit == 1) {
+      if (!MULTI && p.accumulate && a.hsplit == 1) {
         // ring block, one item per (key tile, KV head): dV and dK start as the
         // running accumulators (dK / scale), TMEM lane = key row
         const int64_t key = (int64_t)it.ktile * 128 + r;
@@ -676,14 +708,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const bool is_dk = cg >= 2;
         const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
         const float scale = is_dk ? p.scale : 1.f;
-        const int64_t off = (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
+        // whole-stream accumulators of a batched call: global key rows
+        const int64_t key_row = MULTI ? (int64_t)blks.b[it.blk].kv_start + key : key;
+        const int64_t off = (key_row * p.Hkv + it.g) * HD + (cg & 1) * 64;
+        const int64_t keys_here = MULTI ? (int64_t)blks.b[it.blk].kv_len : n_keys;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + col + c * 32, v);
           tmem_wait_ld();
-          if (key >= n_keys) continue;
-          if (p.accumulate && a.hsplit > 1)     // other items add into the same rows
+          if (key >= keys_here) continue;
+          if (MULTI || (p.accumulate && a.hsplit > 1))     // other items add into the same rows
             red_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
           else if (p.accumulate)                // the running value was preloaded
             store_row32_f32((is_dk ? a.dk_acc : a.dv_acc) + off + c * 32, v, scale);
@@ -712,7 +747,8 @@ constexpr int K_NS = 3;   // K tiles are read until dQ of their tile is done: on
 constexpr int V_NS = 2;
 
 struct QItem {
-  int qtile, h, g, j_lo, n_kv, pad[3];     // n_kv 128-key tiles; -1 stops
+  int qtile, h, g, j_lo, n_kv;     // n_kv 128-key tiles; -1 stops
+  int blk, pad[2];                 // block of a batched call (MULTI)
 };
 
 struct __align__(1024) SmemQ {
@@ -746,11 +782,13 @@ __device__ __forceinline__ bool issue_dp(SmemQ& sm, uint32_t tmem, uint32_t jc,
   return true;
 }
 
+template <bool MULTI>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
+                          const __grid_constant__ CUtensorMap tm_v, const BwdArgs a,
+                          const __grid_constant__ FwdBlocks blks) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
@@ -827,11 +865,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok) {
         const int idx = atomicAdd(&hdr->counter, 1);
         QItem it;
-        it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1;
+        it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1; it.blk = 0;
         if (idx < n_items) {
           const int qt = a.qorder[idx / p.Hq];
           const int2 tr = a.qtiles[qt];
           it.qtile = qt;
+          if constexpr (MULTI) {
+            it.blk = block_of<false>(blks, qt);
+            it.qtile = qt - blks.b[it.blk].tile0;           // query tile within its block
+          }
           it.h = idx - (idx / p.Hq) * p.Hq;
           it.g = it.h / G;
           it.j_lo = tr.x;
@@ -857,8 +899,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTile);
         {
           // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
+          // a batched call's maps span the whole stream (rows = global ids)
           const int hpg = p.Hq / p.q_groups, grp = it.h / hpg;
-          const int qx = (it.h - grp * hpg) * HD, qy = (int)(grp * p.q_len) + it.qtile * 128;
+          const int qx = (it.h - grp * hpg) * HD,
+                    qy = (MULTI ? blks.b[it.blk].q_start : 0) + (int)(grp * p.q_len) + it.qtile * 128;
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
             tma_load_2d(sm.q + cb * kBlk, &tm_q, &sm.q_full, qx + cb * 64, qy);
@@ -866,8 +910,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ++q_count;
+        const int k_base = MULTI ? blks.b[it.blk].kv_start : 0;
         for (int jj = 0; jj < it.n_kv; ++jj) {
-          const int key0 = (it.j_lo + jj) * 128;
+          const int key0 = k_base + (it.j_lo + jj) * 128;
           {
             const uint32_t st = k_count % K_NS, use = k_count / K_NS;
             if (use >= 1 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, wc, hdr)) {
@@ -970,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // (a ring block adds onto the preloaded running dQ)
           mma_t_split<64>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]),
-                          jj > 0 || p.accumulate);                             // dQ += dS K
+                          jj > 0 || (!MULTI && p.accumulate));                 // dQ += dS K
           mma_commit(&sm.dq_done[b]);
           mma_commit(&sm.k_empty[st]);
           ++jc;
@@ -1000,23 +1045,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it_count;
       if (it.n_kv < 0) break;
       const int h = it.h;
-      const int64_t row = (int64_t)it.qtile * 128 + r;
-      const bool valid = row < T;
+      const int64_t row = (int64_t)it.qtile * 128 + r;      // relative to the (block's) query range
+      // the item's ranges: its block's (batched call) or the call's
+      const int64_t it_q_start = MULTI ? (int64_t)blks.b[it.blk].q_start : p.q_start;
+      const bool valid = row < (MULTI ? (int64_t)blks.b[it.blk].q_len : T);
       int lo = 0, hi = 0;                                    // visible keys [lo, hi)
       float nlse2r = 0.f, deltar = 0.f;
       if (valid) {
         // visible keys, relative to the key range
-        const int64_t tg = p.q_start + row;
+        const int64_t kvs = MULTI ? (int64_t)blks.b[it.blk].kv_start : p.kv_start;
+        const int64_t kve = kvs + (MULTI ? (int64_t)blks.b[it.blk].kv_len : p.kv_len);
+        const int64_t tg = it_q_start + row;
         const int b = doc_of(p.cu, p.ndoc, tg);
-        const int64_t glo = max((int64_t)__ldg(p.cu + b), p.kv_start);
-        const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1),
-                                p.kv_start + p.kv_len);
-        lo = (int)(glo - p.kv_start);
-        hi = (int)max(ghi - p.kv_start, glo - p.kv_start);
-        nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + row);
-        deltar = __ldg(a.delta + (int64_t)h * a.Tp + row);
+        const int64_t glo = max((int64_t)__ldg(p.cu + b), kvs);
+        const int64_t ghi = min(p.causal ? tg + 1 : (int64_t)__ldg(p.cu + b + 1), kve);
+        lo = (int)(glo - kvs);
+        hi = (int)max(ghi - kvs, glo - kvs);
+        // delta and -lse log2(e): per call, or over the whole stream (batched)
+        const int64_t vrow = MULTI ? tg : row;
+        nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + vrow);
+        deltar = __ldg(a.delta + (int64_t)h * a.Tp + vrow);
       }
-      if (p.accumulate && it.n_kv > 0) {
+      if (!MULTI && p.accumulate && it.n_kv > 0) {
         // ring block: dQ's TMEM accumulator starts as the running dq / scale
         const float* src = valid ? a.dq_acc + qo_offset(p, row, h) + wg * 64 : nullptr;
         const uint32_t col = tmem + lane_base + 384 + wg * 64;
@@ -1089,7 +1139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + 384 + wg * 64 + c * 32, v);
           tmem_wait_ld();
           if (!valid) continue;
-          if (p.accumulate)           // the running value was preloaded
+          if (MULTI)                  // other blocks add into the same whole-stream rows
+            red_row32_f32(a.dq_acc + ((it_q_start + row) * p.Hq + h) * HD + wg * 64 + c * 32, v,
+                          p.scale);
+          else if (p.accumulate)      // the running value was preloaded
             store_row32_f32(a.dq_acc + qo_offset(p, row, h) + wg * 64 + c * 32, v, p.scale);
           else
             store_row32_bf16(dst + c * 32, v, p.scale);
@@ -1154,7 +1207,8 @@ bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
 
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
-                               const BwdWsLayout& L, char* ws, cudaStream_t s) {
+                               const BwdWsLayout& L, char* ws, cudaStream_t s,
+                               const FwdBlocks* blocks) {
   const int64_t T = p.q_len;
   CUtensorMap mq, mdo, mk, mv;
   const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
@@ -1190,25 +1244,24 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   // writes each dK/dV row once (hsplit = 1).
   const int G = p.Hq / p.Hkv;
   a.hsplit = 1;
-  if (p.accumulate)
+  if (p.accumulate || blocks != nullptr)
     while (a.hsplit < G && G % (2 * a.hsplit) == 0 &&
            L.n_ktiles * p.Hkv * a.hsplit < 2 * (int64_t)grid)
       a.hsplit *= 2;
   constexpr size_t kv_bytes = smem_bytes<SmemKV>();
   constexpr size_t q_bytes = smem_bytes<SmemQ>();
-  e = cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kv_bytes);
+  const FwdBlocks B = blocks ? *blocks : single_block(p);
+  auto kv_kern = blocks ? attn_bwd_dkdv_tc_kernel<true> : attn_bwd_dkdv_tc_kernel<false>;
+  auto q_kern = blocks ? attn_bwd_dq_tc_kernel<true> : attn_bwd_dq_tc_kernel<false>;
+  e = cudaFuncSetAttribute(kv_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_bytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)q_bytes);
+  e = cudaFuncSetAttribute(q_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_bytes);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(attn_bwd_dkdv_tc_kernel, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq,
-                       mdo, mk, mv, a);
+  e = launch_dependent(kv_kern, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq, mdo, mk, mv, a, B);
   count_launches(1);
   count_path(true);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(attn_bwd_dq_tc_kernel, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo,
-                       mk, mv, a);
+  e = launch_dependent(q_kern, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo, mk, mv, a, B);
   count_launches(1);
   count_path(true);
   if (e != cudaSuccess) return e;

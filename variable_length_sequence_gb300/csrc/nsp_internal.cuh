@@ -63,7 +63,7 @@ constexpr int kMaxBlocks = 64;
 struct FwdBlock {
   int32_t q_start, q_len, kv_start, kv_len;   // global token ids
   int32_t tile0;                              // first scheduled query tile of the block
-  int32_t pad;
+  int32_t ktile0;                             // first scheduled key tile (backward)
   void* out;                                  // [q_len, Hq, d]
   float* lse;                                 // [Hq, q_len] or null
 };
@@ -109,13 +109,14 @@ inline FwdWsLayout fwd_ws_layout_blocks(FwdBlocks& B, int32_t tile_rows) {
 constexpr int kBwdSub = 128;       // tile granularity listed by the backward schedules
 
 struct BwdWsLayout {
-  size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_ktiles + 2]
-  size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_qtiles + 2]
+  size_t qtiles, qorder, qhist;    // int2 [n_qtiles], int32 [n_qtiles], int32 [n_qhist]
+  size_t ktiles, korder, khist;    // int2 [n_ktiles], int32 [n_ktiles], int32 [n_khist]
   size_t delta;                    // float [Hq, Tp]
   size_t nlse2;                     // float [Hq, Tp]
   size_t dq_acc;                   // float [q_len, Hq, d] (CUDA-core path)
   size_t total;
   int64_t Tp, n_qtiles, n_ktiles;
+  int64_t n_qhist, n_khist;        // counting-sort buckets of the two schedules
 };
 
 inline BwdWsLayout bwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t d,
@@ -124,18 +125,57 @@ inline BwdWsLayout bwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t Hq, int3
   L.n_qtiles = ceil_div(q_len, kTileM);
   L.n_ktiles = ceil_div(kv_len, kTileN);
   L.Tp = L.n_qtiles * kTileM;
+  L.n_qhist = L.n_ktiles + 2;
+  L.n_khist = L.n_qtiles + 2;
   size_t off = sizeof(WsHeader);
   L.qtiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_qtiles, 256);
   L.qorder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_qtiles, 256);
-  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_ktiles + 2), 256);
+  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_qhist, 256);
   L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)L.n_ktiles, 256);
   L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)L.n_ktiles, 256);
-  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)(L.n_qtiles + 2), 256);
+  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_khist, 256);
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.nlse2 = off;   off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off;
   if (need_dq_acc)
     off = align_up(off + sizeof(float) * (size_t)q_len * (size_t)Hq * (size_t)d, 256);
+  L.total = off;
+  return L;
+}
+
+// Backward of a table of blocks over a whole stream of T tokens: the query
+// tiles and the key tiles of every block, one sort each; delta and -lse
+// log2(e) over the whole stream [Hq, Tp].  Fills in each block's tile0 and
+// ktile0.
+inline BwdWsLayout bwd_ws_layout_blocks(FwdBlocks& B, int64_t T, int32_t Hq) {
+  int64_t nq = 0, nk = 0, max_q = 0, max_k = 0;
+  for (int i = 0; i < B.n; ++i) {
+    B.b[i].tile0 = (int32_t)nq;
+    B.b[i].ktile0 = (int32_t)nk;
+    const int64_t q = ceil_div(B.b[i].q_len, kTileM), k = ceil_div(B.b[i].kv_len, kTileN);
+    nq += q; nk += k;
+    max_q = q > max_q ? q : max_q;
+    max_k = k > max_k ? k : max_k;
+  }
+  BwdWsLayout L;
+  L.n_qtiles = nq;
+  L.n_ktiles = nk;
+  // one spare tile of (zeroed) padding: the dK/dV kernel copies the values
+  // of whole 128-row tiles starting at a block's q_start, which need not be
+  // a multiple of 128, so the last copy may run up to 127 rows past T
+  L.Tp = (ceil_div(T, kTileM) + 1) * kTileM;
+  L.n_qhist = max_k + 2;
+  L.n_khist = max_q + 2;
+  size_t off = sizeof(WsHeader);
+  L.qtiles = off; off = align_up(off + sizeof(int2) * (size_t)nq, 256);
+  L.qorder = off; off = align_up(off + sizeof(int32_t) * (size_t)nq, 256);
+  L.qhist = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_qhist, 256);
+  L.ktiles = off; off = align_up(off + sizeof(int2) * (size_t)nk, 256);
+  L.korder = off; off = align_up(off + sizeof(int32_t) * (size_t)nk, 256);
+  L.khist = off;  off = align_up(off + sizeof(int32_t) * (size_t)L.n_khist, 256);
+  L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
+  L.nlse2 = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
+  L.dq_acc = off;
   L.total = off;
   return L;
 }
@@ -171,8 +211,10 @@ struct AttnProblem {
 // [q_start, +q_len) x [kv_start, +kv_len) of p with p's out and lse.
 cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                 cudaStream_t s, const FwdBlocks* blocks = nullptr);
+// The backward's blocks: `blocks` (tile0 and ktile0 filled in), or when
+// null the one range of p.
 cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
-                                 cudaStream_t s);
+                                 cudaStream_t s, const FwdBlocks* blocks = nullptr);
 cudaError_t launch_attn_fwd_simt(const AttnProblem& p, cudaStream_t s);
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                cudaStream_t s, bool* launched, const FwdBlocks* blocks = nullptr);
@@ -184,9 +226,12 @@ cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const vo
 // True when the tensor-core backward takes this problem (bf16, d = 128,
 // an even number of query heads per KV head).
 bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv);
+// With `blocks`: every block's contributions added into whole-stream float32
+// dq / dk / dv (global rows) with atomics; p covers the whole stream.
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv,
-                               const BwdWsLayout& L, char* ws, cudaStream_t s);
+                               const BwdWsLayout& L, char* ws, cudaStream_t s,
+                               const FwdBlocks* blocks = nullptr);
 cudaError_t launch_bwd_delta(const void* out, const void* dout, const float* lse, float* delta,
                              float* nlse2, int64_t T, int64_t Tp, int Hq, int d, int io_dtype,
                              int P, WsHeader* hdr, cudaStream_t s);

@@ -50,9 +50,11 @@ struct SchedArgs {
   int32_t tile_rows;   // mode 0: rows of a scheduled query tile (128 or 256)
   WsHeader* hdr;
   int32_t second;      // write counters into counter2 / n_items2
-  // mode 0: the blocks whose query tiles are listed; tile i belongs to the
-  // block with the largest tile0 <= i (the range fields above are unused)
+  // the blocks whose tiles are listed: mode 0 tile i belongs to the block
+  // with the largest tile0 <= i, mode 1 tile i (use_blocks) to the block
+  // with the largest ktile0 <= i (the range fields above are then unused)
   FwdBlocks blks;
+  int32_t use_blocks;  // mode 1: take the key tiles of blks instead of the range fields
 };
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_constant__ SchedArgs a) {
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
     if (tid == 0) {
       if (a.ndoc < 1 || a.cu[0] != 0) s_bad = 1;
       const int64_t total = a.cu[a.ndoc];
-      if (a.mode == 0) {
+      if (a.mode == 0 || a.use_blocks) {
         for (int bi = 0; bi < a.blks.n; ++bi) {
           const FwdBlock& B = a.blks.b[bi];
           if (total < (int64_t)B.q_start + B.q_len || total < (int64_t)B.kv_start + B.kv_len)
@@ -124,14 +126,27 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
         hi_t = (int)((hi - 1 - ks) / a.gran);
       }
     } else {
-      const int64_t k0 = a.kv_start + (int64_t)i * kTileN;
-      const int64_t k1 = min(k0 + kTileN, kv_end) - 1;          // last key of the tile
+      int64_t ks = a.kv_start, ke = kv_end, qs = a.q_start, qe = q_end, k0 = a.kv_start;
+      if (a.use_blocks) {
+        int bl = 0, bh = a.blks.n - 1;
+        while (bl < bh) {
+          const int mid = (bl + bh + 1) >> 1;
+          if (a.blks.b[mid].ktile0 <= i) bl = mid; else bh = mid - 1;
+        }
+        const FwdBlock& B = a.blks.b[bl];
+        ks = B.kv_start; ke = (int64_t)B.kv_start + B.kv_len;
+        qs = B.q_start; qe = (int64_t)B.q_start + B.q_len;
+        k0 = ks + (int64_t)(i - B.ktile0) * kTileN;
+      } else {
+        k0 = a.kv_start + (int64_t)i * kTileN;
+      }
+      const int64_t k1 = min(k0 + kTileN, ke) - 1;               // last key of the tile
       const int b0 = doc_of(a.cu, a.ndoc, k0), b1 = doc_of(a.cu, a.ndoc, k1);
-      const int64_t lo = max(a.causal ? k0 : (int64_t)a.cu[b0], a.q_start);
-      const int64_t hi = min((int64_t)a.cu[b1 + 1], q_end);      // exclusive
+      const int64_t lo = max(a.causal ? k0 : (int64_t)a.cu[b0], qs);
+      const int64_t hi = min((int64_t)a.cu[b1 + 1], qe);         // exclusive
       if (hi > lo) {
-        lo_t = (int)((lo - a.q_start) / a.gran);
-        hi_t = (int)((hi - 1 - a.q_start) / a.gran);
+        lo_t = (int)((lo - qs) / a.gran);
+        hi_t = (int)((hi - 1 - qs) / a.gran);
       }
     }
     a.tiles[i] = make_int2(lo_t, hi_t);
@@ -200,7 +215,7 @@ FwdBlocks single_block(const AttnProblem& p) {
   B.global_rows = 0;
   B.b[0].q_start = (int32_t)p.q_start; B.b[0].q_len = (int32_t)p.q_len;
   B.b[0].kv_start = (int32_t)p.kv_start; B.b[0].kv_len = (int32_t)p.kv_len;
-  B.b[0].tile0 = 0; B.b[0].pad = 0;
+  B.b[0].tile0 = 0; B.b[0].ktile0 = 0;
   B.b[0].out = p.out; B.b[0].lse = p.lse;
   return B;
 }
@@ -209,6 +224,7 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
                                 cudaStream_t s, const FwdBlocks* blocks) {
   SchedArgs a;
   a.blks = blocks ? *blocks : single_block(p);
+  a.use_blocks = 0;
   a.gran = kTileN;
   a.tile_rows = L.tile_rows;
   a.cu = p.cu; a.ndoc = p.ndoc;
@@ -225,29 +241,30 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
 }
 
 cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, char* ws,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const FwdBlocks* blocks) {
   // query tiles of 128 rows listing 128-key tiles (validates cu_seqlens)
   SchedArgs a;
   a.cu = p.cu; a.ndoc = p.ndoc;
   a.q_start = p.q_start; a.q_len = p.q_len; a.kv_start = p.kv_start; a.kv_len = p.kv_len;
   a.causal = p.causal; a.mode = 0; a.validate = 1; a.gran = kBwdSub; a.tile_rows = kTileM;
-  a.blks = single_block(p);
+  a.blks = blocks ? *blocks : single_block(p);
+  a.use_blocks = 0;
   a.tiles = reinterpret_cast<int2*>(ws + L.qtiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.qorder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.qhist);
   a.n_tiles = (int32_t)L.n_qtiles;
-  a.n_buckets = (int32_t)L.n_ktiles + 2;
+  a.n_buckets = (int32_t)L.n_qhist;
   a.hdr = p.hdr; a.second = 0;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // key tiles of 128 keys listing 128-row query tiles
-  a.mode = 1; a.validate = 0;
+  a.mode = 1; a.validate = 0; a.use_blocks = blocks != nullptr;
   a.tiles = reinterpret_cast<int2*>(ws + L.ktiles);
   a.order = reinterpret_cast<int32_t*>(ws + L.korder);
   a.hist = reinterpret_cast<int32_t*>(ws + L.khist);
   a.n_tiles = (int32_t)L.n_ktiles;
-  a.n_buckets = (int32_t)L.n_qtiles + 2;
+  a.n_buckets = (int32_t)L.n_khist;
   a.hdr = p.hdr; a.second = 1;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   return cudaGetLastError();

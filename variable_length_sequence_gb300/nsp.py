@@ -43,6 +43,9 @@ _SIGNATURES = {
     "nsp_attn_fwd_blocks_workspace_size": (_sz, [_i32, _vp, _i32, _i32, _i32]),
     "nsp_attn_fwd_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _i32, _i32, _i32, _f32,
                                    _i32, _i32, _i32, _vp, _sz, _vp]),
+    "nsp_attn_bwd_blocks_workspace_size": (_sz, [_i64, _i32, _vp, _i32, _i32, _i32]),
+    "nsp_attn_bwd_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _vp, _i32,
+                                   _i32, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "nsp_attn_fwd_validate": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
                                      _i32, _i32, _i32, _i32, _vp, _i32, _vp, _sz]),
     "nsp_attn_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _i64, _i32,
@@ -77,6 +80,12 @@ class Block(C.Structure):
     """nsp_block_t: one (query range, key range) block of a batched forward."""
     _fields_ = [("q_start", C.c_int64), ("q_len", C.c_int64), ("kv_start", C.c_int64),
                 ("kv_len", C.c_int64), ("out", C.c_void_p), ("lse", C.c_void_p)]
+
+
+class Range(C.Structure):
+    """nsp_range_t: one (query range, key range) block of a batched backward."""
+    _fields_ = [("q_start", C.c_int64), ("q_len", C.c_int64), ("kv_start", C.c_int64),
+                ("kv_len", C.c_int64)]
 
 
 class AttnCost(C.Structure):
@@ -179,6 +188,32 @@ def nsp_attn_fwd_blocks(q, k, v, cu_seqlens, ndoc, T, blocks, Hq, Hkv, d, scale,
                                     int(bool(accumulate)), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream))
     return _check("nsp_attn_fwd_blocks", st)
+
+
+def _range_array(ranges):
+    arr = (Range * len(ranges))()
+    for i, (qs, ql, ks, kl) in enumerate(ranges):
+        arr[i] = Range(int(qs), int(ql), int(ks), int(kl))
+    return arr
+
+
+def nsp_attn_bwd_blocks_workspace_size(T: int, ranges, Hq: int, Hkv: int, d: int) -> int:
+    arr = _range_array(ranges)
+    return int(load().nsp_attn_bwd_blocks_workspace_size(int(T), len(ranges),
+                                                         C.cast(arr, C.c_void_p), int(Hq),
+                                                         int(Hkv), int(d)))
+
+
+def nsp_attn_bwd_blocks(q, k, v, out, dout, lse, cu_seqlens, ndoc, T, ranges, Hq, Hkv, d, scale,
+                        causal, dq_acc, dk_acc, dv_acc, workspace, stream=None) -> int:
+    arr = _range_array(ranges)
+    st = load().nsp_attn_bwd_blocks(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                    _ptr(cu_seqlens), int(ndoc), int(T), len(ranges),
+                                    C.cast(arr, C.c_void_p), int(Hq), int(Hkv), int(d),
+                                    float(scale), int(bool(causal)), _dtype(q), _ptr(dq_acc),
+                                    _ptr(dk_acc), _ptr(dv_acc), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check("nsp_attn_bwd_blocks", st)
 
 
 def nsp_attn_bwd_workspace_size(T: int, Hq: int, Hkv: int, d: int, io_dtype: int = NSP_BF16) -> int:
@@ -451,6 +486,21 @@ def attn_fwd_blocks(q, k, v, cu_seqlens, blocks, scale=None, causal=True, accumu
                                 dtype=torch.uint8, device=q.device)
     nsp_attn_fwd_blocks(q, k, v, cu_seqlens, cu_seqlens.numel() - 1, T, blocks, Hq, Hkv, d, scale,
                         causal, accumulate, workspace, stream)
+
+
+def attn_bwd_blocks(q, k, v, out, dout, lse, cu_seqlens, ranges, dq_acc, dk_acc, dv_acc,
+                    scale=None, causal=True, workspace=None, stream=None):
+    """Add the backward contributions of blocks [(q_start, q_len, kv_start,
+    kv_len), ...] of the whole stream into float32 dq_acc [T, Hq, d] and
+    dk_acc / dv_acc [T, Hkv, d] (lse [Hq, T], the rows' final lse)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(nsp_attn_bwd_blocks_workspace_size(T, ranges, Hq, Hkv, d),
+                                dtype=torch.uint8, device=q.device)
+    nsp_attn_bwd_blocks(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, T, ranges,
+                        Hq, Hkv, d, scale, causal, dq_acc, dk_acc, dv_acc, workspace, stream)
 
 
 def attn_bwd(q, k, v, out, dout, lse, cu_seqlens, scale=None, causal=True, workspace=None,
