@@ -51,6 +51,8 @@
 // sits at row block (h / (Hq/P)) q_len, column block h % (Hq/P).
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "tc_ptx.cuh"
 
 namespace nsp {
@@ -176,9 +178,11 @@ __device__ __forceinline__ void store_row_chunk<float>(float* dst, const uint32_
 // PAIR: an item is two adjacent tiles of one head (odd Hq / Hkv) instead of
 // one tile and two heads.  MULTI: the batched call, ranges and outputs per
 // block of the table and q / k / v rows addressed by global token ids;
-// otherwise the single range and outputs of p.  Both are compile-time so the
-// common case (one range, head pairs) carries none of their bookkeeping.
-template <typename TO, bool PAIR, bool MULTI>
+// otherwise the single range and outputs of p.  ACC: ring accumulation in
+// place (float32 out only).  All three are compile-time so the common cases
+// (one range, head pairs, written output) carry none of the others'
+// bookkeeping or registers.
+template <typename TO, bool PAIR, bool MULTI, bool ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++p_count[t];
             tc_fence_after();
             // a ring accumulation's O starts as the preloaded running output
-            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0 || p.accumulate);
+            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0 || ACC);
             if (t == 1) mma_commit(&sm.v_empty[st]);
             if (!has_next) {
               mma_commit(&sm.o_full[t]);
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tm = tmem + lane_base + col_o(t);
     const float sl2 = p.scale * kLog2e;
     uint32_t it_count = 0, s_count = 0, o_count = 0;
-    if (!p.accumulate) {
+    if (!ACC) {
       // Query tiles that see no key of the range (listed last by the
       // schedule): out = 0 and lse = -inf, written by the softmax warps of
       // every CTA in a grid-stride loop over (tile, head, 32-row group), one
@@ -461,10 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the item's ranges (global ids) and outputs: its block's (batched
       // call) or the call's, read where they are used (kernel parameters,
       // so no register holds them across the tile loop)
-      const int blk = it.blk;
-#define NSP_BLK(field, whole) (MULTI ? (int64_t)blks.b[blk].field : (int64_t)p.whole)
-#define NSP_OUT (reinterpret_cast<TO*>(MULTI ? blks.b[blk].out : p.out))
-#define NSP_LSE (MULTI ? blks.b[blk].lse : p.lse)
+      // (a batched call copies its block's entry once per item; a single
+      // range reads the kernel parameter p at each use)
+      FwdBlock mb{};
+      if constexpr (MULTI) mb = blks.b[it.blk];
+#define NSP_BLK(field, whole) (MULTI ? (int64_t)mb.field : (int64_t)p.whole)
+#define NSP_OUT (reinterpret_cast<TO*>(MULTI ? mb.out : p.out))
+#define NSP_LSE (MULTI ? mb.lse : p.lse)
       const int h = pair_tiles ? it.h0 : it.h0 + t;
       // first row of this role's 128-row tile, query-range relative
       const int64_t tile_base = (int64_t)it.qtile * tile_rows + (pair_tiles ? t * BM : 0);
@@ -490,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // l as the maximum grows covers acc too).  The preload runs while the
       // item's first S is computed; the block's first P V then accumulates
       // onto it.  Every other row starts from O = 0 and is not written.
-      const bool acc_row = p.accumulate && valid && hi > lo;
+      const bool acc_row = ACC && valid && hi > lo;
       if constexpr (sizeof(TO) == 4) {
-        if (p.accumulate && it.n_kv > 0) {
+        if (ACC && it.n_kv > 0) {
           float la2 = -INFINITY;
           if (acc_row) la2 = NSP_LSE[(int64_t)h * NSP_BLK(q_len, q_len) + row] * kLog2e;
           const float4* arow = reinterpret_cast<const float4*>(NSP_OUT + qo_offset(p, row, h));
@@ -611,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the warp's 32 (i = 0..3)
           // (ring accumulation: rows that saw no key of the block keep their
           // running output, so they are skipped)
-          const float wp = (p.accumulate && !acc_row) ? 0.f : inv;
+          const float wp = (ACC && !acc_row) ? 0.f : inv;
           float wpr[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) wpr[i] = __shfl_sync(0xffffffffu, wp, 8 * i + (lane >> 2));
@@ -625,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 16; ++k) {
               const int i = 2 * (k >> 3) + (k & 1);
               const int64_t grow = tile_base + wq * 32 + 8 * i + (lane >> 2);
-              if (grow < NSP_BLK(q_len, q_len) && (!p.accumulate || wpr[i] != 0.f))
+              if (grow < NSP_BLK(q_len, q_len) && (!ACC || wpr[i] != 0.f))
                 *reinterpret_cast<float2*>(NSP_OUT + qo_offset(p, grow, h) + c * 32 +
                                            8 * ((k >> 1) & 3) + 2 * (lane & 3)) =
                     make_float2(__uint_as_float(x[2 * k]) * wpr[i],
@@ -641,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) store_row_chunk<TO>(dst + c * 32, orow, inv);
           }
         }
-      } else if (!p.accumulate) {
+      } else if (!ACC) {
         // no key of the range is visible to any row of the tile: zero rows,
         // each written whole by a warp (16-byte lanes, full sectors)
         constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
@@ -654,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint4*>(NSP_OUT + qo_offset(p, grow, h))[part] = make_uint4(0, 0, 0, 0);
         }
       }
-      if (valid && NSP_LSE != nullptr && (!p.accumulate || acc_row))
+      if (valid && NSP_LSE != nullptr && (!ACC || acc_row))
         NSP_LSE[(int64_t)h * NSP_BLK(q_len, q_len) + row] =
             l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
 #undef NSP_BLK
@@ -700,11 +707,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TO, bool PAIR, bool MULTI>
+template <typename TO, bool PAIR, bool MULTI, bool ACC>
 cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, cudaStream_t s,
                          const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdBlocks& B) {
-  auto kern = attn_fwd_tc_kernel<TO, PAIR, MULTI>;
+  auto kern = attn_fwd_tc_kernel<TO, PAIR, MULTI, ACC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -735,14 +742,19 @@ cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char*
   pk.wait_budget = wait_budget_cycles();
   const FwdBlocks B = blocks ? *blocks : single_block(p);
   const bool pair = ((p.Hq / p.Hkv) & 1) != 0;
-  if (blocks != nullptr)            // batched blocks: float32 partials or accumulators
-    return pair ? launch_typed<float, true, true>(pk, L, ws, s, mq, mk, mv, B)
-                : launch_typed<float, false, true>(pk, L, ws, s, mq, mk, mv, B);
-  if (pk.out_dtype == NSP_F32)
-    return pair ? launch_typed<float, true, false>(pk, L, ws, s, mq, mk, mv, B)
-                : launch_typed<float, false, false>(pk, L, ws, s, mq, mk, mv, B);
-  return pair ? launch_typed<__nv_bfloat16, true, false>(pk, L, ws, s, mq, mk, mv, B)
-              : launch_typed<__nv_bfloat16, false, false>(pk, L, ws, s, mq, mk, mv, B);
+  const bool acc = p.accumulate != 0;                 // (float32 out only)
+  // batched blocks: float32 partials or accumulators
+  auto f32 = [&](auto pair_c, auto multi_c) {
+    constexpr bool P = decltype(pair_c)::value, M = decltype(multi_c)::value;
+    return acc ? launch_typed<float, P, M, true>(pk, L, ws, s, mq, mk, mv, B)
+               : launch_typed<float, P, M, false>(pk, L, ws, s, mq, mk, mv, B);
+  };
+  using T_ = std::true_type;
+  using F_ = std::false_type;
+  if (blocks != nullptr) return pair ? f32(T_{}, T_{}) : f32(F_{}, T_{});
+  if (pk.out_dtype == NSP_F32) return pair ? f32(T_{}, F_{}) : f32(F_{}, F_{});
+  return pair ? launch_typed<__nv_bfloat16, true, false, false>(pk, L, ws, s, mq, mk, mv, B)
+              : launch_typed<__nv_bfloat16, false, false, false>(pk, L, ws, s, mq, mk, mv, B);
 }
 
 }  // namespace nsp
