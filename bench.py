@@ -187,8 +187,9 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- ncu traffic
 
 KERNEL_SOURCES = {"attn_fwd_tc_kernel": "attn_fwd_tc.cu", "attn_bwd_dkdv_tc_kernel": "attn_bwd_tc.cu",
-                  "attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu", "lse_merge_kernel": "merge.cu",
-                  "permute_vec_kernel": "permute.cu"}
+                  "attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu",
+                  "attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu",
+                  "lse_merge_kernel": "merge.cu", "permute_vec_kernel": "permute.cu"}
 
 
 def source_sha(kernel: str) -> str:
@@ -206,8 +207,8 @@ def source_sha(kernel: str) -> str:
 
 def profiled_traffic() -> dict:
     """DRAM bytes per launch from the committed ncu summaries: every line
-    'traffic: KERNEL WORKLOAD BYTES SHA' in profiles/*.md.  Kept only when SHA
-    is the current source_sha(KERNEL): counters of an older kernel are not
+    'traffic: KERNEL WORKLOAD LEG BYTES SHA' in profiles/*.md.  Kept only when
+    SHA is the current source_sha(KERNEL): counters of an older kernel are not
     reported."""
     out = {}
     d = os.path.join(ROOT, "profiles")
@@ -222,11 +223,11 @@ def profiled_traffic() -> dict:
                 if not ln.startswith("traffic:"):
                     continue
                 parts = ln.split()
-                if len(parts) != 5 or parts[1] not in KERNEL_SOURCES:
+                if len(parts) != 6 or parts[1] not in KERNEL_SOURCES:
                     continue
-                kern, wl, nbytes, sha = parts[1], parts[2], float(parts[3]), parts[4]
+                kern, wl, leg, nbytes, sha = parts[1], parts[2], parts[3], float(parts[4]), parts[5]
                 if sha == source_sha(kern):
-                    out[(kern, wl)] = nbytes
+                    out[(kern, wl, leg)] = nbytes
     return out
 
 
@@ -558,7 +559,7 @@ def leg_records(prob, legs: dict, peaks: dict) -> dict:
 def roof_entry(kernel, cid, leg, bound, achieved, peak, unit, work, work_unit, launches,
                traffic_map, peak_kind="burst"):
     wl = CONFIGS[cid].name
-    tr = traffic_map.get((kernel, wl))
+    tr = traffic_map.get((kernel, wl, leg))
     return {"kernel": kernel, "workload": wl, "leg": leg, "bound": bound,
             "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
             "peak_kind": peak_kind, "algorithmic_per_launch": work / max(1, launches),
@@ -592,8 +593,7 @@ def sub_config(nsp, cid, device, stream, flush, peaks, clocks, K, warmup, traffi
     if "ring_partials" in legs:
         roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "ring_partials", "tensor",
                                 rec["legs"]["ring_partials"]["tflops"], peaks["bf16_tflops"],
-                                "TFLOP/s", prob.ring_flop, "FLOP", len(prob.ring_pairs),
-                                traffic_map))
+                                "TFLOP/s", prob.ring_flop, "FLOP", 1, traffic_map))
     for k, kern in (("merge", "lse_merge_kernel"), ("permute", "permute_vec_kernel")):
         if k in legs:
             nb = prob.merge_bytes if k == "merge" else prob.permute_bytes
@@ -682,9 +682,14 @@ def run_ours(args, world, rank, local):
         ach = (prob.fwd_flop + prob.ring_flop) / (legs["fwd"] + legs["ring_partials"]) / 1e9
         roof = roof_entry("attn_fwd_tc_kernel", cid, "fwd + ring_partials", "tensor", ach,
                           peaks["bf16_tflops"], "TFLOP/s", prob.fwd_flop + prob.ring_flop, "FLOP",
-                          1 + len(prob.ring_pairs), traffic_map)
-        roof["traffic"] = None       # per-launch DRAM bytes differ between main and ring launches
-        roof["traffic_unit"] = None
+                          2, traffic_map)
+        # one main forward launch and one batched launch of all ring blocks:
+        # DRAM bytes per launch = the mean of the two profiled launches
+        wl = CONFIGS[cid].name
+        tr = [traffic_map.get(("attn_fwd_tc_kernel", wl, k)) for k in ("fwd", "ring_partials")]
+        roof["traffic"] = sum(tr) / 2 if None not in tr else None
+        roof["traffic_unit"] = "DRAM bytes per launch (ncu), mean of the 2 launches" \
+            if roof["traffic"] else None
     else:
         k0 = "fwd" if "fwd" in legs else "ring_partials"
         roof = roof_entry("attn_fwd_tc_kernel", cid, k0, "tensor", leg_stats[k0]["tflops"],
@@ -698,8 +703,7 @@ def run_ours(args, world, rank, local):
     if "ring_partials" in legs:
         roofs.append(roof_entry("attn_fwd_tc_kernel", cid, "ring_partials", "tensor",
                                 leg_stats["ring_partials"]["tflops"], peaks["bf16_tflops"],
-                                "TFLOP/s", prob.ring_flop, "FLOP", len(prob.ring_pairs),
-                                traffic_map))
+                                "TFLOP/s", prob.ring_flop, "FLOP", 1, traffic_map))
     if "bwd" in legs:
         roofs.append(roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd",
                                 "tensor", leg_stats["bwd"]["tflops"], peaks["bf16_tflops"],
