@@ -59,6 +59,8 @@ CONFIG_LEGS = {2: ("fwd", "bwd", "ring_partials", "merge", "permute"),
                5: ("fwd", "bwd")}
 RING_SHARDS = 8
 PERMUTE_GROUPS = 8
+DS_CACHE = True                    # backward dS cache (--no-ds-cache turns it off)
+DS_CACHE_MAX = 32 << 30            # largest dS cache the bench allocates, bytes
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -189,6 +191,8 @@ class ClockSampler:
 KERNEL_SOURCES = {"attn_fwd_tc_kernel": "attn_fwd_tc.cu", "attn_bwd_dkdv_tc_kernel": "attn_bwd_tc.cu",
                   "attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu",
                   "attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel": "attn_bwd_tc.cu",
+                  "attn_bwd_dq_cached_kernel": "attn_bwd_tc.cu",
+                  "attn_bwd_dkdv_tc_kernel+attn_bwd_dq_cached_kernel": "attn_bwd_tc.cu",
                   "lse_merge_kernel": "merge.cu", "permute_vec_kernel": "permute.cu"}
 
 
@@ -281,8 +285,16 @@ class Problem:
         self.dv = torch.empty_like(self.v) if has_bwd else None
         self.ws_f = torch.empty(nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, d),
                                 dtype=torch.uint8, device=dev)
-        self.ws_b = torch.empty(nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, nsp.NSP_BF16)
-                                if has_bwd else 16, dtype=torch.uint8, device=dev)
+        # the backward's dS cache: every visible tile pair's dS kept in HBM, so
+        # that dQ takes one product per pair instead of recomputing S and dP
+        # (when it fits DS_CACHE_MAX; config 4's 256K-token document needs TBs)
+        self.ds_cache_bytes = 0
+        if has_bwd and DS_CACHE:
+            need = nsp.nsp_attn_bwd_ds_cache_size(w.cu_seqlens, Hq, True)
+            if 0 < need <= DS_CACHE_MAX:
+                self.ds_cache_bytes = need
+        self.ws_b = (nsp.bwd_workspace(T, Hq, Hkv, d, dev, ds_cache_bytes=self.ds_cache_bytes)
+                     if has_bwd else torch.empty(16, dtype=torch.uint8, device=dev))
         # ring legs
         self.bounds = shard_bounds(T, RING_SHARDS)
         self.ring_pairs = (allowed_pairs_blocks(w.cu_seqlens, self.bounds)
@@ -580,6 +592,7 @@ def sub_config(nsp, cid, device, stream, flush, peaks, clocks, K, warmup, traffi
            "legs": leg_records(prob, legs, peaks), "clocks": clocks.summary(t0, t1),
            "gpu_launches_per_step": lps,
            "attention_launches_per_step": prob.path_per_step,
+           "bwd_ds_cache": ds_cache_record(prob),
            "data": "synthetic (seeded lengths; Q/K/V/dOut N(0,1) drawn on the GPU, bf16)"}
     roofs = []
     if "fwd" in legs:
@@ -587,7 +600,7 @@ def sub_config(nsp, cid, device, stream, flush, peaks, clocks, K, warmup, traffi
                                 rec["legs"]["fwd"]["tflops"], peaks["bf16_tflops"], "TFLOP/s",
                                 prob.fwd_flop, "FLOP", 1, traffic_map))
     if "bwd" in legs:
-        roofs.append(roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd",
+        roofs.append(roof_entry(bwd_kernels(prob), cid, "bwd",
                                 "tensor", rec["legs"]["bwd"]["tflops"], peaks["bf16_tflops"],
                                 "TFLOP/s", prob.bwd_flop, "FLOP", 1, traffic_map))
     if "ring_partials" in legs:
@@ -611,7 +624,7 @@ def sub_config(nsp, cid, device, stream, flush, peaks, clocks, K, warmup, traffi
         roofs = [roof_entry("attn_fwd_tc_kernel", cid, "fwd", "hbm",
                             rec["legs"]["fwd"]["gbs_compulsory"], peaks["hbm_gbs"], "GB/s",
                             cost["fwd_bytes"], "compulsory bytes", 1, traffic_map),
-                 roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd", "hbm",
+                 roof_entry(bwd_kernels(prob), cid, "bwd", "hbm",
                             rec["legs"]["bwd"]["gbs_compulsory"], peaks["hbm_gbs"], "GB/s",
                             cost["bwd_bytes"], "compulsory bytes", 1, traffic_map)]
     if cid == 3 and not getattr(sub_config, "skip_extra", False):
@@ -705,7 +718,7 @@ def run_ours(args, world, rank, local):
                                 leg_stats["ring_partials"]["tflops"], peaks["bf16_tflops"],
                                 "TFLOP/s", prob.ring_flop, "FLOP", 1, traffic_map))
     if "bwd" in legs:
-        roofs.append(roof_entry("attn_bwd_dkdv_tc_kernel+attn_bwd_dq_tc_kernel", cid, "bwd",
+        roofs.append(roof_entry(bwd_kernels(prob), cid, "bwd",
                                 "tensor", leg_stats["bwd"]["tflops"], peaks["bf16_tflops"],
                                 "TFLOP/s", prob.bwd_flop, "FLOP", 1, traffic_map))
     for k, kern in (("merge", "lse_merge_kernel"), ("permute", "permute_vec_kernel")):
@@ -769,6 +782,7 @@ def run_ours(args, world, rank, local):
                        "ring_shards": RING_SHARDS, "permute_groups": PERMUTE_GROUPS,
                        "step": " + ".join(CONFIG_LEGS[cid]),
                        "l2": "flushed (256 MiB write) before every timed step",
+                       "bwd_ds_cache": ds_cache_record(prob),
                        "parallelism": f"replicas x{world}"},
             "useful_flop_per_step": useful,
             "legs": leg_stats,
@@ -786,6 +800,22 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def bwd_kernels(prob) -> str:
+    """The backward's two tensor-core kernels (dQ from the dS cache when the
+    step gives it one)."""
+    dq = "attn_bwd_dq_cached_kernel" if prob.ds_cache_bytes else "attn_bwd_dq_tc_kernel"
+    return "attn_bwd_dkdv_tc_kernel+" + dq
+
+
+def ds_cache_record(prob):
+    """The backward's dS cache as the step used it (bytes; whether the
+    device-side check found room for every tile pair)."""
+    if prob.dq is None:
+        return None
+    used = prob.nsp.nsp_bwd_ds_cache_used(prob.ws_b) if prob.ds_cache_bytes else False
+    return {"bytes": int(prob.ds_cache_bytes), "used": bool(used)}
 
 
 def _time_leg(fn, stream, flush, reps):
@@ -992,7 +1022,11 @@ def main():
                     help="skip the sub-records of configs 3, 4 and 5")
     ap.add_argument("--config", type=int, choices=sorted(CONFIG_LEGS), default=CONFIG_ID,
                     help="workload (default: config 2, the bench workload)")
+    ap.add_argument("--no-ds-cache", action="store_true",
+                    help="backward without the dS cache (dQ recomputes S and dP)")
     args = ap.parse_args()
+    global DS_CACHE
+    DS_CACHE = not args.no_ds_cache
     if args.warmup < 3 and args.impl == "ours":
         print("bench: --warmup raised to 3 (minimum)", file=sys.stderr)
         args.warmup = 3

@@ -347,9 +347,34 @@ int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  * dk, dv each written once, deterministic); other shapes run on CUDA cores,
  * whose dq is summed with float atomics in a float32 accumulator that the
  * workspace then also holds (last bits may vary).
+ *
+ * dS cache (tensor-core path only).  Workspace bytes past
+ * nsp_attn_bwd_workspace_size (from the next 1024-byte boundary on) are a
+ * cache for dS = P (dP - delta), the probabilities' gradient: when it holds
+ * every visible (128-row query tile, 128-key tile) pair of every query head
+ * (nsp_attn_bwd_ds_cache_size bytes), the dK/dV kernel copies each dS tile
+ * it builds into the cache and dq is computed from the cached tiles (one
+ * 128 x 128 x 128 product per pair instead of recomputing S and dP: three).
+ * Otherwise, or with no such bytes, dq recomputes them.  The decision is
+ * taken on the device from cu_seqlens; results agree within rounding (dq
+ * then uses the dS rounded to bf16 that dk uses; deterministic either way).
  * ---------------------------------------------------------------------- */
 size_t nsp_attn_bwd_workspace_size(int64_t T, int32_t Hq, int32_t Hkv, int32_t d,
                                    int32_t io_dtype);
+
+/* Bytes of dS cache that let nsp_attn_bwd / nsp_attn_bwd_headgroups compute
+ * dq from cached tiles: Hq x (visible 128 x 128 tile pairs) x 32768, from
+ * HOST cu_seqlens [ndoc + 1] (int32, non-decreasing from 0).  Pass at least
+ * nsp_attn_bwd_workspace_size rounded up to 1024, plus this, as the
+ * workspace.  0 for a bad argument. */
+size_t nsp_attn_bwd_ds_cache_size(const int32_t* cu_seqlens_host, int32_t ndoc, int32_t Hq,
+                                  int32_t causal);
+
+/* Whether the last backward on this workspace computed dq from the dS cache:
+ * *used = 1 or 0, read from the workspace header (a copy to the host on
+ * stream, then a synchronisation of stream).  NSP_ERR_CUDA if the copy
+ * fails. */
+int32_t nsp_bwd_ds_cache_used(const void* workspace, int32_t* used, nsp_stream_t stream);
 
 int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, const int32_t* cu_seqlens,

@@ -119,6 +119,36 @@ def test_attn_pairs_counts_allowed_pairs(lib):
         nsp.nsp_attn_pairs(np.array([0, 5, 3], dtype=np.int32))
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_ds_cache_size_matches_enumeration(lib, causal):
+    """nsp_attn_bwd_ds_cache_size = Hq x (128-row query tile, 128-key tile)
+    pairs holding at least one visible (query, key) pair x 32768 bytes, by
+    enumerating the pairs of ragged streams (empty and one-token documents,
+    documents that end inside and on tile edges)."""
+    rng = np.random.default_rng(41)
+    cases = [[1], [128], [129], [0, 5, 0, 260, 0, 1], [300, 77, 150], [33] * 20,
+             [127, 1, 128, 256, 3]]
+    cases += [list(rng.integers(0, 400, rng.integers(1, 9))) for _ in range(6)]
+    for lens in cases:
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        doc = np.repeat(np.arange(len(lens)), lens)
+        nt = (T + 127) // 128
+        pairs = 0
+        for i in range(nt):
+            for j in range(nt):
+                t = np.arange(i * 128, min(T, i * 128 + 128))
+                s = np.arange(j * 128, min(T, j * 128 + 128))
+                vis = doc[t][:, None] == doc[s][None, :]
+                if causal:
+                    vis &= s[None, :] <= t[:, None]
+                pairs += bool(vis.any())
+        assert nsp.nsp_attn_bwd_ds_cache_size(cu, 6, causal) == 6 * pairs * 32768, lens
+    assert nsp.nsp_attn_bwd_ds_cache_size(np.array([0, 5, 3], dtype=np.int32), 4) == 0
+    assert nsp.nsp_attn_bwd_ds_cache_size(np.array([1, 5], dtype=np.int32), 4) == 0
+    assert nsp.nsp_attn_bwd_ds_cache_size(np.array([0, 5], dtype=np.int32), 0) == 0
+
+
 def test_accumulate_rejects_on_host(lib):
     """nsp_attn_fwd_accumulate: lse_acc is required and 16-byte aligned, and
     the scale must be positive; all three are refused before any launch."""

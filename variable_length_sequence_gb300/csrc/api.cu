@@ -442,6 +442,49 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
   return NSP_OK;
 }
 
+// Workspace bytes past the layout, from the next 1024-byte boundary, are the
+// whole-stream tensor-core backward's dS cache.
+static void attach_ds_cache(BwdWsLayout& L, size_t workspace_bytes) {
+  const size_t base = align_up(L.total, 1024);
+  if (workspace_bytes >= base + kDsTileBytes) {
+    L.ds_cache = base;
+    L.ds_cache_bytes = workspace_bytes - base;
+  }
+}
+
+size_t nsp_attn_bwd_ds_cache_size(const int32_t* cu, int32_t ndoc, int32_t Hq, int32_t causal) {
+  if (cu == nullptr || ndoc < 1 || Hq < 1 || cu[0] != 0) return 0;
+  for (int32_t b = 0; b < ndoc; ++b)
+    if (cu[b] > cu[b + 1]) return 0;
+  // the backward schedule's rule: query tile [r0, r1] sees the key tiles
+  // from its first row's document start to r1 (causal) or to the end of its
+  // last row's document
+  const int64_t T = cu[ndoc];
+  int64_t pairs = 0;
+  int32_t b0 = 0;
+  for (int64_t r0 = 0; r0 < T; r0 += kTileM) {
+    const int64_t r1 = (r0 + kTileM < T ? r0 + kTileM : T) - 1;
+    while (cu[b0 + 1] <= r0) ++b0;
+    int32_t b1 = b0;
+    while (cu[b1 + 1] <= r1) ++b1;
+    const int64_t lo = cu[b0], hi = causal ? r1 + 1 : (int64_t)cu[b1 + 1];
+    if (hi > lo) pairs += (hi - 1) / kBwdSub - lo / kBwdSub + 1;
+  }
+  return (size_t)pairs * (size_t)Hq * kDsTileBytes;
+}
+
+int32_t nsp_bwd_ds_cache_used(const void* workspace, int32_t* used, nsp_stream_t stream) {
+  if (!workspace || !used) return NSP_ERR_INVALID;
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(workspace);
+  int32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, &hdr->ds_on, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  *used = v;
+  return NSP_OK;
+}
+
 int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                      const void* dout, const float* lse, const int32_t* cu_seqlens,
                      int32_t ndoc, int64_t T, int32_t Hq, int32_t Hkv, int32_t d, float scale,
@@ -454,7 +497,8 @@ int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* ou
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
   const bool tc = bwd_tc_eligible(io_dtype, d, Hq, Hkv);
-  const BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
+  BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
+  if (tc) attach_ds_cache(L, workspace_bytes);
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;
@@ -483,7 +527,8 @@ int32_t nsp_attn_bwd_headgroups(const void* q, const void* k, const void* v, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
   const bool tc = bwd_tc_eligible(io_dtype, d, Hq, Hkv);
-  const BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
+  BwdWsLayout L = bwd_ws_layout(T, T, Hq, d, !tc);
+  if (tc) attach_ds_cache(L, workspace_bytes);
   AttnProblem p;
   p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens; p.ndoc = ndoc;
   p.q_start = 0; p.q_len = T; p.kv_start = 0; p.kv_len = T;

@@ -190,6 +190,12 @@ struct BwdArgs {
   const int* qorder;
   const int2* ktiles;     // per 128-key tile: first/last 128-row query tile
   const int* korder;
+  // dS cache (whole-stream call, header flag ds_on): the dK/dV kernel copies
+  // every dS^T tile it builds to slot h * ds_pairs + qoff[i] + (key tile -
+  // first key tile of query tile i), and the dQ kernel of the cache reads
+  // them instead of recomputing S and dP
+  uint8_t* ds_cache;
+  const int64_t* qoff;
 };
 
 // Block of a batched call's scheduled tile t: the largest index whose first
@@ -230,6 +236,7 @@ struct __align__(1024) SmemKV {
   uint64_t item_full[2], item_empty[2];
   KvItem items[2];
   uint64_t drain1, drain2;      // each MMA stream's own barrier for its final drain
+  uint64_t ds_stored;           // dS cache: the copy of the previous dS^T has left ds
   uint32_t tmem_base;
   WaitCtl wait;
 };
@@ -280,6 +287,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(&sm.dkv_empty, kKvSoftmaxWarps);
     mbar_init(&sm.drain1, 1);
     mbar_init(&sm.drain2, 1);
+    mbar_init(&sm.ds_stored, 1);
     wait_ctl_init(&sm.wait, p.wait_budget);
     fence_mbar_init();
   }
@@ -304,6 +312,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int n_per_tile = p.Hkv * a.hsplit;   // items per key tile
   const int n_items = hdr->n_items2 * n_per_tile;
   const int heads_per_item = G / a.hsplit;
+  // the schedule found room for every visible tile pair's dS in the cache
+  const bool ds_on =
+      !MULTI && a.ds_cache != nullptr && *((volatile const int32_t*)&hdr->ds_on) != 0;
+  const int64_t ds_pairs = ds_on ? *((volatile const int64_t*)&hdr->ds_pairs) : 0;
 
   if (warp >= 16) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kKvRegsControl));
@@ -457,7 +469,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (lane == 0) {
         const uint32_t ds_s = smem_u32(sm.ds);
         uint32_t it_count = 0, items_done = 0, qc = 0;
-        bool ok = true;
+        bool ok = true, ds_pending = false;
         while (ok) {
           const uint32_t slot = it_count & 1;
           if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
@@ -468,7 +480,26 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (it.steps == 0) continue;
           for (int n = 0; n < it.steps; ++n) {
             const uint32_t sq = qc & 3, sd = (qc + 2) & 3, fp = (qc >> 1) & 1, rb = qc & 1;
+            uint8_t* ds_dst = nullptr;               // this step's dS slot
+            if (ds_on) {
+              const int hh = n / it.n_q;
+              const int i = it.i_lo + (n - hh * it.n_q);
+              const int2 tr = __ldg(a.qtiles + i);
+              const int kofs = it.ktile - tr.x;      // < the tile's listed count (schedules agree)
+              if (kofs >= 0 && kofs <= tr.y - tr.x)
+                ds_dst = a.ds_cache +
+                         ((int64_t)(it.h0 + hh) * ds_pairs + __ldg(a.qoff + i) + kofs) *
+                             (int64_t)kTile;
+              else
+                atomicCAS(&hdr->status, 0, (int32_t)NSP_ERR_INVALID);   // no copy out of bounds
+            }
             if (!mbar_wait(&sm.p_ready[rb], fp, wc, hdr)) { ok = false; break; }
+            if (ds_pending) {
+              // the copy of the previous dS^T has read its shared memory
+              bulk_wait_read_all();
+              mbar_arrive(&sm.ds_stored);
+              ds_pending = false;
+            }
             if (n == 0 && items_done > 0 &&
                 !mbar_wait(&sm.dkv_empty, (items_done - 1) & 1, wc, hdr)) {
               ok = false;
@@ -497,12 +528,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             mma_commit(&sm.dk_done);
             mma_commit(&sm.slot_empty[sq]);
+            if (ds_on) {
+              if (ds_dst != nullptr) {
+                bulk_store(ds_dst, sm.ds, kTile);
+                bulk_commit();
+              }
+              ds_pending = true;
+            }
             ++qc;
           }
           if (!ok) break;
           mma_commit(&sm.dkv_full);
           ++items_done;
         }
+        if (ds_on) bulk_wait_all();       // the cached dS is in memory before the CTA exits
         mma_drain(&sm.drain2);
       }
     }
@@ -676,8 +715,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.dp_free);
-        // the dS^T buffer is free once dK has read the previous one
+        // the dS^T buffer is free once dK (and the cache copy) have read the previous one
         if (qc >= 1 && !mbar_wait_warp(&sm.dk_done, (qc - 1) & 1, wc, hdr)) { ok = false; break; }
+        if (ds_on && qc >= 1 && !mbar_wait_warp(&sm.ds_stored, (qc - 1) & 1, wc, hdr)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int j = (k >> 1) & 3;
@@ -797,7 +840,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // complete.  It reads nothing the dK/dV kernel writes, so it starts on the
   // SMs that kernel frees and waits for it only before it exits (work after
   // this call in the stream then also follows the dK/dV kernel).
-  if (status_bad(hdr)) {
+  // (with the dS cache in use, the cache's dQ kernel does this call's dQ)
+  if (status_bad(hdr) ||
+      (a.ds_cache != nullptr && *((volatile const int32_t*)&hdr->ds_on) != 0)) {
     grid_dep_wait();
     return;
   }
@@ -1169,6 +1214,222 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();
 }
 
+// ================================================================ dQ from the dS cache
+//
+// dQ = scale dS K with dS read back from the cache the dK/dV kernel filled:
+// one 128 x 128 x 128 product per visible (query tile, key tile) pair
+// instead of three.  Work item: one 128-row query tile of one query head
+// (the dQ kernel's items and order); its cached tiles are consecutive
+// slots.  Warps 0-3 write dQ (TMEM lane = query row), warp 4 loads (a bulk
+// copy of the cached tile, a TMA load of K), one thread of warp 5 issues the
+// products into one of two TMEM accumulators (items alternate, so the
+// epilogue of one item overlaps the products of the next).  The cached tile
+// is dS^T as the dK/dV kernel laid it out ([query block][key][64 queries],
+// 128-byte swizzle): for dQ it is the A operand in MN-major form, with the
+// same descriptor as K, the MN-major B operand.
+
+constexpr int kCqThreads = 192;
+constexpr int kCqWarpProducer = 4, kCqWarpMma = 5;
+constexpr int CQ_NS = 3;
+constexpr uint32_t kIdescMM = idesc_bf16_f32(128, 128, true, true);   // A, B MN-major
+
+struct __align__(1024) SmemCQ {
+  uint8_t ds[CQ_NS][kTile];
+  uint8_t k[CQ_NS][kTile];
+  uint64_t full[CQ_NS], empty[CQ_NS];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t item_full[2], item_empty[2];
+  QItem items[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  WaitCtl wait;
+};
+static_assert(sizeof(SmemCQ) <= kSmemLimit, "cached-dS tile set exceeds shared memory");
+
+__global__ void __launch_bounds__(kCqThreads, 1)
+    attn_bwd_dq_cached_kernel(const __grid_constant__ CUtensorMap tm_k, const BwdArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const AttnProblem& p = a.p;
+  WsHeader* hdr = p.hdr;
+  grid_dep_wait();                          // the dK/dV kernel (and its cache copies) are done
+  if (status_bad(hdr) || *((volatile const int32_t*)&hdr->ds_on) == 0) return;
+  SmemCQ* smp = smem_view<SmemCQ>(smem_raw, hdr);
+  if (smp == nullptr) return;
+  SmemCQ& sm = *smp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < CQ_NS; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 4);          // one arrival per epilogue warp
+      mbar_init(&sm.item_full[b], 1);
+      mbar_init(&sm.item_empty[b], 1 + 4);     // MMA thread and the epilogue warps
+    }
+    mbar_init(&sm.drain, 1);
+    wait_ctl_init(&sm.wait, p.wait_budget);
+    fence_mbar_init();
+  }
+  if (warp == kCqWarpMma) {
+    tmem_alloc(&sm.tmem_base, 256);
+    tmem_relinquish();
+  }
+  if (warp == kCqWarpProducer && lane == 0) tma_prefetch_desc(&tm_k);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = sm.tmem_base;
+  WaitCtl* const wc = &sm.wait;
+  const int G = p.Hq / p.Hkv;
+  const int n_items = hdr->n_items * p.Hq;
+  const int64_t ds_pairs = *((volatile const int64_t*)&hdr->ds_pairs);
+
+  if (warp == kCqWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it_count = 0, loads = 0;
+      bool ok = true;
+      while (ok) {
+        const int idx = atomicAdd(&hdr->counter, 1);
+        QItem it;
+        it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1; it.blk = 0;
+        if (idx < n_items) {
+          const int qt = a.qorder[idx / p.Hq];
+          const int2 tr = a.qtiles[qt];
+          it.qtile = qt;
+          it.h = idx - (idx / p.Hq) * p.Hq;
+          it.g = it.h / G;
+          it.j_lo = tr.x;
+          it.n_kv = tr.y - tr.x + 1;
+        }
+        const uint32_t slot = it_count & 1;
+        if (it_count >= 2 &&
+            !mbar_wait(&sm.item_empty[slot], ((it_count >> 1) - 1) & 1, wc, hdr)) {
+          ok = false;
+          break;
+        }
+        sm.items[slot] = it;
+        mbar_arrive(&sm.item_full[slot]);
+        ++it_count;
+        if (it.n_kv <= 0) {
+          if (it.n_kv < 0) break;
+          continue;
+        }
+        // the item's cached tiles: consecutive slots from qoff[qtile]
+        const uint8_t* src =
+            a.ds_cache + ((int64_t)it.h * ds_pairs + a.qoff[it.qtile]) * (int64_t)kTile;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = loads % CQ_NS, use = loads / CQ_NS;
+          if (use >= 1 && !mbar_wait(&sm.empty[st], (use - 1) & 1, wc, hdr)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.full[st], 2 * kTile);
+          bulk_load(sm.ds[st], src + (int64_t)jj * kTile, kTile, &sm.full[st]);
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.full[st], it.g * HD + cb * 64,
+                        (it.j_lo + jj) * 128);
+          ++loads;
+        }
+      }
+      // leaving, normally or on an abort: every issued copy lands first
+      for (uint32_t j = (loads > CQ_NS ? loads - CQ_NS : 0); j < loads; ++j)
+        drain_wait(&sm.full[j % CQ_NS], (j / CQ_NS) & 1);
+    }
+  } else if (warp == kCqWarpMma) {
+    // ------------------------------------------------------------ dQ += dS K
+    if (lane == 0) {
+      uint32_t it_count = 0, items_done = 0, used = 0;
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = it_count & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
+        const QItem it = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        ++it_count;
+        if (it.n_kv < 0) break;
+        if (it.n_kv == 0) continue;
+        const uint32_t b = items_done & 1;
+        // accumulator b is free once the epilogue has read it two items ago
+        if (items_done >= 2 &&
+            !mbar_wait(&sm.acc_empty[b], ((items_done >> 1) - 1) & 1, wc, hdr))
+          break;
+        for (int jj = 0; jj < it.n_kv; ++jj) {
+          const uint32_t st = used % CQ_NS, use = used / CQ_NS;
+          if (!mbar_wait(&sm.full[st], use & 1, wc, hdr)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(smem_u32(sm.ds[st]), kBlk, 1024);
+          const uint64_t bd = smem_desc_sw128(smem_u32(sm.k[st]), kBlk, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)        // 16 keys per product, 2048 bytes apart
+            mma_ss(tmem + 128 * b, ad + ((kk * 2048) >> 4), bd + ((kk * 2048) >> 4), kIdescMM,
+                   (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&sm.empty[st]);
+          ++used;
+        }
+        if (!ok) break;
+        mma_commit(&sm.acc_full[b]);
+        ++items_done;
+      }
+      mma_drain(&sm.drain);               // every product done before TMEM is freed
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ dQ epilogue
+    const int r = warp * 32 + lane;                        // TMEM lane = query row
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int64_t T = p.q_len;
+    uint32_t it_count = 0, items_done = 0;
+    while (true) {
+      const uint32_t slot = it_count & 1;
+      if (!mbar_wait_warp(&sm.item_full[slot], (it_count >> 1) & 1, wc, hdr)) break;
+      const QItem it = sm.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
+      ++it_count;
+      if (it.n_kv < 0) break;
+      const int64_t row = (int64_t)it.qtile * 128 + r;
+      const bool valid = row < T;
+      __nv_bfloat16* dst = a.dq + qo_offset(p, row, it.h);
+      if (it.n_kv == 0) {
+        // no visible key (not met in a whole stream): zero rows
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+        if (valid)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
+        continue;
+      }
+      const uint32_t b = items_done & 1;
+      if (!mbar_wait_warp(&sm.acc_full[b], (items_done >> 1) & 1, wc, hdr)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + 128 * b + c * 32, v);
+        tmem_wait_ld();
+        if (valid) store_row32_bf16(dst + c * 32, v, p.scale);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+      ++items_done;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kCqWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 // ================================================================ host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1237,6 +1498,11 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   a.qorder = reinterpret_cast<const int*>(ws + L.qorder);
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);
   a.korder = reinterpret_cast<const int*>(ws + L.korder);
+  // dS cache: whole-stream calls given workspace past the layout (the
+  // schedule decides whether every visible pair's dS fits)
+  const bool cache = blocks == nullptr && !p.accumulate && L.ds_cache_bytes > 0;
+  a.ds_cache = cache ? reinterpret_cast<uint8_t*>(ws + L.ds_cache) : nullptr;
+  a.qoff = reinterpret_cast<const int64_t*>(ws + L.qoff);
   const int grid = persistent_grid();
   // A ring block has few key tiles: split each (key tile, KV head) item over
   // query-head subsets until there are two items per SM (the subsets add
@@ -1265,6 +1531,18 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   count_launches(1);
   count_path(true);
   if (e != cudaSuccess) return e;
+  if (cache) {
+    // exactly one of the two dQ kernels does the work (header flag ds_on)
+    constexpr size_t cq_bytes = smem_bytes<SmemCQ>();
+    e = cudaFuncSetAttribute(attn_bwd_dq_cached_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)cq_bytes);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(attn_bwd_dq_cached_kernel, dim3(grid), dim3(kCqThreads), cq_bytes, s, mk,
+                         a);
+    count_launches(1);
+    count_path(true);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 

@@ -18,7 +18,9 @@ struct WsHeader {
   int32_t counter2;     // second work counter (backward dK/dV)
   int32_t n_items2;
   int32_t n_nonempty;   // query tiles that see a key (listed first in the order)
-  int32_t pad[57];      // header is 256 bytes
+  int32_t ds_on;        // backward: dS of every visible tile pair fits the cache
+  int64_t ds_pairs;     // backward: visible (query tile, key tile) pairs per head
+  int32_t pad[54];      // header is 256 bytes
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must stay 256 bytes");
 
@@ -114,7 +116,11 @@ struct BwdWsLayout {
   size_t delta;                    // float [Hq, Tp]
   size_t nlse2;                     // float [Hq, Tp]
   size_t dq_acc;                   // float [q_len, Hq, d] (CUDA-core path)
+  size_t qoff;                     // int64 [n_qtiles]: first dS slot of each query tile
   size_t total;
+  // dS cache (whole-stream tensor-core backward): the workspace bytes past
+  // total, from ds_cache on (0 bytes: dQ recomputes S and dP)
+  size_t ds_cache = 0, ds_cache_bytes = 0;
   int64_t Tp, n_qtiles, n_ktiles;
   int64_t n_qhist, n_khist;        // counting-sort buckets of the two schedules
 };
@@ -139,6 +145,7 @@ inline BwdWsLayout bwd_ws_layout(int64_t q_len, int64_t kv_len, int32_t Hq, int3
   L.dq_acc = off;
   if (need_dq_acc)
     off = align_up(off + sizeof(float) * (size_t)q_len * (size_t)Hq * (size_t)d, 256);
+  L.qoff = off;   off = align_up(off + sizeof(int64_t) * (size_t)L.n_qtiles, 256);
   L.total = off;
   return L;
 }
@@ -176,9 +183,13 @@ inline BwdWsLayout bwd_ws_layout_blocks(FwdBlocks& B, int64_t T, int32_t Hq) {
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.nlse2 = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off;
+  L.qoff = off;
   L.total = off;
   return L;
 }
+
+// Bytes of one cached dS tile: 128 x 128 bf16.
+constexpr size_t kDsTileBytes = 128 * 128 * 2;
 
 // Problem description passed by value to kernels.
 struct AttnProblem {

@@ -55,6 +55,12 @@ struct SchedArgs {
   // with the largest ktile0 <= i (the range fields above are then unused)
   FwdBlocks blks;
   int32_t use_blocks;  // mode 1: take the key tiles of blks instead of the range fields
+  // mode 0 of a whole-stream backward with a dS cache: per query tile, the
+  // first of its dS slots (an exclusive prefix sum of the listed counts, in
+  // tile order); the header records whether Hq heads' slots fit the cache
+  int64_t* qoff;
+  int64_t ds_cache_bytes;
+  int32_t Hq;
 };
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_constant__ SchedArgs a) {
@@ -62,6 +68,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
   __shared__ int s_bad;
   __shared__ int s_max;
   __shared__ int s_warp[kSchedThreads / 32];
+  __shared__ long long s_warp64[kSchedThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int* const hist = a.n_buckets <= kSmemBuckets ? s_hist_dyn : a.hist;
   grid_dep_trigger();                       // the attention kernel may launch (it waits)
@@ -91,6 +98,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
         a.hdr->n_items = 0; a.hdr->counter = 0;
         a.hdr->n_items2 = 0; a.hdr->counter2 = 0;
         a.hdr->max_cost = 0; a.hdr->n_nonempty = 0;
+        a.hdr->ds_on = 0; a.hdr->ds_pairs = 0;
       }
       return;
     }
@@ -155,6 +163,48 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
     atomicMax(&s_max, cost);
   }
   __syncthreads();
+
+  if (a.mode == 0 && !a.second) {
+    // dS slots: thread t owns a contiguous run of tiles; block-wide scan of
+    // the runs' listed counts
+    const int per_t = (a.n_tiles + kSchedThreads - 1) / kSchedThreads;
+    const int t_begin = min(tid * per_t, a.n_tiles), t_end = min(t_begin + per_t, a.n_tiles);
+    long long cnt = 0;
+    for (int i = t_begin; i < t_end; ++i) cnt += a.tiles[i].y - a.tiles[i].x + 1;
+    long long xs = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) xs += y;
+    }
+    if (lane == 31) s_warp64[wid] = xs;
+    __syncthreads();
+    if (wid == 0) {
+      long long w = s_warp64[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      s_warp64[lane] = w;
+    }
+    __syncthreads();
+    if (a.qoff != nullptr) {
+      long long run = xs - cnt + (wid > 0 ? s_warp64[wid - 1] : 0);
+      for (int i = t_begin; i < t_end; ++i) {
+        a.qoff[i] = run;
+        run += a.tiles[i].y - a.tiles[i].x + 1;
+      }
+    }
+    if (tid == 0) {
+      const long long pairs = s_warp64[kSchedThreads / 32 - 1];
+      const long long cap = a.qoff != nullptr && a.Hq > 0
+                                ? a.ds_cache_bytes / ((long long)a.Hq * (long long)kDsTileBytes)
+                                : -1;
+      a.hdr->ds_pairs = pairs;
+      a.hdr->ds_on = pairs <= cap ? 1 : 0;
+    }
+  }
 
   // Exclusive scan in descending cost order: start[c] = sum_{c' > c} hist[c'].
   // Thread t owns a contiguous run of reversed bucket indices.
@@ -236,6 +286,7 @@ cudaError_t launch_fwd_schedule(const AttnProblem& p, const FwdWsLayout& L, char
   a.n_tiles = (int32_t)L.n_qtiles;
   a.n_buckets = (int32_t)L.n_kvtiles + 2;
   a.hdr = p.hdr; a.second = 0;
+  a.qoff = nullptr; a.ds_cache_bytes = 0; a.Hq = p.Hq;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   return cudaGetLastError();
 }
@@ -255,6 +306,11 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.n_tiles = (int32_t)L.n_qtiles;
   a.n_buckets = (int32_t)L.n_qhist;
   a.hdr = p.hdr; a.second = 0;
+  // the dS cache serves the whole-stream backward only
+  const bool cache = blocks == nullptr && !p.accumulate && L.ds_cache_bytes > 0;
+  a.qoff = cache ? reinterpret_cast<int64_t*>(ws + L.qoff) : nullptr;
+  a.ds_cache_bytes = cache ? (int64_t)L.ds_cache_bytes : 0;
+  a.Hq = p.Hq;
   schedule_kernel<<<1, kSchedThreads, sched_smem(a), s>>>(a); count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -70,6 +70,8 @@ _SIGNATURES = {
     "nsp_seq2head_permute_groups": (_i32, [_vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32,
                                            _vp]),
     "nsp_status_query": (_i32, [_vp, _vp]),
+    "nsp_attn_bwd_ds_cache_size": (_sz, [_vp, _i32, _i32, _i32]),
+    "nsp_bwd_ds_cache_used": (_i32, [_vp, C.POINTER(C.c_int32), _vp]),
     "nsp_attn_pairs": (_i32, [_vp, _i32, _i32, C.POINTER(C.c_double)]),
     "nsp_attn_cost": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                              _vp]),
@@ -370,6 +372,29 @@ def nsp_set_wait_timeout_cycles(cycles: int) -> int:
 
 def nsp_status_query(workspace, stream=None) -> int:
     return int(load().nsp_status_query(_ptr(workspace), _stream(stream)))
+
+
+def nsp_attn_bwd_ds_cache_size(cu_seqlens_host, Hq, causal=True) -> int:
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    return int(load().nsp_attn_bwd_ds_cache_size(cu.ctypes.data, len(cu) - 1, int(Hq),
+                                                 int(bool(causal))))
+
+
+def nsp_bwd_ds_cache_used(workspace, stream=None) -> bool:
+    used = C.c_int32(0)
+    _check("nsp_bwd_ds_cache_used",
+           load().nsp_bwd_ds_cache_used(_ptr(workspace), C.byref(used), _stream(stream)))
+    return bool(used.value)
+
+
+def bwd_workspace(T, Hq, Hkv, d, device, io_dtype=NSP_BF16, ds_cache_bytes=0):
+    """A backward workspace; ds_cache_bytes > 0 appends a dS cache of that
+    size (nsp_attn_bwd_ds_cache_size gives the size that holds every tile)."""
+    base = nsp_attn_bwd_workspace_size(T, Hq, Hkv, d, io_dtype)
+    if ds_cache_bytes > 0:
+        base = (base + 1023) // 1024 * 1024 + int(ds_cache_bytes)
+    return torch.empty(base, dtype=torch.uint8, device=device)
 
 
 def nsp_attn_pairs(cu_seqlens_host, causal=True) -> float:
