@@ -84,7 +84,7 @@ int64_t nsp_kernel_launches(void);
 /* Number of attention kernels (forward, dK/dV and dQ kernels) this library
  * has launched in this process on the tensor-core path (tensor_core = 1:
  * tcgen05, TMEM, TMA) or on the CUDA-core path (tensor_core = 0: float32
- * I/O, d = 64, or no tensor-map support in the driver).
+ * I/O, or no tensor-map support in the driver).
  * Lets a caller see which path its calls took. */
 int64_t nsp_path_launches(int32_t tensor_core);
 
@@ -130,11 +130,11 @@ int64_t nsp_set_wait_timeout_cycles(int64_t cycles);
  *   NULL when not needed); workspace device, at least
  *   nsp_attn_fwd_workspace_size(...) bytes, contents need no initialisation.
  *
- * Kernel choice: bf16 with d = 128 runs on the tensor cores (tcgen05, TMEM,
- * TMA), any Hq / Hkv (an even ratio pairs two query heads of a KV group per
- * work item, an odd one, multi-head attention among them, pairs two
- * adjacent query tiles of one head).  float32 I/O and d = 64 run on the
- * CUDA cores: a correct but much slower path (nsp_path_launches tells which
+ * Kernel choice: bf16 (d = 128 or 64) runs on the tensor cores (tcgen05,
+ * TMEM, TMA), any Hq / Hkv (an even ratio pairs two query heads of a KV
+ * group per work item, an odd one, multi-head attention among them, pairs
+ * two adjacent query tiles of one head).  float32 I/O runs on the CUDA
+ * cores: a correct but much slower path (nsp_path_launches tells which
  * ran).
  * ---------------------------------------------------------------------- */
 size_t nsp_attn_fwd_workspace_size(int64_t q_len, int64_t kv_len, int32_t Hq, int32_t Hkv,
@@ -207,7 +207,7 @@ int32_t nsp_attn_fwd_accumulate(const void* q, const void* k, const void* v,
  * arithmetic), without either permutation pass: the kernels address the
  * grouped rows directly (TMA coordinates of a [P T, (Hq/P) d] map).
  * P must divide Hq; P T must fit in int32.  Kernel choice as nsp_attn_fwd
- * (tensor cores for bf16, d = 128; CUDA cores otherwise).
+ * (tensor cores for bf16; CUDA cores for float32 I/O).
  * Other arguments and errors: as nsp_attn_fwd
  * with q_start = kv_start = 0, q_len = kv_len = T (workspace sized by
  * nsp_attn_fwd_workspace_size(T, T, ...)); a bad P is NSP_ERR_INVALID.
@@ -276,7 +276,7 @@ int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
  *     [T][Hkv][d]: every block's contributions are ADDED at global rows with
  *     float atomics (the caller zeroes them first; the order of the
  *     additions, hence the last bits, may vary between runs).
- * Tensor cores only: bf16 with d = 128 (other shapes: NSP_ERR_UNSUPPORTED;
+ * Tensor cores only: bf16 with d = 128 or 64 (float32: NSP_ERR_UNSUPPORTED;
  * use nsp_attn_bwd_accumulate per block).  Every q_start must be a multiple
  * of 4 (NSP_ERR_UNSUPPORTED otherwise).  Workspace: at least
  * nsp_attn_bwd_blocks_workspace_size(T, nranges, ranges, Hq, Hkv, d) bytes.
@@ -343,8 +343,8 @@ int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  * dq, dk, dv are written (not accumulated) in io_dtype.  The workspace (at
  * least nsp_attn_bwd_workspace_size bytes for the same T, heads, d and
  * io_dtype) holds the tile schedules, delta and lse * log2(e); its contents
- * need no initialisation.  bf16 with d = 128 runs on the tensor cores (dq,
- * dk, dv each written once, deterministic); other shapes run on CUDA cores,
+ * need no initialisation.  bf16 (d = 128 or 64) runs on the tensor cores
+ * (dq, dk, dv each written once, deterministic); float32 runs on CUDA cores,
  * whose dq is summed with float atomics in a float32 accumulator that the
  * workspace then also holds (last bits may vary).
  *
@@ -433,9 +433,9 @@ int32_t nsp_attn_bwd_headgroups(const void* q, const void* k, const void* v, con
  *   workspace: device, at least nsp_attn_bwd_accumulate_workspace_size(q_len,
  *     kv_len, ...) bytes, no initialisation.
  * Pairs no query of the block can see add nothing; a block with no visible
- * pair leaves the accumulators unchanged.  bf16 with d = 128 runs on the
+ * pair leaves the accumulators unchanged.  bf16 (d = 128 or 64) runs on the
  * tensor cores (each accumulator element read and written once per call);
- * other shapes run on CUDA cores (dq_acc summed with float atomics).
+ * float32 runs on CUDA cores (dq_acc summed with float atomics).
  * Errors: as nsp_attn_bwd (NULL or misaligned buffers, bad scalars before
  * any launch; a bad cu_seqlens through the workspace status word).
  * ---------------------------------------------------------------------- */

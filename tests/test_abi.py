@@ -220,9 +220,9 @@ def test_fwd_blocks_rejects_on_host(lib):
 
 
 def test_bwd_blocks_rejects_on_host(lib):
-    """nsp_attn_bwd_blocks: tensor-core shapes only, q_start a multiple of 4,
-    ranges inside [0, T), a workspace large enough; refused before any
-    launch."""
+    """nsp_attn_bwd_blocks: tensor-core shapes only (bf16, d = 64 or 128),
+    q_start a multiple of 4, ranges inside [0, T), a workspace large enough;
+    refused before any launch."""
     T = 1000
 
     def call(ranges, io=nsp.NSP_BF16, d=128, nr=None, ws=1 << 26):
@@ -233,7 +233,7 @@ def test_bwd_blocks_rejects_on_host(lib):
     ok = [(0, 500, 0, 500), (500, 500, 0, 1000)]
     assert nsp.nsp_attn_bwd_blocks_workspace_size(T, ok, 8, 2, 128) > 0
     assert call(ok, io=nsp.NSP_F32) == nsp.NSP_ERR_UNSUPPORTED
-    assert call(ok, d=64) == nsp.NSP_ERR_UNSUPPORTED
+    assert call(ok, d=96) == nsp.NSP_ERR_UNSUPPORTED               # head dimension 64 or 128
     assert call([(2, 10, 0, 10)]) == nsp.NSP_ERR_UNSUPPORTED       # q_start not a multiple of 4
     assert call([(0, 10, 995, 10)]) == nsp.NSP_ERR_INVALID         # keys past T
     assert call(ok, nr=0) == nsp.NSP_ERR_INVALID

@@ -320,7 +320,7 @@ int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
   bool launched = false;
   if (launch_attn_fwd_tc(p, L, ws, s, &launched, &B) != cudaSuccess) return NSP_ERR_CUDA;
   if (launched) return NSP_OK;
-  // CUDA-core path (float32 I/O, d = 64): one launch per block, on pointers
+  // CUDA-core path (float32 I/O): one launch per block, on pointers
   // to the block's own rows
   const size_t es = io_dtype == NSP_BF16 ? 2 : 4;
   for (int32_t i = 0; i < nblocks; ++i) {

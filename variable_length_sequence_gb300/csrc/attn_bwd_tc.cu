@@ -57,7 +57,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int HD = 128;
 constexpr int kThreads = 352;                        // dQ kernel
 constexpr int kKvThreads = 640;                      // dK/dV kernel: 16 softmax warps + 4
 constexpr int kKvSoftmaxWarps = 16;
@@ -70,26 +69,31 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr size_t kSmemLimit = 232448;
 
 constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);   // A, B K-major
-constexpr uint32_t kIdescKM = idesc_bf16_f32(128, 128, true, false);    // B MN-major
+// B MN-major, N = the head dimension D
+template <int D>
+__host__ __device__ constexpr uint32_t idesc_km() { return idesc_bf16_f32(128, D, true, false); }
 
-// D = A B^T, A and B K-major 128 x 128 tiles (128-byte swizzle), K = 128.
+// D = A B^T, A and B K-major 128-row tiles (128-byte swizzle), K = the
+// head dimension HK (128, or 64: the first column block only).
+template <int HK>
 __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
                                        bool accumulate) {
   const uint64_t ad = smem_desc_sw128(a_saddr, 16, 1024);
   const uint64_t bd = smem_desc_sw128(b_saddr, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+  for (int kk = 0; kk < HK / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
     mma_ss(d_tmem, ad + off, bd + off, kIdescKK, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
 // D (+)= A B, A from TMEM, B MN-major in shared memory (K along its rows,
-// 16 rows = 2048 B per step; N blocks 16 KB apart).  A holds bf16 pairs
-// written by the softmax warps in groups of QPG K-columns: group j sits at
-// TMEM columns a_tmem + j QPG + [0, QPG / 2), so K-step kk (16 columns, 8
-// TMEM columns) starts at (kk / (QPG / 16)) QPG + (kk % (QPG / 16)) 8.
-template <int QPG>
+// 16 rows = 2048 B per step; N = D columns, blocks of 64 16 KB apart).  A
+// holds bf16 pairs written by the softmax warps in groups of QPG K-columns:
+// group j sits at TMEM columns a_tmem + j QPG + [0, QPG / 2), so K-step kk
+// (16 columns, 8 TMEM columns) starts at (kk / (QPG / 16)) QPG +
+// (kk % (QPG / 16)) 8.
+template <int QPG, int D>
 __device__ __forceinline__ void mma_t_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
                                             bool accumulate) {
   constexpr int kSteps = QPG / 16;
@@ -97,7 +101,7 @@ __device__ __forceinline__ void mma_t_split(uint32_t d_tmem, uint32_t a_tmem, ui
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t a_col = (kk / kSteps) * QPG + (kk % kSteps) * 8;
-    mma_ts(d_tmem, a_tmem + a_col, bd + ((kk * 2048) >> 4), kIdescKM,
+    mma_ts(d_tmem, a_tmem + a_col, bd + ((kk * 2048) >> 4), idesc_km<D>(),
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -244,8 +248,11 @@ static_assert(sizeof(SmemKV) <= kSmemLimit, "dK/dV tile set exceeds shared memor
 
 // MULTI: a batched call (nsp_attn_bwd_blocks): the tiles of every block of
 // blks, rows addressed by global token ids, every contribution added into the
-// whole-stream float32 accumulators with atomics (no preload).
-template <bool MULTI>
+// whole-stream float32 accumulators with atomics (no preload).  D: the head
+// dimension, 128 or 64 (tiles of 64 columns use the first column block of
+// each tile buffer, dV and dK the first 64 of their TMEM columns, and the
+// column groups of the epilogue that would hold columns 64-127 idle).
+template <bool MULTI, int D>
 __global__ void __launch_bounds__(kKvThreads, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_do,
@@ -312,6 +319,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int n_per_tile = p.Hkv * a.hsplit;   // items per key tile
   const int n_items = hdr->n_items2 * n_per_tile;
   const int heads_per_item = G / a.hsplit;
+  constexpr int kBlocks = D / 64;                        // 64-column blocks of a row
+  constexpr uint32_t kLoad = kBlocks * kBlk;             // one Q, dOut, K or V tile
   // the schedule found room for every visible tile pair's dS in the cache
   const bool ds_on =
       !MULTI && a.ds_cache != nullptr && *((volatile const int32_t*)&hdr->ds_on) != 0;
@@ -358,15 +367,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * kLoad);
           // a batched call's maps span the whole stream (rows = global ids)
           const int k_base = MULTI ? blks.b[it.blk].kv_start : 0;
           const int q_base = MULTI ? blks.b[it.blk].q_start : 0;
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
-            tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * HD + cb * 64,
+          for (int cb = 0; cb < kBlocks; ++cb) {
+            tma_load_2d(sm.k + cb * kBlk, &tm_k, &sm.kv_full, it.g * D + cb * 64,
                         k_base + it.ktile * 128);
-            tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * HD + cb * 64,
+            tma_load_2d(sm.v + cb * kBlk, &tm_v, &sm.kv_full, it.g * D + cb * 64,
                         k_base + it.ktile * 128);
           }
           ++kv_count;
@@ -381,16 +390,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.slot_full[sq], kTile + 128 * sizeof(float));
+            mbar_arrive_expect_tx(&sm.slot_full[sq], kLoad + 128 * sizeof(float));
             // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
-            int qx = h * HD, qy = q_base + i * 128;
+            int qx = h * D, qy = q_base + i * 128;
             if (p.q_groups > 1) {
               const int hpg = p.Hq / p.q_groups, grp = h / hpg;
-              qx = (h - grp * hpg) * HD;
+              qx = (h - grp * hpg) * D;
               qy += (int)(grp * p.q_len);
             }
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb)
+            for (int cb = 0; cb < kBlocks; ++cb)
               tma_load_2d(sm.qd[sq] + cb * kBlk, &tm_q, &sm.slot_full[sq], qx + cb * 64, qy);
             const int64_t row = (int64_t)h * a.Tp + q_base + (int64_t)i * 128;
             bulk_load(sm.vec[sq], a.nlse2 + row, 128 * sizeof(float), &sm.slot_full[sq]);
@@ -400,9 +409,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.slot_full[sd], kTile + 128 * sizeof(float));
+            mbar_arrive_expect_tx(&sm.slot_full[sd], kLoad + 128 * sizeof(float));
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb)
+            for (int cb = 0; cb < kBlocks; ++cb)
               tma_load_2d(sm.qd[sd] + cb * kBlk, &tm_do, &sm.slot_full[sd], qx + cb * 64, qy);
             bulk_load(sm.vec[sd], a.delta + row, 128 * sizeof(float), &sm.slot_full[sd]);
             ++loads;
@@ -443,7 +452,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // region rb held the previous dP^T: free once the softmax has read it
             if (qc >= 1 && !mbar_wait(&sm.dp_free, (qc - 1) & 1, wc, hdr)) { ok = false; break; }
             tc_fence_after();
-            mma_kk(tmem + 128 * rb, k_s, smem_u32(sm.qd[sq]), false);         // S^T = K Q^T
+            mma_kk<D>(tmem + 128 * rb, k_s, smem_u32(sm.qd[sq]), false);      // S^T = K Q^T
             mma_commit(&sm.s_full);
             mma_commit(&sm.slot_empty[sq]);
             if (!mbar_wait(&sm.slot_full[sd], fp, wc, hdr)) { ok = false; break; }
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               break;
             }
             tc_fence_after();
-            mma_kk(tmem + 128 * (rb ^ 1), v_s, smem_u32(sm.qd[sd]), false);   // dP^T = V dOut^T
+            mma_kk<D>(tmem + 128 * (rb ^ 1), v_s, smem_u32(sm.qd[sd]), false);   // dP^T = V dOut^T
             mma_commit(&sm.dp_full);
             mma_commit(&sm.slot_empty[sd]);
             ++qc;
@@ -468,6 +477,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // ------------------------------------------------------------ stream 2: dV, dK
       if (lane == 0) {
         const uint32_t ds_s = smem_u32(sm.ds);
+        const uint64_t ds_pol = l2_evict_first_policy();   // cached dS: not read in this kernel
         uint32_t it_count = 0, items_done = 0, qc = 0;
         bool ok = true, ds_pending = false;
         while (ok) {
@@ -510,7 +520,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             // a ring block with one item per (key tile, KV head) adds onto the
             // preloaded running dK / dV
             const bool acc = n > 0 || (!MULTI && p.accumulate && a.hsplit == 1);
-            mma_t_split<32>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
+            mma_t_split<32, D>(tmem + 256, tmem + 128 * rb, smem_u32(sm.qd[sd]), acc);   // dV += P^T dOut
             mma_commit(&sm.dv_done[rb]);
             mma_commit(&sm.slot_empty[sd]);
             if (!mbar_wait(&sm.ds_ready, qc & 1, wc, hdr)) { ok = false; break; }
@@ -522,7 +532,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t aoff = ((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
-                mma_ss(tmem + 384, ad + aoff, bd + ((kk * 2048) >> 4), kIdescKM,
+                mma_ss(tmem + 384, ad + aoff, bd + ((kk * 2048) >> 4), idesc_km<D>(),
                        (acc || kk > 0) ? 1u : 0u);
               }
             }
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_commit(&sm.slot_empty[sq]);
             if (ds_on) {
               if (ds_dst != nullptr) {
-                bulk_store(ds_dst, sm.ds, kTile);
+                bulk_store(ds_dst, sm.ds, kTile, ds_pol);
                 bulk_commit();
               }
               ds_pending = true;
@@ -558,6 +568,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int cg = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                          // epilogue: TMEM lane = key row
+    // epilogue: column group cg & 1 holds head-dimension columns 64 (cg & 1) ..
+    const bool epi_cols = (cg & 1) * 64 < D;
     const int tr = lane >> 2, tc2 = 2 * (lane & 3);
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float sl2 = p.scale * kLog2e;
@@ -578,9 +590,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (it.steps == 0) {
         // no query of the range sees these keys: the whole-stream backward
         // writes zero rows (a ring block adds nothing)
-        if (!p.accumulate) {
+        if (!p.accumulate && epi_cols) {
           const int64_t key = (int64_t)it.ktile * 128 + r;
-          __nv_bfloat16* dst = (cg >= 2 ? a.dk : a.dv) + (key * p.Hkv + it.g) * HD + (cg & 1) * 64;
+          __nv_bfloat16* dst = (cg >= 2 ? a.dk : a.dv) + (key * p.Hkv + it.g) * D + (cg & 1) * 64;
           uint32_t z[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] = 0u;
@@ -611,13 +623,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           qhi[i] = (int)min(max(ghi - it_q_start, (int64_t)0), it_q_len);
         }
       }
-      if (!MULTI && p.accumulate && a.hsplit == 1) {
+      if (!MULTI && p.accumulate && a.hsplit == 1 && epi_cols) {
         // ring block, one item per (key tile, KV head): dV and dK start as the
         // running accumulators (dK / scale), TMEM lane = key row
         const int64_t key = (int64_t)it.ktile * 128 + r;
         const bool is_dk = cg >= 2;
         const float* src = key < n_keys ? (is_dk ? a.dk_acc : a.dv_acc) +
-                                              (key * p.Hkv + it.g) * HD + (cg & 1) * 64
+                                              (key * p.Hkv + it.g) * D + (cg & 1) * 64
                                         : nullptr;
         const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
         const float mul = is_dk ? 1.f / p.scale : 1.f;
@@ -746,14 +758,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // columns each), TMEM lane = key row
       if (!mbar_wait_warp(&sm.dkv_full, items_done & 1, wc, hdr)) break;
       tc_fence_after();
-      {
+      if (epi_cols) {
         const int64_t key = (int64_t)it.ktile * 128 + r;
         const bool is_dk = cg >= 2;
         const uint32_t col = (is_dk ? 384u : 256u) + (cg & 1) * 64;
         const float scale = is_dk ? p.scale : 1.f;
         // whole-stream accumulators of a batched call: global key rows
         const int64_t key_row = MULTI ? (int64_t)blks.b[it.blk].kv_start + key : key;
-        const int64_t off = (key_row * p.Hkv + it.g) * HD + (cg & 1) * 64;
+        const int64_t off = (key_row * p.Hkv + it.g) * D + (cg & 1) * 64;
         const int64_t keys_here = MULTI ? (int64_t)blks.b[it.blk].kv_len : n_keys;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -813,19 +825,20 @@ static_assert(sizeof(SmemQ) <= kSmemLimit, "dQ tile set exceeds shared memory");
 
 // dP = dOut V^T for tile jc (any stream): dP region free once the softmax
 // has read the previous dP.
+template <int D>
 __device__ __forceinline__ bool issue_dp(SmemQ& sm, uint32_t tmem, uint32_t jc,
                                          WaitCtl* wc, WsHeader* hdr) {
   const uint32_t vst = jc % V_NS, vuse = jc / V_NS;
   if (!mbar_wait(&sm.v_full[vst], vuse & 1, wc, hdr)) return false;
   if (jc >= 1 && !mbar_wait(&sm.dp_free, (jc - 1) & 1, wc, hdr)) return false;
   tc_fence_after();
-  mma_kk(tmem + 256, smem_u32(sm.dout), smem_u32(sm.v[vst]), false);
+  mma_kk<D>(tmem + 256, smem_u32(sm.dout), smem_u32(sm.v[vst]), false);
   mma_commit(&sm.dp_full);
   mma_commit(&sm.v_empty[vst]);
   return true;
 }
 
-template <bool MULTI>
+template <bool MULTI, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
@@ -901,6 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t T = p.q_len;
   // a ring block's query tiles that see no key add nothing: not work items
   const int n_items = (p.accumulate ? hdr->n_nonempty : hdr->n_items) * p.Hq;
+  constexpr int kBlocks = D / 64;                        // 64-column blocks of a row
+  constexpr uint32_t kLoad = kBlocks * kBlk;             // one Q, dOut, K or V tile
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -941,15 +956,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.q_full, 2 * kTile);
+        mbar_arrive_expect_tx(&sm.q_full, 2 * kLoad);
         {
           // packed q / dOut: map [q_len, Hq d]; head groups: [P q_len, (Hq/P) d]
           // a batched call's maps span the whole stream (rows = global ids)
           const int hpg = p.Hq / p.q_groups, grp = it.h / hpg;
-          const int qx = (it.h - grp * hpg) * HD,
+          const int qx = (it.h - grp * hpg) * D,
                     qy = (MULTI ? blks.b[it.blk].q_start : 0) + (int)(grp * p.q_len) + it.qtile * 128;
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb) {
+          for (int cb = 0; cb < kBlocks; ++cb) {
             tma_load_2d(sm.q + cb * kBlk, &tm_q, &sm.q_full, qx + cb * 64, qy);
             tma_load_2d(sm.dout + cb * kBlk, &tm_do, &sm.q_full, qx + cb * 64, qy);
           }
@@ -964,10 +979,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.k_full[st], kTile);
+            mbar_arrive_expect_tx(&sm.k_full[st], kLoad);
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.k_full[st], it.g * HD + cb * 64, key0);
+            for (int cb = 0; cb < kBlocks; ++cb)
+              tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.k_full[st], it.g * D + cb * 64, key0);
             ++k_count;
           }
           {
@@ -976,10 +991,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.v_full[st], kTile);
+            mbar_arrive_expect_tx(&sm.v_full[st], kLoad);
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d(sm.v[st] + cb * kBlk, &tm_v, &sm.v_full[st], it.g * HD + cb * 64, key0);
+            for (int cb = 0; cb < kBlocks; ++cb)
+              tma_load_2d(sm.v[st] + cb * kBlk, &tm_v, &sm.v_full[st], it.g * D + cb * 64, key0);
             ++v_count;
           }
         }
@@ -1018,10 +1033,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_kk(tmem + 128 * b, q_s, smem_u32(sm.k[st]), false);        // S = Q K^T
+          mma_kk<D>(tmem + 128 * b, q_s, smem_u32(sm.k[st]), false);     // S = Q K^T
           mma_commit(&sm.s_full[b]);
           mma_commit(&sm.k_empty[st]);
-          if ((jj & 1) == 0 && !issue_dp(sm, tmem, jc, wc, hdr)) { ok = false; break; }
+          if ((jj & 1) == 0 && !issue_dp<D>(sm, tmem, jc, wc, hdr)) { ok = false; break; }
           ++jc;
         }
         if (!ok) break;
@@ -1047,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dP of the next tile when its in-item index is odd: it is due
           // before this tile's dQ (the softmax frees dP mid-tile)
           if (((jj + 1) & 1) == 1 && jj + 1 < it.n_kv &&
-              !issue_dp(sm, tmem, jc + 1, wc, hdr)) {
+              !issue_dp<D>(sm, tmem, jc + 1, wc, hdr)) {
             ok = false;
             break;
           }
@@ -1059,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           // (a ring block adds onto the preloaded running dQ)
-          mma_t_split<64>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]),
+          mma_t_split<64, D>(tmem + 384, tmem + 128 * b, smem_u32(sm.k[st]),
                           jj > 0 || (!MULTI && p.accumulate));                 // dQ += dS K
           mma_commit(&sm.dq_done[b]);
           mma_commit(&sm.k_empty[st]);
@@ -1075,6 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + dQ epilogue
     const int wg = warp >> 2;                             // key columns 64 wg .. 64 wg + 63
+    const bool epi_cols = wg * 64 < D;                    // epilogue: head-dimension columns 64 wg ..
     const int wq = warp & 3;
     const int r = wq * 32 + lane;                          // TMEM lane = query row
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -1111,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nlse2r = __ldg(a.nlse2 + (int64_t)h * a.Tp + vrow);
         deltar = __ldg(a.delta + (int64_t)h * a.Tp + vrow);
       }
-      if (!MULTI && p.accumulate && it.n_kv > 0) {
+      if (!MULTI && p.accumulate && it.n_kv > 0 && epi_cols) {
         // ring block: dQ's TMEM accumulator starts as the running dq / scale
         const float* src = valid ? a.dq_acc + qo_offset(p, row, h) + wg * 64 : nullptr;
         const uint32_t col = tmem + lane_base + 384 + wg * 64;
@@ -1180,12 +1196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          if (!epi_cols) continue;
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + 384 + wg * 64 + c * 32, v);
           tmem_wait_ld();
           if (!valid) continue;
           if (MULTI)                  // other blocks add into the same whole-stream rows
-            red_row32_f32(a.dq_acc + ((it_q_start + row) * p.Hq + h) * HD + wg * 64 + c * 32, v,
+            red_row32_f32(a.dq_acc + ((it_q_start + row) * p.Hq + h) * D + wg * 64 + c * 32, v,
                           p.scale);
           else if (p.accumulate)      // the running value was preloaded
             store_row32_f32(a.dq_acc + qo_offset(p, row, h) + wg * 64 + c * 32, v, p.scale);
@@ -1195,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.epi_done);
         ++items_done;
-      } else if (valid && !p.accumulate) {
+      } else if (valid && !p.accumulate && epi_cols) {
         uint32_t z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0u;
@@ -1231,7 +1248,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCqThreads = 192;
 constexpr int kCqWarpProducer = 4, kCqWarpMma = 5;
 constexpr int CQ_NS = 3;
-constexpr uint32_t kIdescMM = idesc_bf16_f32(128, 128, true, true);   // A, B MN-major
 
 struct __align__(1024) SmemCQ {
   uint8_t ds[CQ_NS][kTile];
@@ -1246,8 +1262,11 @@ struct __align__(1024) SmemCQ {
 };
 static_assert(sizeof(SmemCQ) <= kSmemLimit, "cached-dS tile set exceeds shared memory");
 
+template <int D>
 __global__ void __launch_bounds__(kCqThreads, 1)
     attn_bwd_dq_cached_kernel(const __grid_constant__ CUtensorMap tm_k, const BwdArgs a) {
+  constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);   // A, B MN-major, N = D
+  constexpr int kBlocks = D / 64;                        // 64-column blocks of a K row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const AttnProblem& p = a.p;
   WsHeader* hdr = p.hdr;
@@ -1291,6 +1310,7 @@ __global__ void __launch_bounds__(kCqThreads, 1)
   if (warp == kCqWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t ds_pol = l2_evict_first_policy();   // each cached tile is read once
       uint32_t it_count = 0, loads = 0;
       bool ok = true;
       while (ok) {
@@ -1328,11 +1348,11 @@ __global__ void __launch_bounds__(kCqThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.full[st], 2 * kTile);
-          bulk_load(sm.ds[st], src + (int64_t)jj * kTile, kTile, &sm.full[st]);
+          mbar_arrive_expect_tx(&sm.full[st], kTile + kBlocks * kBlk);
+          bulk_load(sm.ds[st], src + (int64_t)jj * kTile, kTile, &sm.full[st], ds_pol);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.full[st], it.g * HD + cb * 64,
+          for (int cb = 0; cb < kBlocks; ++cb)
+            tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.full[st], it.g * D + cb * 64,
                         (it.j_lo + jj) * 128);
           ++loads;
         }
@@ -1402,14 +1422,14 @@ __global__ void __launch_bounds__(kCqThreads, 1)
         for (int i = 0; i < 32; ++i) z[i] = 0u;
         if (valid)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
+          for (int c = 0; c < D / 32; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
         continue;
       }
       const uint32_t b = items_done & 1;
       if (!mbar_wait_warp(&sm.acc_full[b], (items_done >> 1) & 1, wc, hdr)) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + 128 * b + c * 32, v);
         tmem_wait_ld();
@@ -1460,10 +1480,48 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The three kernels of one head dimension D (dK/dV, dQ, dQ from the cache).
+template <int D>
+cudaError_t launch_kernels_d(const BwdArgs& a, const FwdBlocks* blocks, bool cache,
+                             const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                             const CUtensorMap& mv, cudaStream_t s) {
+  const int grid = persistent_grid();
+  constexpr size_t kv_bytes = smem_bytes<SmemKV>();
+  constexpr size_t q_bytes = smem_bytes<SmemQ>();
+  const FwdBlocks B = blocks ? *blocks : single_block(a.p);
+  auto kv_kern = blocks ? attn_bwd_dkdv_tc_kernel<true, D> : attn_bwd_dkdv_tc_kernel<false, D>;
+  auto q_kern = blocks ? attn_bwd_dq_tc_kernel<true, D> : attn_bwd_dq_tc_kernel<false, D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kv_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(q_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_bytes);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(kv_kern, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq, mdo, mk, mv, a, B);
+  count_launches(1);
+  count_path(true);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(q_kern, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo, mk, mv, a, B);
+  count_launches(1);
+  count_path(true);
+  if (e != cudaSuccess) return e;
+  if (cache) {
+    // exactly one of the two dQ kernels does the work (header flag ds_on)
+    constexpr size_t cq_bytes = smem_bytes<SmemCQ>();
+    auto cq_kern = attn_bwd_dq_cached_kernel<D>;
+    e = cudaFuncSetAttribute(cq_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cq_bytes);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(cq_kern, dim3(grid), dim3(kCqThreads), cq_bytes, s, mk, a);
+    count_launches(1);
+    count_path(true);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
-  return io_dtype == NSP_BF16 && d == HD && Hkv > 0 && Hq % Hkv == 0;
+  return io_dtype == NSP_BF16 && (d == 128 || d == 64) && Hkv > 0 && Hq % Hkv == 0;
 }
 
 cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void* dout,
@@ -1472,14 +1530,14 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
                                const FwdBlocks* blocks) {
   const int64_t T = p.q_len;
   CUtensorMap mq, mdo, mk, mv;
-  const int64_t qc = (int64_t)p.Hq * HD, kc = (int64_t)p.Hkv * HD;
+  const int64_t qc = (int64_t)p.Hq * p.d, kc = (int64_t)p.Hkv * p.d;
   const int64_t qrows = T * p.q_groups, qcols = qc / p.q_groups;   // grouped: [P T, (Hq/P) d]
   if (!make_map(&mq, p.q, qrows, qcols) || !make_map(&mdo, dout, qrows, qcols) ||
       !make_map(&mk, p.k, p.kv_len, kc) || !make_map(&mv, p.v, p.kv_len, kc))
     return cudaErrorNotSupported;
   float* delta = reinterpret_cast<float*>(ws + L.delta);
   float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
-  cudaError_t e = launch_bwd_delta(out, dout, lse, delta, nlse2, T, L.Tp, p.Hq, HD, p.io_dtype,
+  cudaError_t e = launch_bwd_delta(out, dout, lse, delta, nlse2, T, L.Tp, p.Hq, p.d, p.io_dtype,
                                    p.q_groups, p.hdr, s);
   if (e != cudaSuccess) return e;
   BwdArgs a;
@@ -1514,36 +1572,8 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
     while (a.hsplit < G && G % (2 * a.hsplit) == 0 &&
            L.n_ktiles * p.Hkv * a.hsplit < 2 * (int64_t)grid)
       a.hsplit *= 2;
-  constexpr size_t kv_bytes = smem_bytes<SmemKV>();
-  constexpr size_t q_bytes = smem_bytes<SmemQ>();
-  const FwdBlocks B = blocks ? *blocks : single_block(p);
-  auto kv_kern = blocks ? attn_bwd_dkdv_tc_kernel<true> : attn_bwd_dkdv_tc_kernel<false>;
-  auto q_kern = blocks ? attn_bwd_dq_tc_kernel<true> : attn_bwd_dq_tc_kernel<false>;
-  e = cudaFuncSetAttribute(kv_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_bytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(q_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_bytes);
-  if (e != cudaSuccess) return e;
-  e = launch_dependent(kv_kern, dim3(grid), dim3(kKvThreads), kv_bytes, s, mq, mdo, mk, mv, a, B);
-  count_launches(1);
-  count_path(true);
-  if (e != cudaSuccess) return e;
-  e = launch_dependent(q_kern, dim3(grid), dim3(kThreads), q_bytes, s, mq, mdo, mk, mv, a, B);
-  count_launches(1);
-  count_path(true);
-  if (e != cudaSuccess) return e;
-  if (cache) {
-    // exactly one of the two dQ kernels does the work (header flag ds_on)
-    constexpr size_t cq_bytes = smem_bytes<SmemCQ>();
-    e = cudaFuncSetAttribute(attn_bwd_dq_cached_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)cq_bytes);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(attn_bwd_dq_cached_kernel, dim3(grid), dim3(kCqThreads), cq_bytes, s, mk,
-                         a);
-    count_launches(1);
-    count_path(true);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
+  return p.d == 128 ? launch_kernels_d<128>(a, blocks, cache, mq, mdo, mk, mv, s)
+                    : launch_kernels_d<64>(a, blocks, cache, mq, mdo, mk, mv, s);
 }
 
 }  // namespace nsp

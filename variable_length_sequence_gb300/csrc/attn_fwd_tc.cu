@@ -117,24 +117,26 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;      // + alignment slack
 // the head dimension lives in the next 16 KB column block.  The start
 // address field holds address >> 4 and never carries (shared memory <
 // 256 KB), so descriptors are advanced by adding offset >> 4.
+template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_saddr, uint32_t k_saddr) {
   constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false);
   const uint64_t qd = smem_desc_sw128(q_saddr, 16, 1024);
   const uint64_t kd = smem_desc_sw128(k_saddr, 16, 1024);
 #pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kColBlockBytes + (kk & 3) * 32) >> 4;
     mma_ss(d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O (+)= P V: P (bf16) from TMEM, 8 columns per K = 16 keys; V is MN-major
-// (keys are K, the head dimension is N): 16 keys = two 8-row groups
-// (SBO = 1024 B), the two 64-wide halves of N are one column block apart
-// (LBO = 16 KB).
+// (keys are K, the head dimension is N = D): 16 keys = two 8-row groups
+// (SBO = 1024 B), the two 64-wide halves of N (D = 128) are one column block
+// apart (LBO = 16 KB).
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_saddr,
                                          bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(BM, HD, true);
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, D, true);
   const uint64_t vd = smem_desc_sw128(v_saddr, kColBlockBytes, 1024);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
@@ -181,8 +183,10 @@ __device__ __forceinline__ void store_row_chunk<float>(float* dst, const uint32_
 // otherwise the single range and outputs of p.  ACC: ring accumulation in
 // place (float32 out only).  All three are compile-time so the common cases
 // (one range, head pairs, written output) carry none of the others'
-// bookkeeping or registers.
-template <typename TO, bool PAIR, bool MULTI, bool ACC>
+// bookkeeping or registers.  D: the head dimension, 128 or 64 (Q, K, V
+// tiles of 64 columns use the first column block of each tile buffer, and O
+// the first 64 of its TMEM columns).
+template <typename TO, bool PAIR, bool MULTI, bool ACC, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -241,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // query tiles no key of the range reaches are not work items: the softmax
   // warps zero-fill them up front (or, accumulating, leave them alone)
   const int n_items = hdr->n_nonempty * per_tile;
+  constexpr int kBlocks = D / 64;                               // 64-column blocks of a row
+  constexpr uint32_t kLoadBytes = kBlocks * kColBlockBytes;     // one Q, K or V tile
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+        mbar_arrive_expect_tx(&sm.q_full, 2 * kLoadBytes);
         // packed layout: map [q_len, Hq d]; head groups: map [P q_len, (Hq/P) d],
         // head h at column block h % (Hq/P) of rows (h / (Hq/P)) q_len + row;
         // a batched call's maps span the whole stream (rows = global ids)
@@ -303,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row0 = q_row_base + grp * q_len_b + it.qtile * tile_rows +
                            (pair_tiles ? t * BM : 0);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
+          for (int cb = 0; cb < kBlocks; ++cb)
             tma_load_2d(sm.q[t] + cb * kColBlockBytes, &tm_q, &sm.q_full,
-                        (head - grp * hpg) * HD + cb * 64, row0);
+                        (head - grp * hpg) * D + cb * 64, row0);
         }
         ++q_count;
         for (int jj = 0; jj < it.n_kv; ++jj) {
@@ -315,10 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+          mbar_arrive_expect_tx(&sm.k_full[st], kLoadBytes);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.k[st] + cb * kColBlockBytes, &tm_k, &sm.k_full[st], it.g * HD + cb * 64,
+          for (int cb = 0; cb < kBlocks; ++cb)
+            tma_load_2d(sm.k[st] + cb * kColBlockBytes, &tm_k, &sm.k_full[st], it.g * D + cb * 64,
                         key0);
           if (use >= 1 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, wc, hdr)) {
             // the K copy just issued is in flight: drain it before leaving
@@ -326,10 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+          mbar_arrive_expect_tx(&sm.v_full[st], kLoadBytes);
 #pragma unroll
-          for (int cb = 0; cb < 2; ++cb)
-            tma_load_2d(sm.v[st] + cb * kColBlockBytes, &tm_v, &sm.v_full[st], it.g * HD + cb * 64,
+          for (int cb = 0; cb < kBlocks; ++cb)
+            tma_load_2d(sm.v[st] + cb * kColBlockBytes, &tm_v, &sm.v_full[st], it.g * D + cb * 64,
                         key0);
           ++kv_count;
         }
@@ -367,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&sm.k_full[st], use & 1, wc, hdr)) break;
           tc_fence_after();
           const uint32_t ks = smem_u32(sm.k[st]);
-          issue_qk(tmem + col_s(0), q_saddr[0], ks);
+          issue_qk<D>(tmem + col_s(0), q_saddr[0], ks);
           mma_commit(&sm.s_full[0]);
-          issue_qk(tmem + col_s(1), q_saddr[1], ks);
+          issue_qk<D>(tmem + col_s(1), q_saddr[1], ks);
           mma_commit(&sm.s_full[1]);
           mma_commit(&sm.k_empty[st]);
           if (it.n_kv == 1) mma_commit(&sm.q_empty);
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++p_count[t];
             tc_fence_after();
             // a ring accumulation's O starts as the preloaded running output
-            issue_pv(tmem + col_o(t), tmem + col_s(t), vs, jj > 0 || ACC);
+            issue_pv<D>(tmem + col_o(t), tmem + col_s(t), vs, jj > 0 || ACC);
             if (t == 1) mma_commit(&sm.v_empty[st]);
             if (!has_next) {
               mma_commit(&sm.o_full[t]);
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!mbar_wait(&sm.k_full[stn], usen & 1, wc, hdr)) { ok = false; continue; }
               tc_fence_after();
             }
-            issue_qk(tmem + col_s(t), q_saddr[t], smem_u32(sm.k[stn]));
+            issue_qk<D>(tmem + col_s(t), q_saddr[t], smem_u32(sm.k[stn]));
             mma_commit(&sm.s_full[t]);
             if (t == 1) {
               mma_commit(&sm.k_empty[stn]);
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_empty = hdr->n_items - hdr->n_nonempty;
       const int groups = tile_rows / 32;                        // 32-row groups per tile
       const int64_t units = (int64_t)n_empty * p.Hq * groups;
-      constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
+      constexpr int kLanesPerRow = D * (int)sizeof(TO) / 16;    // 32, 16 or 8
       constexpr int kRowsPerPass = 32 / kLanesPerRow;
       const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
       for (int64_t u = (int64_t)blockIdx.x * 8 + warp; u < units; u += (int64_t)gridDim.x * 8) {
@@ -504,11 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (acc_row) la2 = NSP_LSE[(int64_t)h * NSP_BLK(q_len, q_len) + row] * kLog2e;
           const float4* arow = reinterpret_cast<const float4*>(NSP_OUT + qo_offset(p, row, h));
           {
-            // the whole 512-byte row in flight at once (one DRAM round trip;
-            // S's registers are not live yet)
-            uint32_t v[4][32];
+            // the whole row (4 D bytes) in flight at once (one DRAM round
+            // trip; S's registers are not live yet)
+            uint32_t v[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < D / 32; ++c)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float4 x = la2 != -INFINITY ? __ldcg(arow + c * 8 + i)
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[c][4 * i + 3] = __float_as_uint(x.w);
               }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_st32(o_tm + c * 32, v[c]);
+            for (int c = 0; c < D / 32; ++c) tmem_st32(o_tm + c * 32, v[c]);
           }
           tmem_wait_st();              // before a first-tile rescale reads O back
           if (la2 != -INFINITY) {
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * corr + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t orow[32];
             tmem_ld32(o_tm + c * 32, orow);
             tmem_wait_ld();
@@ -623,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) wpr[i] = __shfl_sync(0xffffffffu, wp, 8 * i + (lane >> 2));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t x[32];
             tmem_ld16x256_x4(o_tm + c * 32, x);
             tmem_ld16x256_x4(o_tm + (16u << 16) + c * 32, x + 16);
@@ -641,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t orow[32];
             tmem_ld32(o_tm + c * 32, orow);
             tmem_wait_ld();
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (!ACC) {
         // no key of the range is visible to any row of the tile: zero rows,
         // each written whole by a warp (16-byte lanes, full sectors)
-        constexpr int kLanesPerRow = HD * (int)sizeof(TO) / 16;   // 32 or 16
+        constexpr int kLanesPerRow = D * (int)sizeof(TO) / 16;    // 32, 16 or 8
         constexpr int kRowsPerPass = 32 / kLanesPerRow;
         const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
 #pragma unroll 4
@@ -707,11 +713,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TO, bool PAIR, bool MULTI, bool ACC>
+template <typename TO, bool PAIR, bool MULTI, bool ACC, int D>
 cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, cudaStream_t s,
                          const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdBlocks& B) {
-  auto kern = attn_fwd_tc_kernel<TO, PAIR, MULTI, ACC>;
+  auto kern = attn_fwd_tc_kernel<TO, PAIR, MULTI, ACC, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -725,36 +731,45 @@ cudaError_t launch_typed(const AttnProblem& p, const FwdWsLayout& L, char* ws, c
   return cudaGetLastError();
 }
 
+// Every variant of one head dimension D.
+template <int D>
+cudaError_t launch_d(const AttnProblem& pk, const FwdWsLayout& L, char* ws, cudaStream_t s,
+                     const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                     const FwdBlocks& B, bool batched) {
+  const bool pair = ((pk.Hq / pk.Hkv) & 1) != 0;
+  const bool acc = pk.accumulate != 0;                // (float32 out only)
+  // batched blocks: float32 partials or accumulators
+  auto f32 = [&](auto pair_c, auto multi_c) {
+    constexpr bool P = decltype(pair_c)::value, M = decltype(multi_c)::value;
+    return acc ? launch_typed<float, P, M, true, D>(pk, L, ws, s, mq, mk, mv, B)
+               : launch_typed<float, P, M, false, D>(pk, L, ws, s, mq, mk, mv, B);
+  };
+  using T_ = std::true_type;
+  using F_ = std::false_type;
+  if (batched) return pair ? f32(T_{}, T_{}) : f32(F_{}, T_{});
+  if (pk.out_dtype == NSP_F32) return pair ? f32(T_{}, F_{}) : f32(F_{}, F_{});
+  return pair ? launch_typed<__nv_bfloat16, true, false, false, D>(pk, L, ws, s, mq, mk, mv, B)
+              : launch_typed<__nv_bfloat16, false, false, false, D>(pk, L, ws, s, mq, mk, mv, B);
+}
+
 }  // namespace
 
 cudaError_t launch_attn_fwd_tc(const AttnProblem& p, const FwdWsLayout& L, char* ws,
                                cudaStream_t s, bool* launched, const FwdBlocks* blocks) {
   *launched = false;
-  if (p.io_dtype != NSP_BF16 || p.d != HD) return cudaSuccess;
+  if (p.io_dtype != NSP_BF16 || (p.d != 128 && p.d != 64)) return cudaSuccess;
   if (p.q_len <= 0 || p.kv_len <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.q_len * p.q_groups, (int64_t)(p.Hq / p.q_groups) * HD) ||
-      !make_map(&mk, p.k, p.kv_len, (int64_t)p.Hkv * HD) ||
-      !make_map(&mv, p.v, p.kv_len, (int64_t)p.Hkv * HD))
+  if (!make_map(&mq, p.q, p.q_len * p.q_groups, (int64_t)(p.Hq / p.q_groups) * p.d) ||
+      !make_map(&mk, p.k, p.kv_len, (int64_t)p.Hkv * p.d) ||
+      !make_map(&mv, p.v, p.kv_len, (int64_t)p.Hkv * p.d))
     return cudaSuccess;                       // no tensor-map support: CUDA-core path
   *launched = true;
   AttnProblem pk = p;
   pk.wait_budget = wait_budget_cycles();
   const FwdBlocks B = blocks ? *blocks : single_block(p);
-  const bool pair = ((p.Hq / p.Hkv) & 1) != 0;
-  const bool acc = p.accumulate != 0;                 // (float32 out only)
-  // batched blocks: float32 partials or accumulators
-  auto f32 = [&](auto pair_c, auto multi_c) {
-    constexpr bool P = decltype(pair_c)::value, M = decltype(multi_c)::value;
-    return acc ? launch_typed<float, P, M, true>(pk, L, ws, s, mq, mk, mv, B)
-               : launch_typed<float, P, M, false>(pk, L, ws, s, mq, mk, mv, B);
-  };
-  using T_ = std::true_type;
-  using F_ = std::false_type;
-  if (blocks != nullptr) return pair ? f32(T_{}, T_{}) : f32(F_{}, T_{});
-  if (pk.out_dtype == NSP_F32) return pair ? f32(T_{}, F_{}) : f32(F_{}, F_{});
-  return pair ? launch_typed<__nv_bfloat16, true, false, false>(pk, L, ws, s, mq, mk, mv, B)
-              : launch_typed<__nv_bfloat16, false, false, false>(pk, L, ws, s, mq, mk, mv, B);
+  return p.d == 128 ? launch_d<128>(pk, L, ws, s, mq, mk, mv, B, blocks != nullptr)
+                    : launch_d<64>(pk, L, ws, s, mq, mk, mv, B, blocks != nullptr);
 }
 
 }  // namespace nsp

@@ -47,12 +47,13 @@ struct FwdWsLayout {
 };
 
 // Rows of a scheduled forward query tile: 256 when the tensor-core forward
-// takes the problem (bf16, d = 128) with an odd number of query heads per
+// takes the problem (bf16, d = 128 or 64) with an odd number of query heads per
 // KV head (multi-head attention among them): a work item is then two
 // adjacent 128-row tiles of one head, which read the same K/V tiles; 128
 // otherwise (a work item is one tile and two heads of a KV group).
 inline int32_t fwd_tile_rows(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv) {
-  return (io_dtype == NSP_BF16 && d == 128 && Hkv > 0 && ((Hq / Hkv) & 1)) ? 2 * kTileM : kTileM;
+  return (io_dtype == NSP_BF16 && (d == 128 || d == 64) && Hkv > 0 && ((Hq / Hkv) & 1)) ? 2 * kTileM
+                                                                                  : kTileM;
 }
 
 // One (query range, key range) block of a forward call, and the table of a
