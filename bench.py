@@ -763,6 +763,7 @@ def run_ours(args, world, rank, local):
                                     "GB/s", nb, "bytes", 1 if k == "merge" else 2, traffic_map))
 
     prob_path = prob.path_per_step
+    ds_rec = ds_cache_record(prob)
     e2e = None
     if "bwd" in legs and not args.no_e2e:
         e2e = run_e2e(args, prob, nsp, w, device, stream, world)
@@ -817,7 +818,7 @@ def run_ours(args, world, rank, local):
                        "ring_shards": RING_SHARDS, "permute_groups": PERMUTE_GROUPS,
                        "step": " + ".join(CONFIG_LEGS[cid]),
                        "l2": "flushed (256 MiB write) before every timed step",
-                       "bwd_ds_cache": ds_cache_record(prob),
+                       "bwd_ds_cache": ds_rec,
                        "parallelism": f"replicas x{world}"},
             "useful_flop_per_step": useful,
             "legs": leg_stats,
