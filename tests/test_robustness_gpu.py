@@ -29,10 +29,12 @@ PATTERN = 0x5A
 
 
 def _run_all(nsp, w, dev):
-    """Bit-identical across grids: forward, backward, a ring partial block,
-    the ring accumulation in place, the head-grouped forward, the forward
-    without a workspace and two batched blocks.  Returned last: the ring-block backward's
-    (dq, dk, dv), grid-dependent in the last bits."""
+    """Bit-identical across grids: forward, backward (recomputing and with
+    the dS cache), a ring partial block, the ring accumulation in place, the
+    head-grouped forward, the forward without a workspace, two batched
+    blocks, and the forward and backward at head dimension 64.  Returned
+    last: the ring-block backward's (dq, dk, dv), grid-dependent in the last
+    bits."""
     sc = w.cfg.d ** -0.5
     T, Hq, Hkv = w.T, w.cfg.Hq, w.cfg.Hkv
     out, lse = nsp.attn_fwd(dev["q"], dev["k"], dev["v"], dev["cu"], scale=sc)
@@ -62,10 +64,19 @@ def _run_all(nsp, w, dev):
     nsp.attn_bwd_accumulate(dev["q"][qa:], dev["k"][ka:], dev["v"][ka:], out[qa:], dev["dout"][qa:],
                             lse[:, qa:].contiguous(), dev["cu"], gq, gk, gv, scale=sc,
                             q_start=qa, kv_start=ka)
+    need = nsp.nsp_attn_bwd_ds_cache_size(w.cu_seqlens, Hq)
+    ws_c = nsp.bwd_workspace(T, Hq, Hkv, w.cfg.d, "cuda", ds_cache_bytes=need)
+    cq, ck, cv = nsp.attn_bwd(dev["q"], dev["k"], dev["v"], out, dev["dout"], lse, dev["cu"],
+                              scale=sc, workspace=ws_c)
+    assert nsp.nsp_bwd_ds_cache_used(ws_c)
+    # head dimension 64: the first half of every head's columns as its own problem
+    h64 = {n: dev[n][:, :, :64].contiguous() for n in ("q", "k", "v", "dout")}
+    o64, l64 = nsp.attn_fwd(h64["q"], h64["k"], h64["v"], dev["cu"])
+    g64 = nsp.attn_bwd(h64["q"], h64["k"], h64["v"], o64, h64["dout"], l64, dev["cu"])
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    return ([out, lse, dq, dk, dv, po, pl, acc, lacc, og, lg, on, ln] + [t for b in bl for t in b[4:]],
-            (gq, gk, gv))
+    return ([out, lse, dq, dk, dv, po, pl, acc, lacc, og, lg, on, ln] + [t for b in bl for t in b[4:]]
+            + [cq, ck, cv, o64, l64, *g64], (gq, gk, gv))
 
 
 @pytest.mark.parametrize("lens", [[100, 1, 300, 60, 250, 0, 517], [33] * 40 + [700]],
@@ -161,6 +172,27 @@ def test_outputs_stay_inside_their_buffers(nsp):
     back = g("back", (T, Hq, d), torch.bfloat16)
     nsp.nsp_seq2head_permute(dev["q"], perm, T, Hq, d, 4, False)
     nsp.nsp_seq2head_permute(perm, back, T, Hq, d, 4, True)
+    # the backward with an exactly sized dS cache (the guard follows its last
+    # slot), and the forward and backward at head dimension 64
+    need = nsp.nsp_attn_bwd_ds_cache_size(w.cu_seqlens, Hq)
+    base = (nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, d) + 1023) // 1024 * 1024
+    ws_c = g("ws_c", (base + need,), torch.uint8)
+    cq = g("cq", (T, Hq, d), torch.bfloat16)
+    ck, cv = g("ck", (T, Hkv, d), torch.bfloat16), g("cv", (T, Hkv, d), torch.bfloat16)
+    nsp.nsp_attn_bwd(dev["q"], dev["k"], dev["v"], out, dev["dout"], lse, dev["cu"],
+                     len(w.lengths), T, Hq, Hkv, d, sc, True, cq, ck, cv, ws_c)
+    assert nsp.nsp_bwd_ds_cache_used(ws_c)
+    h64 = {n: dev[n][:, :, :64].contiguous() for n in ("q", "k", "v", "dout")}
+    o64, l64 = g("o64", (T, Hq, 64), torch.bfloat16), g("l64", (Hq, T), torch.float32)
+    ws_f64 = g("ws_f64", (nsp.nsp_attn_fwd_workspace_size(T, T, Hq, Hkv, 64),), torch.uint8)
+    nsp.nsp_attn_fwd(h64["q"], h64["k"], h64["v"], dev["cu"], len(w.lengths), 0, T, 0, T, Hq,
+                     Hkv, 64, 64 ** -0.5, True, o64, l64, ws_f64)
+    q64 = g("q64", (T, Hq, 64), torch.bfloat16)
+    k64, v64 = g("k64", (T, Hkv, 64), torch.bfloat16), g("v64", (T, Hkv, 64), torch.bfloat16)
+    base64 = (nsp.nsp_attn_bwd_workspace_size(T, Hq, Hkv, 64) + 1023) // 1024 * 1024
+    ws_b64 = g("ws_b64", (base64 + need,), torch.uint8)
+    nsp.nsp_attn_bwd(h64["q"], h64["k"], h64["v"], o64, h64["dout"], l64, dev["cu"],
+                     len(w.lengths), T, Hq, Hkv, 64, 64 ** -0.5, True, q64, k64, v64, ws_b64)
     torch.cuda.synchronize()
     bad = [name for name, b in bufs.items() if not _guards_intact(b)]
     assert not bad, f"guard bytes overwritten around: {bad}"
