@@ -405,9 +405,18 @@ class Problem:
                 "dq": torch.zeros((self.T, self.Hq, self.d), dtype=torch.float32, device=dev),
                 "dk": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
                 "dv": torch.zeros((self.T, self.Hkv, self.d), dtype=torch.float32, device=dev),
-                "ranges": ranges,
-                "ws": torch.empty(self.nsp.nsp_attn_bwd_blocks_workspace_size(
-                    self.T, ranges, self.Hq, self.Hkv, self.d), dtype=torch.uint8, device=dev)}
+                "ranges": ranges}
+            # the same dS cache as the whole-stream backward, when it fits
+            nb = self.nsp.nsp_attn_bwd_blocks_workspace_size(self.T, ranges, self.Hq, self.Hkv,
+                                                            self.d)
+            cache = self.nsp.nsp_attn_bwd_blocks_ds_cache_size(self.w.cu_seqlens, ranges,
+                                                              self.Hq) if DS_CACHE else 0
+            if cache > DS_CACHE_MAX:
+                cache = 0
+            self._rb["ds_cache_bytes"] = cache
+            if cache:
+                nb = (nb + 1023) // 1024 * 1024 + cache
+            self._rb["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev)
         rb = self._rb
         for t in (rb["dq"], rb["dk"], rb["dv"]):
             t.zero_()
@@ -927,7 +936,9 @@ def time_extra_legs(prob, stream, flush, K, peaks):
         tf = flop / ms / 1e9
         extra["ring_bwd"] = {"ms": ms, "tflops": tf, "frac_bf16": tf / peaks["bf16_tflops"],
                              "blocks": len(prob.ring_pairs),
-                             "out": "float32 dq, dk, dv accumulated over the blocks"}
+                             "out": "float32 dq, dk, dv accumulated over the blocks",
+                             "ds_cache_bytes": int(prob._rb["ds_cache_bytes"]),
+                             "ds_cache_used": prob.nsp.nsp_bwd_ds_cache_used(prob._rb["ws"])}
     return extra
 
 

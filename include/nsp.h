@@ -279,7 +279,10 @@ int32_t nsp_attn_fwd_blocks(const void* q, const void* k, const void* v,
  * Tensor cores only: bf16 with d = 128 or 64 (float32: NSP_ERR_UNSUPPORTED;
  * use nsp_attn_bwd_accumulate per block).  Every q_start must be a multiple
  * of 4 (NSP_ERR_UNSUPPORTED otherwise).  Workspace: at least
- * nsp_attn_bwd_blocks_workspace_size(T, nranges, ranges, Hq, Hkv, d) bytes.
+ * nsp_attn_bwd_blocks_workspace_size(T, nranges, ranges, Hq, Hkv, d) bytes;
+ * bytes past it (from the next 1024-byte boundary) are a dS cache as for
+ * nsp_attn_bwd, used when it holds every visible tile pair of every block
+ * (nsp_attn_bwd_blocks_ds_cache_size bytes).
  * Other arguments and errors as nsp_attn_bwd_accumulate.
  * ---------------------------------------------------------------------- */
 typedef struct {
@@ -288,6 +291,14 @@ typedef struct {
 
 size_t nsp_attn_bwd_blocks_workspace_size(int64_t T, int32_t nranges, const nsp_range_t* ranges,
                                           int32_t Hq, int32_t Hkv, int32_t d);
+
+/* Bytes of dS cache that let nsp_attn_bwd_blocks compute dq from cached
+ * tiles: Hq x (visible 128 x 128 tile pairs of every block, tiles aligned to
+ * the block's q_start and kv_start) x 32768, from HOST cu_seqlens [ndoc + 1].
+ * 0 for a bad argument. */
+size_t nsp_attn_bwd_blocks_ds_cache_size(const int32_t* cu_seqlens_host, int32_t ndoc,
+                                         int32_t nranges, const nsp_range_t* ranges, int32_t Hq,
+                                         int32_t causal);
 
 int32_t nsp_attn_bwd_blocks(const void* q, const void* k, const void* v, const void* out,
                             const void* dout, const float* lse, const int32_t* cu_seqlens,

@@ -124,7 +124,8 @@ def test_ds_cache_size_matches_enumeration(lib, causal):
     """nsp_attn_bwd_ds_cache_size = Hq x (128-row query tile, 128-key tile)
     pairs holding at least one visible (query, key) pair x 32768 bytes, by
     enumerating the pairs of ragged streams (empty and one-token documents,
-    documents that end inside and on tile edges)."""
+    documents that end inside and on tile edges); the batched form sums the
+    pairs of every block, tiles aligned to the block's own starts."""
     rng = np.random.default_rng(41)
     cases = [[1], [128], [129], [0, 5, 0, 260, 0, 1], [300, 77, 150], [33] * 20,
              [127, 1, 128, 256, 3]]
@@ -144,6 +145,25 @@ def test_ds_cache_size_matches_enumeration(lib, causal):
                     vis &= s[None, :] <= t[:, None]
                 pairs += bool(vis.any())
         assert nsp.nsp_attn_bwd_ds_cache_size(cu, 6, causal) == 6 * pairs * 32768, lens
+    # a table of blocks: every block's tiles aligned to its own q_start and kv_start
+    lens = [300, 77, 1, 150, 400]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    doc = np.repeat(np.arange(len(lens)), lens)
+    ranges = [(0, T, 0, T), (4, 300, 100, 500), (320, 11, 0, 330), (500, 428, 700, 228),
+              (0, 0, 0, 10), (128, 256, 128, 256)]
+    total = 0
+    for qa, ql, ka, kl in ranges:
+        for i0 in range(qa, qa + ql, 128):
+            for j0 in range(ka, ka + kl, 128):
+                t = np.arange(i0, min(qa + ql, i0 + 128))
+                s_ = np.arange(j0, min(ka + kl, j0 + 128))
+                vis = doc[t][:, None] == doc[s_][None, :]
+                if causal:
+                    vis &= s_[None, :] <= t[:, None]
+                total += bool(vis.any())
+    assert nsp.nsp_attn_bwd_blocks_ds_cache_size(cu, ranges, 6, causal) == 6 * total * 32768
+    assert nsp.nsp_attn_bwd_blocks_ds_cache_size(cu, [(0, 10, T - 5, 10)], 6, causal) == 0
     assert nsp.nsp_attn_bwd_ds_cache_size(np.array([0, 5, 3], dtype=np.int32), 4) == 0
     assert nsp.nsp_attn_bwd_ds_cache_size(np.array([1, 5], dtype=np.int32), 4) == 0
     assert nsp.nsp_attn_bwd_ds_cache_size(np.array([0, 5], dtype=np.int32), 0) == 0

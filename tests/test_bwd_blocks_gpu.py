@@ -8,7 +8,9 @@ arithmetic per block; only the order of the float additions differs), against
 the oracle's ring-block backward summed over the blocks, and, for every
 block of a ring (causal and not), against the oracle's whole-stream
 gradients.  Config 2 as a ring of 8 shards in one call is compared with the
-whole-stream backward and the oracle on sampled rows and keys.
+whole-stream backward and the oracle on sampled rows and keys.  With a dS
+cache (every block's dS tiles kept, dQ from them), the batched backward is
+compared with the same call without it and with the oracle.
 """
 import numpy as np
 import pytest
@@ -121,3 +123,73 @@ def test_config2_ring_one_call(nsp):
     kidx = torch.from_numpy(keys).cuda()
     assert rel_l2(f64(dk[kidx, 1]), rk) <= TOL_GRAD
     assert rel_l2(f64(dv[kidx, 1]), rv) <= TOL_GRAD
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_blocks_with_ds_cache(nsp, causal):
+    """The batched backward with a dS cache sized by
+    nsp_attn_bwd_blocks_ds_cache_size: the cache is used, and the gradients
+    match the batched backward without it (1e-5: only the order of the float
+    additions differs) and the oracle's blocks summed."""
+    w = make_custom([600, 129, 300, 1, 500], 8, 2, 128, seed=115)
+    d = to_dev(w)
+    T = w.T
+    out, lse = nsp.attn_fwd(d["q"], d["k"], d["v"], d["cu"], causal=causal)
+    ranges = [(0, 400, 0, 400), (400, 400, 0, 400), (400, 400, 400, 400), (800, 300, 0, 800),
+              (800, 730, 800, 730), (4, 1, 0, 1000), (128, 700, 650, 300), (0, 0, 0, 10),
+              (400, 400, 0, 400)]
+    need = nsp.nsp_attn_bwd_blocks_ds_cache_size(w.cu_seqlens, ranges, 8, causal)
+    assert need > 0
+    base = (nsp.nsp_attn_bwd_blocks_workspace_size(T, ranges, 8, 2, 128) + 1023) // 1024 * 1024
+    res = {}
+    for cache in (0, need):
+        ws = torch.empty(base + cache, dtype=torch.uint8, device="cuda")
+        g = _zeros(w)
+        nsp.attn_bwd_blocks(d["q"], d["k"], d["v"], out, d["dout"], lse, d["cu"], ranges, *g,
+                            causal=causal, workspace=ws)
+        torch.cuda.synchronize()
+        assert nsp.nsp_bwd_ds_cache_used(ws) == (cache > 0)
+        res[cache > 0] = g
+    for name, a, b in zip(("dq", "dk", "dv"), res[True], res[False]):
+        e = rel_l2(f64(a), f64(b))
+        print(f"[blocks cached vs not] {name} rel L2 {e:.2e}")
+        assert e <= 1e-5, name
+    q, k, v, do = oracle_inputs(w)
+    oq, ok, ov = (np.zeros(t.shape) for t in res[True])
+    for qa, ql, ka, kl in ranges:
+        if ql == 0 or kl == 0:
+            continue
+        bq, bk, bv = oracle.attn_bwd_block(q, k, v, do, w.cu_seqlens, 128 ** -0.5, causal,
+                                           (qa, qa + ql), (ka, ka + kl))
+        oq[qa:qa + ql] += bq
+        ok[ka:ka + kl] += bk
+        ov[ka:ka + kl] += bv
+    for name, a, r in zip(("dq", "dk", "dv"), res[True], (oq, ok, ov)):
+        assert rel_l2(f64(a), r) <= TOL_GRAD, name
+
+
+def test_config2_ring_one_call_ds_cache(nsp):
+    """Config 2's 36-block ring in one call with the dS cache: used, and
+    within 1e-5 of the same call without it."""
+    w = workload(2)
+    d = to_dev(w)
+    out, lse = nsp.attn_fwd(d["q"], d["k"], d["v"], d["cu"])
+    bounds = shard_bounds(w.T, 8)
+    ranges = [(qa, qb - qa, ka, kb - ka) for i, (qa, qb) in enumerate(bounds)
+              for ka, kb in bounds[:i + 1]]
+    need = nsp.nsp_attn_bwd_blocks_ds_cache_size(w.cu_seqlens, ranges, w.cfg.Hq)
+    base = (nsp.nsp_attn_bwd_blocks_workspace_size(w.T, ranges, 32, 4, 128) + 1023) // 1024 * 1024
+    res = {}
+    for cache in (0, need):
+        ws = torch.empty(base + cache, dtype=torch.uint8, device="cuda")
+        g = _zeros(w)
+        nsp.attn_bwd_blocks(d["q"], d["k"], d["v"], out, d["dout"], lse, d["cu"], ranges, *g,
+                            workspace=ws)
+        torch.cuda.synchronize()
+        assert nsp.nsp_bwd_ds_cache_used(ws) == (cache > 0)
+        res[cache > 0] = g
+        del ws
+    for name, a, b in zip(("dq", "dk", "dv"), res[True], res[False]):
+        e = rel_l2(f64(a), f64(b))
+        print(f"[C2 ring cached vs not] {name} rel L2 {e:.2e}")
+        assert e <= 1e-5, name

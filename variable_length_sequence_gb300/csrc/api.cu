@@ -364,6 +364,76 @@ bool ranges_ok(int64_t T, int32_t nranges, const nsp_range_t* ranges) {
 
 }  // namespace
 
+// Workspace bytes past the layout, from the next 1024-byte boundary, are the
+// whole-stream tensor-core backward's dS cache.
+static void attach_ds_cache(BwdWsLayout& L, size_t workspace_bytes) {
+  const size_t base = align_up(L.total, 1024);
+  if (workspace_bytes >= base + kDsTileBytes) {
+    L.ds_cache = base;
+    L.ds_cache_bytes = workspace_bytes - base;
+  }
+}
+
+// Visible (128-row query tile, 128-key tile) pairs of the query rows
+// [qs, qs + ql) against the keys [ks, ks + kl), tiles aligned to qs and ks
+// (the backward schedule's rule: query tile [r0, r1] sees the key tiles from
+// its first row's document start to r1 (causal) or to the end of its last
+// row's document, clipped to the key range).  cu validated by the caller.
+static int64_t visible_tile_pairs(const int32_t* cu, int32_t ndoc, int64_t qs, int64_t ql,
+                                  int64_t ks, int64_t kl, int32_t causal) {
+  int64_t pairs = 0;
+  int32_t b0 = 0;
+  for (int64_t r0 = qs; r0 < qs + ql; r0 += kTileM) {
+    const int64_t r1 = (r0 + kTileM < qs + ql ? r0 + kTileM : qs + ql) - 1;
+    while (cu[b0 + 1] <= r0) ++b0;
+    int32_t b1 = b0;
+    while (cu[b1 + 1] <= r1) ++b1;
+    int64_t lo = cu[b0], hi = causal ? r1 + 1 : (int64_t)cu[b1 + 1];
+    lo = lo > ks ? lo : ks;
+    hi = hi < ks + kl ? hi : ks + kl;
+    if (hi > lo) pairs += (hi - 1 - ks) / kBwdSub - (lo - ks) / kBwdSub + 1;
+  }
+  (void)ndoc;
+  return pairs;
+}
+
+static bool cu_host_ok(const int32_t* cu, int32_t ndoc) {
+  if (cu == nullptr || ndoc < 1 || cu[0] != 0) return false;
+  for (int32_t b = 0; b < ndoc; ++b)
+    if (cu[b] > cu[b + 1]) return false;
+  return true;
+}
+
+size_t nsp_attn_bwd_ds_cache_size(const int32_t* cu, int32_t ndoc, int32_t Hq, int32_t causal) {
+  if (!cu_host_ok(cu, ndoc) || Hq < 1) return 0;
+  const int64_t T = cu[ndoc];
+  return (size_t)visible_tile_pairs(cu, ndoc, 0, T, 0, T, causal) * (size_t)Hq * kDsTileBytes;
+}
+
+size_t nsp_attn_bwd_blocks_ds_cache_size(const int32_t* cu, int32_t ndoc, int32_t nranges,
+                                         const nsp_range_t* ranges, int32_t Hq, int32_t causal) {
+  if (!cu_host_ok(cu, ndoc) || Hq < 1) return 0;
+  const int64_t T = cu[ndoc];
+  if (!ranges_ok(T, nranges, ranges)) return 0;
+  int64_t pairs = 0;
+  for (int32_t i = 0; i < nranges; ++i)
+    pairs += visible_tile_pairs(cu, ndoc, ranges[i].q_start, ranges[i].q_len, ranges[i].kv_start,
+                                ranges[i].kv_len, causal);
+  return (size_t)pairs * (size_t)Hq * kDsTileBytes;
+}
+
+int32_t nsp_bwd_ds_cache_used(const void* workspace, int32_t* used, nsp_stream_t stream) {
+  if (!workspace || !used) return NSP_ERR_INVALID;
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(workspace);
+  int32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, &hdr->ds_on, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NSP_ERR_CUDA;
+  *used = v;
+  return NSP_OK;
+}
+
 size_t nsp_attn_bwd_blocks_workspace_size(int64_t T, int32_t nranges, const nsp_range_t* ranges,
                                           int32_t Hq, int32_t Hkv, int32_t d) {
   (void)Hkv; (void)d;
@@ -393,8 +463,9 @@ int32_t nsp_attn_bwd_blocks(const void* q, const void* k, const void* v, const v
   for (const void* x : ptrs)
     if (!aligned16(x)) return NSP_ERR_ALIGN;
   FwdBlocks B = range_table(nranges, ranges);
-  const BwdWsLayout L = bwd_ws_layout_blocks(B, T, Hq);
+  BwdWsLayout L = bwd_ws_layout_blocks(B, T, Hq);
   if (!workspace || workspace_bytes < L.total) return NSP_ERR_WORKSPACE;
+  attach_ds_cache(L, workspace_bytes);
   if (!aligned16(workspace)) return NSP_ERR_ALIGN;
   if (T == 0) return NSP_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -439,49 +510,6 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
       workspace_bytes < bwd_ws_layout(T, T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total)
     return NSP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NSP_ERR_ALIGN;
-  return NSP_OK;
-}
-
-// Workspace bytes past the layout, from the next 1024-byte boundary, are the
-// whole-stream tensor-core backward's dS cache.
-static void attach_ds_cache(BwdWsLayout& L, size_t workspace_bytes) {
-  const size_t base = align_up(L.total, 1024);
-  if (workspace_bytes >= base + kDsTileBytes) {
-    L.ds_cache = base;
-    L.ds_cache_bytes = workspace_bytes - base;
-  }
-}
-
-size_t nsp_attn_bwd_ds_cache_size(const int32_t* cu, int32_t ndoc, int32_t Hq, int32_t causal) {
-  if (cu == nullptr || ndoc < 1 || Hq < 1 || cu[0] != 0) return 0;
-  for (int32_t b = 0; b < ndoc; ++b)
-    if (cu[b] > cu[b + 1]) return 0;
-  // the backward schedule's rule: query tile [r0, r1] sees the key tiles
-  // from its first row's document start to r1 (causal) or to the end of its
-  // last row's document
-  const int64_t T = cu[ndoc];
-  int64_t pairs = 0;
-  int32_t b0 = 0;
-  for (int64_t r0 = 0; r0 < T; r0 += kTileM) {
-    const int64_t r1 = (r0 + kTileM < T ? r0 + kTileM : T) - 1;
-    while (cu[b0 + 1] <= r0) ++b0;
-    int32_t b1 = b0;
-    while (cu[b1 + 1] <= r1) ++b1;
-    const int64_t lo = cu[b0], hi = causal ? r1 + 1 : (int64_t)cu[b1 + 1];
-    if (hi > lo) pairs += (hi - 1) / kBwdSub - lo / kBwdSub + 1;
-  }
-  return (size_t)pairs * (size_t)Hq * kDsTileBytes;
-}
-
-int32_t nsp_bwd_ds_cache_used(const void* workspace, int32_t* used, nsp_stream_t stream) {
-  if (!workspace || !used) return NSP_ERR_INVALID;
-  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(workspace);
-  int32_t v = 0;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&v, &hdr->ds_on, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return NSP_ERR_CUDA;
-  *used = v;
   return NSP_OK;
 }
 

@@ -194,10 +194,10 @@ struct BwdArgs {
   const int* qorder;
   const int2* ktiles;     // per 128-key tile: first/last 128-row query tile
   const int* korder;
-  // dS cache (whole-stream call, header flag ds_on): the dK/dV kernel copies
-  // every dS^T tile it builds to slot h * ds_pairs + qoff[i] + (key tile -
-  // first key tile of query tile i), and the dQ kernel of the cache reads
-  // them instead of recomputing S and dP
+  // dS cache (whole-stream or batched call, header flag ds_on): the dK/dV
+  // kernel copies every dS^T tile it builds to slot h * ds_pairs + qoff[i] +
+  // (key tile - first key tile of scheduled query tile i), and the dQ kernel
+  // of the cache reads them instead of recomputing S and dP
   uint8_t* ds_cache;
   const int64_t* qoff;
 };
@@ -322,8 +322,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   constexpr int kBlocks = D / 64;                        // 64-column blocks of a row
   constexpr uint32_t kLoad = kBlocks * kBlk;             // one Q, dOut, K or V tile
   // the schedule found room for every visible tile pair's dS in the cache
-  const bool ds_on =
-      !MULTI && a.ds_cache != nullptr && *((volatile const int32_t*)&hdr->ds_on) != 0;
+  const bool ds_on = a.ds_cache != nullptr && *((volatile const int32_t*)&hdr->ds_on) != 0;
   const int64_t ds_pairs = ds_on ? *((volatile const int64_t*)&hdr->ds_pairs) : 0;
 
   if (warp >= 16) {
@@ -493,7 +492,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             uint8_t* ds_dst = nullptr;               // this step's dS slot
             if (ds_on) {
               const int hh = n / it.n_q;
-              const int i = it.i_lo + (n - hh * it.n_q);
+              // scheduled query tile (a batched call's tiles follow its blocks)
+              const int i = it.i_lo + (n - hh * it.n_q) + (MULTI ? blks.b[it.blk].tile0 : 0);
               const int2 tr = __ldg(a.qtiles + i);
               const int kofs = it.ktile - tr.x;      // < the tile's listed count (schedules agree)
               if (kofs >= 0 && kofs <= tr.y - tr.x)
@@ -1262,9 +1262,12 @@ struct __align__(1024) SmemCQ {
 };
 static_assert(sizeof(SmemCQ) <= kSmemLimit, "cached-dS tile set exceeds shared memory");
 
-template <int D>
+// MULTI: a batched call; its tiles' dQ contributions are added into the
+// whole-stream float32 accumulator (global rows) with atomics.
+template <bool MULTI, int D>
 __global__ void __launch_bounds__(kCqThreads, 1)
-    attn_bwd_dq_cached_kernel(const __grid_constant__ CUtensorMap tm_k, const BwdArgs a) {
+    attn_bwd_dq_cached_kernel(const __grid_constant__ CUtensorMap tm_k, const BwdArgs a,
+                              const __grid_constant__ FwdBlocks blks) {
   constexpr uint32_t kIdescMM = idesc_bf16_f32(128, D, true, true);   // A, B MN-major, N = D
   constexpr int kBlocks = D / 64;                        // 64-column blocks of a K row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1304,7 +1307,8 @@ __global__ void __launch_bounds__(kCqThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   WaitCtl* const wc = &sm.wait;
   const int G = p.Hq / p.Hkv;
-  const int n_items = hdr->n_items * p.Hq;
+  // (a batched call's query tiles that see no key add nothing: not work items)
+  const int n_items = (MULTI ? hdr->n_nonempty : hdr->n_items) * p.Hq;
   const int64_t ds_pairs = *((volatile const int64_t*)&hdr->ds_pairs);
 
   if (warp == kCqWarpProducer) {
@@ -1317,10 +1321,15 @@ __global__ void __launch_bounds__(kCqThreads, 1)
         const int idx = atomicAdd(&hdr->counter, 1);
         QItem it;
         it.qtile = 0; it.h = 0; it.g = 0; it.j_lo = 0; it.n_kv = -1; it.blk = 0;
+        int qt = 0;                               // scheduled query tile
         if (idx < n_items) {
-          const int qt = a.qorder[idx / p.Hq];
+          qt = a.qorder[idx / p.Hq];
           const int2 tr = a.qtiles[qt];
           it.qtile = qt;
+          if constexpr (MULTI) {
+            it.blk = block_of<false>(blks, qt);
+            it.qtile = qt - blks.b[it.blk].tile0;           // query tile within its block
+          }
           it.h = idx - (idx / p.Hq) * p.Hq;
           it.g = it.h / G;
           it.j_lo = tr.x;
@@ -1339,9 +1348,11 @@ __global__ void __launch_bounds__(kCqThreads, 1)
           if (it.n_kv < 0) break;
           continue;
         }
-        // the item's cached tiles: consecutive slots from qoff[qtile]
+        // the item's cached tiles: consecutive slots from qoff[qt]; a batched
+        // call's maps span the whole stream (key rows = global ids)
         const uint8_t* src =
-            a.ds_cache + ((int64_t)it.h * ds_pairs + a.qoff[it.qtile]) * (int64_t)kTile;
+            a.ds_cache + ((int64_t)it.h * ds_pairs + a.qoff[qt]) * (int64_t)kTile;
+        const int k_base = MULTI ? blks.b[it.blk].kv_start : 0;
         for (int jj = 0; jj < it.n_kv; ++jj) {
           const uint32_t st = loads % CQ_NS, use = loads / CQ_NS;
           if (use >= 1 && !mbar_wait(&sm.empty[st], (use - 1) & 1, wc, hdr)) {
@@ -1353,7 +1364,7 @@ __global__ void __launch_bounds__(kCqThreads, 1)
 #pragma unroll
           for (int cb = 0; cb < kBlocks; ++cb)
             tma_load_2d(sm.k[st] + cb * kBlk, &tm_k, &sm.full[st], it.g * D + cb * 64,
-                        (it.j_lo + jj) * 128);
+                        k_base + (it.j_lo + jj) * 128);
           ++loads;
         }
       }
@@ -1412,10 +1423,11 @@ __global__ void __launch_bounds__(kCqThreads, 1)
       if (lane == 0) mbar_arrive(&sm.item_empty[slot]);
       ++it_count;
       if (it.n_kv < 0) break;
-      const int64_t row = (int64_t)it.qtile * 128 + r;
-      const bool valid = row < T;
+      const int64_t row = (int64_t)it.qtile * 128 + r;   // within the (block's) query range
+      const bool valid = row < (MULTI ? (int64_t)blks.b[it.blk].q_len : T);
       __nv_bfloat16* dst = a.dq + qo_offset(p, row, it.h);
       if (it.n_kv == 0) {
+        if (MULTI) continue;               // (not listed: see n_items)
         // no visible key (not met in a whole stream): zero rows
         uint32_t z[32];
 #pragma unroll
@@ -1433,7 +1445,13 @@ __global__ void __launch_bounds__(kCqThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + 128 * b + c * 32, v);
         tmem_wait_ld();
-        if (valid) store_row32_bf16(dst + c * 32, v, p.scale);
+        if (!valid) continue;
+        if (MULTI)                        // other blocks add into the same whole-stream rows
+          red_row32_f32(a.dq_acc + (((int64_t)blks.b[it.blk].q_start + row) * p.Hq + it.h) * D +
+                            c * 32,
+                        v, p.scale);
+        else
+          store_row32_bf16(dst + c * 32, v, p.scale);
       }
       tc_fence_before();
       __syncwarp();
@@ -1507,10 +1525,10 @@ cudaError_t launch_kernels_d(const BwdArgs& a, const FwdBlocks* blocks, bool cac
   if (cache) {
     // exactly one of the two dQ kernels does the work (header flag ds_on)
     constexpr size_t cq_bytes = smem_bytes<SmemCQ>();
-    auto cq_kern = attn_bwd_dq_cached_kernel<D>;
+    auto cq_kern = blocks ? attn_bwd_dq_cached_kernel<true, D> : attn_bwd_dq_cached_kernel<false, D>;
     e = cudaFuncSetAttribute(cq_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cq_bytes);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(cq_kern, dim3(grid), dim3(kCqThreads), cq_bytes, s, mk, a);
+    e = launch_dependent(cq_kern, dim3(grid), dim3(kCqThreads), cq_bytes, s, mk, a, B);
     count_launches(1);
     count_path(true);
     if (e != cudaSuccess) return e;
@@ -1556,9 +1574,9 @@ cudaError_t launch_attn_bwd_tc(const AttnProblem& p, const void* out, const void
   a.qorder = reinterpret_cast<const int*>(ws + L.qorder);
   a.ktiles = reinterpret_cast<const int2*>(ws + L.ktiles);
   a.korder = reinterpret_cast<const int*>(ws + L.korder);
-  // dS cache: whole-stream calls given workspace past the layout (the
-  // schedule decides whether every visible pair's dS fits)
-  const bool cache = blocks == nullptr && !p.accumulate && L.ds_cache_bytes > 0;
+  // dS cache: whole-stream and batched calls given workspace past the layout
+  // (the schedule decides whether every visible pair's dS fits)
+  const bool cache = (blocks != nullptr || !p.accumulate) && L.ds_cache_bytes > 0;
   a.ds_cache = cache ? reinterpret_cast<uint8_t*>(ws + L.ds_cache) : nullptr;
   a.qoff = reinterpret_cast<const int64_t*>(ws + L.qoff);
   const int grid = persistent_grid();

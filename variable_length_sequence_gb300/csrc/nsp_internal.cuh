@@ -119,8 +119,9 @@ struct BwdWsLayout {
   size_t dq_acc;                   // float [q_len, Hq, d] (CUDA-core path)
   size_t qoff;                     // int64 [n_qtiles]: first dS slot of each query tile
   size_t total;
-  // dS cache (whole-stream tensor-core backward): the workspace bytes past
-  // total, from ds_cache on (0 bytes: dQ recomputes S and dP)
+  // dS cache (tensor-core backward of the whole stream or of a table of
+  // blocks): the workspace bytes past total, from ds_cache on (0 bytes: dQ
+  // recomputes S and dP)
   size_t ds_cache = 0, ds_cache_bytes = 0;
   int64_t Tp, n_qtiles, n_ktiles;
   int64_t n_qhist, n_khist;        // counting-sort buckets of the two schedules
@@ -184,7 +185,7 @@ inline BwdWsLayout bwd_ws_layout_blocks(FwdBlocks& B, int64_t T, int32_t Hq) {
   L.delta = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.nlse2 = off;  off = align_up(off + sizeof(float) * (size_t)Hq * (size_t)L.Tp, 256);
   L.dq_acc = off;
-  L.qoff = off;
+  L.qoff = off;   off = align_up(off + sizeof(int64_t) * (size_t)nq, 256);
   L.total = off;
   return L;
 }

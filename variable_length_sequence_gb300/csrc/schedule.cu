@@ -306,8 +306,9 @@ cudaError_t launch_bwd_schedules(const AttnProblem& p, const BwdWsLayout& L, cha
   a.n_tiles = (int32_t)L.n_qtiles;
   a.n_buckets = (int32_t)L.n_qhist;
   a.hdr = p.hdr; a.second = 0;
-  // the dS cache serves the whole-stream backward only
-  const bool cache = blocks == nullptr && !p.accumulate && L.ds_cache_bytes > 0;
+  // the dS cache serves the whole-stream backward and the batched blocks (not
+  // a single accumulated ring block)
+  const bool cache = (blocks != nullptr || !p.accumulate) && L.ds_cache_bytes > 0;
   a.qoff = cache ? reinterpret_cast<int64_t*>(ws + L.qoff) : nullptr;
   a.ds_cache_bytes = cache ? (int64_t)L.ds_cache_bytes : 0;
   a.Hq = p.Hq;

@@ -71,6 +71,7 @@ _SIGNATURES = {
                                            _vp]),
     "nsp_status_query": (_i32, [_vp, _vp]),
     "nsp_attn_bwd_ds_cache_size": (_sz, [_vp, _i32, _i32, _i32]),
+    "nsp_attn_bwd_blocks_ds_cache_size": (_sz, [_vp, _i32, _i32, _vp, _i32, _i32]),
     "nsp_bwd_ds_cache_used": (_i32, [_vp, C.POINTER(C.c_int32), _vp]),
     "nsp_attn_pairs": (_i32, [_vp, _i32, _i32, C.POINTER(C.c_double)]),
     "nsp_attn_cost": (_i32, [_vp, _i32, _i64, _i64, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
@@ -381,6 +382,15 @@ def nsp_attn_bwd_ds_cache_size(cu_seqlens_host, Hq, causal=True) -> int:
                                                  int(bool(causal))))
 
 
+def nsp_attn_bwd_blocks_ds_cache_size(cu_seqlens_host, ranges, Hq, causal=True) -> int:
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_host, dtype=np.int32))
+    arr = _range_array(ranges)
+    return int(load().nsp_attn_bwd_blocks_ds_cache_size(cu.ctypes.data, len(cu) - 1, len(ranges),
+                                                        C.cast(arr, C.c_void_p), int(Hq),
+                                                        int(bool(causal))))
+
+
 def nsp_bwd_ds_cache_used(workspace, stream=None) -> bool:
     used = C.c_int32(0)
     _check("nsp_bwd_ds_cache_used",
@@ -514,16 +524,19 @@ def attn_fwd_blocks(q, k, v, cu_seqlens, blocks, scale=None, causal=True, accumu
 
 
 def attn_bwd_blocks(q, k, v, out, dout, lse, cu_seqlens, ranges, dq_acc, dk_acc, dv_acc,
-                    scale=None, causal=True, workspace=None, stream=None):
+                    scale=None, causal=True, workspace=None, stream=None, ds_cache_bytes=0):
     """Add the backward contributions of blocks [(q_start, q_len, kv_start,
     kv_len), ...] of the whole stream into float32 dq_acc [T, Hq, d] and
-    dk_acc / dv_acc [T, Hkv, d] (lse [Hq, T], the rows' final lse)."""
+    dk_acc / dv_acc [T, Hkv, d] (lse [Hq, T], the rows' final lse).  A new
+    workspace gets ds_cache_bytes of dS cache appended."""
     T, Hq, d = q.shape
     Hkv = k.shape[1]
     scale = d ** -0.5 if scale is None else scale
     if workspace is None:
-        workspace = torch.empty(nsp_attn_bwd_blocks_workspace_size(T, ranges, Hq, Hkv, d),
-                                dtype=torch.uint8, device=q.device)
+        n = nsp_attn_bwd_blocks_workspace_size(T, ranges, Hq, Hkv, d)
+        if ds_cache_bytes > 0:
+            n = (n + 1023) // 1024 * 1024 + int(ds_cache_bytes)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
     nsp_attn_bwd_blocks(q, k, v, out, dout, lse, cu_seqlens, cu_seqlens.numel() - 1, T, ranges,
                         Hq, Hkv, d, scale, causal, dq_acc, dk_acc, dv_acc, workspace, stream)
 
