@@ -1,5 +1,6 @@
 // Varlen attention backward on the tcgen05 tensor cores, bf16 inputs,
-// float32 accumulation, d = 128: two persistent kernels, no atomics.
+// float32 accumulation, head dimension D = 128 or 64: persistent kernels,
+// no atomics on the whole-stream path.
 //
 // Gradients of L = sum(dOut * out) for document-masked attention (BASP
 // Sec. II-A, HSAP Sec. 2.1), recomputing the probabilities from the saved
@@ -40,14 +41,23 @@
 // are read until dQ of their tile is done), V tiles two.  dQ is scaled and
 // written once per item, in bf16.
 //
-// Roles: warps 0-3 and 4-7 are the softmax / epilogue warpgroups (one TMEM
-// lane each; they split the 128 columns of each tile in halves), warp 8 is
-// the TMA producer and work fetcher, warp 9 allocates TMEM and one of its
-// threads issues stream 1, one thread of warp 10 issues stream 2.  The dK/dV
-// kernel adds an idle warp 11 so that its control warpgroup can hand
-// registers to the softmax warpgroups (setmaxnreg).  Masking is one unsigned compare per element against the row's
-// (or key's) visible interval, skipped for fully visible chunks.  All waits
-// are bounded.
+// dS cache (workspace past the layout, when every visible tile pair's dS
+// fits): the dK/dV kernel also bulk-copies each dS^T tile it builds to the
+// cache, and a third kernel computes dQ += dS K from the cached tiles (one
+// product per tile pair instead of the dQ kernel's three); the dQ kernel
+// then returns at once.
+//
+// Roles, dQ kernel: warps 0-3 and 4-7 are the softmax / epilogue
+// warpgroups (one TMEM lane each; they split the 128 columns of each tile in
+// halves), warp 8 is the TMA producer and work fetcher, warp 9 allocates
+// TMEM and one of its threads issues stream 1, one thread of warp 10 issues
+// stream 2.  dK/dV kernel: 16 softmax / epilogue warps (four column groups
+// of four lane quadrants), warp 16 the producer, warp 17 TMEM and stream 1,
+// warp 18 stream 2 (and the dS cache copies), warp 19 idle so that the
+// control warpgroup can hand registers to the softmax warps (setmaxnreg).
+// Masking is one unsigned compare per element against the row's (or key's)
+// visible interval, skipped for fully visible chunks.  All waits are
+// bounded.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"

@@ -1,5 +1,6 @@
 // Varlen attention forward on the 5th-generation tensor cores (tcgen05,
-// TMEM accumulators, TMA loads), bf16 inputs, float32 accumulation, d = 128.
+// TMEM accumulators, TMA loads), bf16 inputs, float32 accumulation, head
+// dimension 128 or 64.
 //
 // What it computes is the definition of the CUDA-core path (scaled
 // dot-product attention inside each packed document, BASP Sec. II-A, HSAP

@@ -236,8 +236,8 @@ FwdBlocks single_block(const AttnProblem& p);
 cudaError_t launch_attn_bwd_simt(const AttnProblem& p, const void* out, const void* dout,
                                  const float* lse, void* dq, void* dk, void* dv,
                                  const BwdWsLayout& L, char* ws, cudaStream_t s);
-// True when the tensor-core backward takes this problem (bf16, d = 128,
-// an even number of query heads per KV head).
+// True when the tensor-core backward takes this problem (bf16, d = 128 or
+// 64, Hq a multiple of Hkv).
 bool bwd_tc_eligible(int32_t io_dtype, int32_t d, int32_t Hq, int32_t Hkv);
 // With `blocks`: every block's contributions added into whole-stream float32
 // dq / dk / dv (global rows) with atomics; p covers the whole stream.
