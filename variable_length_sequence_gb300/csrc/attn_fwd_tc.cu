@@ -112,10 +112,10 @@ struct __align__(1024) Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;      // + alignment slack
 
-// S = Q K^T: 8 MMAs of K = 16 over the head dimension.  Both operands are
-// K-major with 128-byte swizzle; stepping K by 16 elements moves the start
-// address by 32 bytes inside a swizzle span, and the second 64-wide half of
-// the head dimension lives in the next 16 KB column block.  The start
+// S = Q K^T: D / 16 MMAs of K = 16 over the head dimension D.  Both operands
+// are K-major with 128-byte swizzle; stepping K by 16 elements moves the
+// start address by 32 bytes inside a swizzle span, and the second 64-wide
+// half of the head dimension (D = 128) lives in the next 16 KB column block.  The start
 // address field holds address >> 4 and never carries (shared memory <
 // 256 KB), so descriptors are advanced by adding offset >> 4.
 template <int D>
