@@ -24,7 +24,9 @@
  *   synchronises the stream (except nsp_status_query) and enqueues all work
  *   on `stream`.  Calls on different streams with different workspaces may
  *   run concurrently.
- * Alignment: every device pointer must be 16-byte aligned.
+ * Alignment: every device pointer must be 16-byte aligned; the bf16 outputs
+ * of attention (out of a forward, dq / dk / dv of a backward) must be
+ * 32-byte aligned (they are written as 32-byte vectors).
  * Errors: scalar, alignment and size errors are detected on the host and
  *   returned before anything is enqueued.  Errors in device data (a bad
  *   cu_seqlens) are detected by the first kernel, recorded in the status word
@@ -65,7 +67,7 @@ typedef enum {
   NSP_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
   NSP_ERR_CUDA = 4,         /* a CUDA call or launch failed                   */
   NSP_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired             */
-  NSP_ERR_ALIGN = 6         /* a pointer is not 16-byte aligned               */
+  NSP_ERR_ALIGN = 6         /* a pointer is not 16 (bf16 outputs: 32)-byte aligned */
 } nsp_status;
 
 typedef enum { NSP_F32 = 0, NSP_BF16 = 1 } nsp_dtype;

@@ -64,6 +64,8 @@ def call_fwd_validate(lib, a):
     ({"q_len": -1}, nsp.NSP_ERR_INVALID),
     ({"q": A + 8}, nsp.NSP_ERR_ALIGN),
     ({"cu": A + 4}, nsp.NSP_ERR_ALIGN),
+    ({"out": A + 16384 + 16}, nsp.NSP_ERR_ALIGN),       # bf16 out: 32-byte vectors
+    ({"out": A + 16384 + 16, "out_dtype": nsp.NSP_F32}, nsp.NSP_OK),
     ({"q": 0}, nsp.NSP_ERR_INVALID),
     ({"ws": 0}, nsp.NSP_ERR_WORKSPACE),
     ({"ws_bytes": 100}, nsp.NSP_ERR_WORKSPACE),
@@ -88,6 +90,13 @@ def test_bwd_validation(lib):
     bad[5] = A + 4                                 # lse misaligned
     assert lib.nsp_attn_bwd_validate(*bad[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
                                      *bad[7:10], A + (1 << 16), ws) == nsp.NSP_ERR_ALIGN
+    for i in (7, 8, 9):                            # bf16 dq / dk / dv: 32-byte vectors
+        bad = list(ptrs)
+        bad[i] += 16
+        assert lib.nsp_attn_bwd_validate(*bad[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_BF16,
+                                         *bad[7:10], A + (1 << 16), ws) == nsp.NSP_ERR_ALIGN
+        assert lib.nsp_attn_bwd_validate(*bad[:7], 5, 1000, 32, 4, 128, 1, nsp.NSP_F32,
+                                         *bad[7:10], A + (1 << 16), ws32) == nsp.NSP_OK
 
 
 def test_merge_and_permute_validation(lib):

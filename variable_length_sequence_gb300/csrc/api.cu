@@ -65,6 +65,9 @@ using namespace nsp;
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// bf16 outputs of the attention kernels are written as 32-byte vectors (a
+// whole sector per lane), so their base must be 32-byte aligned
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 inline bool dtype_ok(int32_t t) { return t == NSP_F32 || t == NSP_BF16; }
 
 constexpr int64_t kMaxTokens = (int64_t)1 << 30;   // keeps tile counts in int32
@@ -133,6 +136,7 @@ int32_t nsp_attn_fwd_validate(const void* q, const void* k, const void* v,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(cu_seqlens))
     return NSP_ERR_ALIGN;
+  if (out_dtype == NSP_BF16 && !aligned32(out)) return NSP_ERR_ALIGN;
   if (!workspace || workspace_bytes < fwd_ws_layout(q_len, kv_len).total)
     return NSP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return NSP_ERR_ALIGN;
@@ -506,6 +510,8 @@ int32_t nsp_attn_bwd_validate(const void* q, const void* k, const void* v, const
   const void* ptrs[] = {q, k, v, out, dout, lse, cu_seqlens, dq, dk, dv};
   for (const void* x : ptrs)
     if (!aligned16(x)) return NSP_ERR_ALIGN;
+  if (io_dtype == NSP_BF16 && (!aligned32(dq) || !aligned32(dk) || !aligned32(dv)))
+    return NSP_ERR_ALIGN;
   if (!workspace ||
       workspace_bytes < bwd_ws_layout(T, T, Hq, d, !bwd_tc_eligible(io_dtype, d, Hq, Hkv)).total)
     return NSP_ERR_WORKSPACE;
