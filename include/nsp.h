@@ -361,7 +361,8 @@ int32_t nsp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
  * whose dq is summed with float atomics in a float32 accumulator that the
  * workspace then also holds (last bits may vary).
  *
- * dS cache (tensor-core path only).  Workspace bytes past
+ * dS cache (tensor-core path only; storing instead of recomputing, the
+ * trade NSP Sec. 2.3 weighs for attention's backward).  Workspace bytes past
  * nsp_attn_bwd_workspace_size (from the next 1024-byte boundary on) are a
  * cache for dS = P (dP - delta), the probabilities' gradient: when it holds
  * every visible (128-row query tile, 128-key tile) pair of every query head
@@ -385,8 +386,8 @@ size_t nsp_attn_bwd_ds_cache_size(const int32_t* cu_seqlens_host, int32_t ndoc, 
 
 /* Whether the last backward on this workspace computed dq from the dS cache:
  * *used = 1 or 0, read from the workspace header (a copy to the host on
- * stream, then a synchronisation of stream).  NSP_ERR_CUDA if the copy
- * fails. */
+ * stream, then a synchronisation of stream).  NSP_ERR_INVALID for a NULL
+ * argument, NSP_ERR_CUDA if the copy fails. */
 int32_t nsp_bwd_ds_cache_used(const void* workspace, int32_t* used, nsp_stream_t stream);
 
 int32_t nsp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
